@@ -1,0 +1,161 @@
+// da_internal.cuh -- definitions shared by the kernels and the C-ABI layer of libdecode_attn.
+//
+// Partition rules (turboquant-rs 0.4.1, src/cache/cuda/attention.rs, fused_attention():
+// PARTITION_SIZE = 512 and num_partitions = ceil(kv_len / 512); attention.rs README, the
+// sentence under the KV Cache Formats table: split-K decode only for contexts of 1024+
+// tokens). With a sliding window the partitions are counted from the first attended token.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "../../include/decode_attn.h"
+
+namespace da {
+
+constexpr int kBlockSize = 16;      // tokens per page (the only page size built)
+constexpr int kMaxPartitions = 8192;
+
+// Everything a kernel needs, passed by value (no pointers into host memory).
+struct Args {
+  const uint16_t* q;          // [B][Hq][D] bf16 bits
+  const void* k_cache;        // layout by format, see decode_attn.h
+  const void* v_cache;
+  const float* k_scales;      // fp8: [1]; cb4: [num_blocks][Hkv][bs]
+  const float* v_scales;
+  const float* codebook;      // cb4: [16]
+  const float* sign;          // cb4: [D]
+  const int32_t* block_tables;  // [B][max_blocks]
+  const int32_t* context_lens;  // [B]
+  float* out;                 // [B][Hq][D]
+  int B, Hq, Hkv, D, bs, num_blocks, max_blocks, max_ctx, fmt;
+  float scale, softcap;
+  int window, psize, thresh;
+  int P;                      // partitions the grid and the workspace are sized for
+  // workspace pieces
+  uint32_t* err;              // device error word (DA_DEVERR_* bits)
+  float* q_rot;               // [B][Hq][D] (cb4)
+  float* part_o;              // [B][Hq][P][D], unnormalised partial outputs
+  float* part_m;              // [B][Hq][P], running max in log2 units
+  float* part_l;              // [B][Hq][P], running sum of 2^(s - m)
+};
+
+// Start of the attended positions of a sequence of length L.
+__host__ __device__ __forceinline__ int attended_start(int L, int window) {
+  return (window > 0 && L > window) ? L - window : 0;
+}
+
+// Partitions of an attended length n: 0 when empty, ceil(n / psize) when split, else 1.
+__host__ __device__ __forceinline__ int num_partitions(int n, int psize, int thresh) {
+  if (n <= 0) return 0;
+  return (psize > 0 && n >= thresh) ? (n + psize - 1) / psize : 1;
+}
+
+struct Range {
+  int start, end;  // [start, end) token positions; start >= end means "no such partition"
+};
+
+// Token range of partition p of a sequence of (already clamped) length L.
+__host__ __device__ __forceinline__ Range partition_range(int L, int p, int window, int psize, int thresh) {
+  const int s = attended_start(L, window);
+  const int n = L - s;
+  const int np = num_partitions(n, psize, thresh);
+  Range r{0, 0};
+  if (p >= np) return r;
+  if (np == 1) return Range{s, L};
+  r.start = s + p * psize;
+  r.end = r.start + psize < L ? r.start + psize : L;
+  return r;
+}
+
+// Largest length a context_lens entry may take.
+__host__ __device__ __forceinline__ int max_valid_len(const Args& a) {
+  const long long cap = (long long)a.max_blocks * a.bs;
+  return cap < a.max_ctx ? (int)cap : a.max_ctx;
+}
+
+// Context length of sequence b, clamped into [0, max_valid_len]; flags bad input.
+__device__ __forceinline__ int load_len(const Args& a, int b, bool report) {
+  int L = __ldg(a.context_lens + b);
+  const int lim = max_valid_len(a);
+  if (L < 0 || L > lim) {
+    if (report) atomicOr(a.err, DA_DEVERR_CONTEXT_LEN);
+    L = L < 0 ? 0 : lim;
+  }
+  return L;
+}
+
+// Physical block of page `page` of sequence b, or -1 (flagged) when out of range.
+__device__ __forceinline__ int load_block(const Args& a, int b, int page) {
+  const int phys = __ldg(a.block_tables + (size_t)b * a.max_blocks + page);
+  if (phys < 0 || phys >= a.num_blocks) {
+    atomicOr(a.err, DA_DEVERR_BLOCK_ID);
+    return -1;
+  }
+  return phys;
+}
+
+__device__ __forceinline__ float bf16_to_f32(uint16_t h) { return __uint_as_float((uint32_t)h << 16); }
+
+// Workspace layout; every piece starts on a 256-byte boundary.
+struct Layout {
+  size_t err, q_rot, part_o, part_m, part_l, total;
+};
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+inline int host_max_partitions(const da_params& p) {
+  int n = p.max_context_len;
+  if (p.window > 0 && n > p.window) n = p.window;
+  const int np = num_partitions(n, p.partition_size, p.split_threshold);
+  return np < 1 ? 1 : np;
+}
+
+inline Layout workspace_layout(const da_params& p) {
+  Layout l{};
+  const size_t BH = (size_t)p.batch * p.num_q_heads;
+  const size_t P = (size_t)host_max_partitions(p);
+  size_t off = 0;
+  l.err = off;
+  off = align256(off + sizeof(uint32_t));
+  l.q_rot = off;
+  off = align256(off + (p.kv_format == DA_KV_CB4 ? BH * p.head_dim * sizeof(float) : 0));
+  l.part_o = off;
+  off = align256(off + BH * P * p.head_dim * sizeof(float));
+  l.part_m = off;
+  off = align256(off + BH * P * sizeof(float));
+  l.part_l = off;
+  off = align256(off + BH * P * sizeof(float));
+  l.total = off;
+  return l;
+}
+
+// Per-device "done once" flags (up to 64 devices).
+struct DeviceFlags {
+  unsigned long long bits = 0;
+};
+
+// Raise a kernel's dynamic shared-memory limit once per device.
+template <typename Kernel>
+cudaError_t ensure_dynamic_smem(Kernel kern, size_t bytes, DeviceFlags& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = 1ull << (dev & 63);
+  if (__atomic_load_n(&done.bits, __ATOMIC_ACQUIRE) & bit) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess) __atomic_fetch_or(&done.bits, bit, __ATOMIC_RELEASE);
+  return e;
+}
+
+// Launchers (one translation unit each). They return cudaGetLastError() of their launch.
+cudaError_t launch_rotate_q(const Args& a, cudaStream_t s);
+cudaError_t launch_partition(const Args& a, cudaStream_t s);
+cudaError_t launch_reduce(const Args& a, cudaStream_t s);
+cudaError_t launch_debug_bounds(const Args& a, int32_t* bounds, cudaStream_t s);
+cudaError_t launch_debug_dequant(const Args& a, const void* cache, const float* scales, const int32_t* ids, int n,
+                                 float* out, cudaStream_t s);
+
+}  // namespace da

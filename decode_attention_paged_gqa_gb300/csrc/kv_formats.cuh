@@ -1,0 +1,83 @@
+// kv_formats.cuh -- in-register dequantisation of the three KV cache formats
+// (attention.rs README, KV Cache Formats table: BF16, FP8 E4M3, 4-bit Walsh-Hadamard
+// codebook). The codebook format is dequantised in its rotated basis only: the value of
+// coordinate d is scale_t * codebook[idx_d] (turboquant-rs 0.4.1, src/cache/cuda/
+// attention.rs: the fused kernel "reads directly from the compressed KV-cache (no full
+// dequantization needed)").
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
+#include "da_internal.cuh"
+
+namespace da {
+
+template <int FMT>
+struct KvFormat;
+
+// bf16: the upper half of a binary32 word, converted exactly.
+template <>
+struct KvFormat<DA_KV_BF16> {
+  static constexpr int kBitsPerElem = 16;
+  // 8 consecutive elements of cache row `row`, starting at column `col` (a multiple of 8).
+  __device__ static __forceinline__ void load8(const void* cache, size_t row, int D, int col, float /*scale*/,
+                                               const float* /*cb*/, float* x) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(cache) + row * D + col));
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      x[2 * i] = __uint_as_float(w[i] << 16);
+      x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+  }
+};
+
+// E4M3 -> f16 is exact (3 mantissa bits, exponents 2^-9 .. 2^8 fit f16); then one fp32
+// multiply by the tensor's dequant scale.
+template <>
+struct KvFormat<DA_KV_FP8_E4M3> {
+  static constexpr int kBitsPerElem = 8;
+  __device__ static __forceinline__ float2 e4m3x2_to_float2(uint32_t two_codes) {
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two_codes & 0xffffu), __NV_E4M3);
+    return __half22float2(*reinterpret_cast<const __half2*>(&h));
+  }
+  __device__ static __forceinline__ void load8(const void* cache, size_t row, int D, int col, float scale,
+                                               const float* /*cb*/, float* x) {
+    const uint2 v = __ldg(reinterpret_cast<const uint2*>(static_cast<const uint8_t*>(cache) + row * D + col));
+    const uint32_t w[2] = {v.x, v.y};
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const float2 a = e4m3x2_to_float2(w[i]);
+      const float2 b = e4m3x2_to_float2(w[i] >> 16);
+      x[4 * i + 0] = scale * a.x;
+      x[4 * i + 1] = scale * a.y;
+      x[4 * i + 2] = scale * b.x;
+      x[4 * i + 3] = scale * b.y;
+    }
+  }
+};
+
+// 4-bit codebook: byte k of a row holds coordinate 2k in its low nibble, 2k+1 in its high
+// nibble; value = scale_t * codebook[idx] (rotated basis).
+template <>
+struct KvFormat<DA_KV_CB4> {
+  static constexpr int kBitsPerElem = 4;
+  __device__ static __forceinline__ void load8(const void* cache, size_t row, int D, int col, float scale,
+                                               const float* cb, float* x) {
+    const uint32_t v = __ldg(reinterpret_cast<const uint32_t*>(static_cast<const uint8_t*>(cache) + row * (D / 2) +
+                                                               col / 2));
+#pragma unroll
+    for (int i = 0; i < 8; ++i) x[i] = scale * cb[(v >> (4 * i)) & 15u];
+  }
+};
+
+// Per-row scale: fp8 has one per tensor, cb4 one per (block, kv head, slot), bf16 none.
+template <int FMT>
+__device__ __forceinline__ float row_scale(const float* scales, size_t row) {
+  if constexpr (FMT == DA_KV_FP8_E4M3) return __ldg(scales);
+  else if constexpr (FMT == DA_KV_CB4) return __ldg(scales + row);
+  else return 1.0f;
+}
+
+}  // namespace da

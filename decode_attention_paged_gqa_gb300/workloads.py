@@ -87,19 +87,22 @@ class PagedLayout:
     num_blocks: int            # physical blocks in the pool
 
 
-def make_layout(spec: WorkloadSpec) -> PagedLayout:
+def make_layout(spec: WorkloadSpec, lens=None) -> PagedLayout:
     """Context lengths and block tables. Sequence b needs ceil(L_b / bs) pages; the pool
     holds at least the sum of those, and one seeded permutation of the pool is dealt out
-    to the sequences in order."""
+    to the sequences in order. `lens` gives explicit context lengths instead of drawing them."""
     g = _gen(_sub_seed(spec.seed, 1))
     B, bs = spec.batch, spec.block_size
-    if spec.ctx_min == spec.ctx_max:
+    if lens is not None:
+        lens = torch.as_tensor(np.asarray(lens), dtype=torch.int64)
+        assert lens.shape == (B,) and int(lens.max(initial=0)) <= spec.ctx_max
+    elif spec.ctx_min == spec.ctx_max:
         lens = torch.full((B,), spec.ctx_min, dtype=torch.int64)
     else:
         lens = torch.randint(spec.ctx_min, spec.ctx_max + 1, (B,), generator=g)
     pages = (lens + bs - 1) // bs
     need = int(pages.sum())
-    pool = max(need, spec.pool_blocks or 0)
+    pool = max(need, spec.pool_blocks or 0, 1)
     perm = torch.randperm(pool, generator=_gen(_sub_seed(spec.seed, 2))).to(torch.int32)
     tables = torch.full((B, spec.max_blocks_per_seq), -1, dtype=torch.int32)
     off = 0

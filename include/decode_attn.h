@@ -1,0 +1,178 @@
+/*
+ * decode_attn.h -- C ABI of libdecode_attn, single-token (decode) grouped-query
+ * attention over a paged KV cache on a GB300 (sm_103a) GPU.
+ *
+ * For every sequence b and query head h (kv head g = h / G, G = Hq / Hkv):
+ *     out[b][h] = softmax_t( cap(scale * q[b][h] . K[b][g][t]) ) . V[b][g][t]
+ * over the attended positions t of sequence b, where K/V rows are gathered through the
+ * sequence's block table and dequantised from the cache format. Long contexts are split
+ * into partitions, each producing a partial output with its running max and sum, and a
+ * float reduce combines them.
+ *   - Operation, formats, split-K + float reduce, features: attention.rs README,
+ *     "KV Cache Formats" table and the sentence under it ("dedicated Split-K decode
+ *     kernels (triggered at 1024+ context length) ... sharing a common float-precision
+ *     reduce kernel"); "Features: Softcapping, sliding window, GQA/MQA, paged block tables".
+ *   - Two-phase structure, partition size 512, ceil(kv_len / 512) partitions, partial
+ *     output/max/sum buffers, f32 output [heads, head_dim], zero output for an empty
+ *     context, codebook + sign_pattern inputs of the codebook format: turboquant-rs 0.4.1,
+ *     src/cache/cuda/attention.rs, fused_attention() and its FFI call.
+ *
+ * Conventions for every entry point:
+ *   - Every pointer argument is a DEVICE pointer unless its comment says "host". The caller
+ *     owns every buffer; the library allocates no device memory and keeps no state
+ *     between calls except what lives in the caller's workspace.
+ *   - Work is enqueued on `stream` (a cudaStream_t passed as void*; NULL = legacy default
+ *     stream) and runs asynchronously. No entry point synchronises, except
+ *     decode_attn_get_device_error, which says so.
+ *   - Return value: DA_OK (0) or a negative DA_ERR_* code. Argument checks happen on the
+ *     host before anything is enqueued: a call that returns DA_ERR_INVALID_ARG,
+ *     DA_ERR_UNSUPPORTED or DA_ERR_WORKSPACE has enqueued nothing.
+ *   - Bad DATA found by a kernel (a block id outside [0, num_blocks), a context length
+ *     outside [0, min(max_context_len, max_blocks_per_seq * block_size)]) does not fault:
+ *     the kernel skips the bad page or clamps the length, sets a bit in the workspace's
+ *     error word, and carries on. The affected outputs are then unspecified.
+ *     decode_attn_get_device_error reports the bits.
+ */
+#ifndef DECODE_ATTN_H_
+#define DECODE_ATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* KV cache formats (attention.rs README, KV Cache Formats table). */
+enum da_kv_format {
+  /* Unquantized bfloat16. Cache layout [num_blocks][Hkv][block_size][D] bf16. */
+  DA_KV_BF16 = 0,
+  /* FP8 E4M3 (OCP "E4M3FN": bias 7, max 448, no infinity) with one fp32 dequant scale
+   * per cache tensor: value = scale * e4m3(code). Layout [num_blocks][Hkv][block_size][D]
+   * bytes; k_scales / v_scales point to ONE float each. */
+  DA_KV_FP8_E4M3 = 1,
+  /* 4-bit codebook on a random-sign Walsh-Hadamard basis ("Turbo4"). Each K or V vector x
+   * is stored as r = H diag(sign) x / sqrt(D) (H: D x D Sylvester Hadamard matrix,
+   * sign: sign_pattern), quantised per coordinate to the nearest of 16 codebook values
+   * after division by ||x||_2. Layout: [num_blocks][Hkv][block_size][D/2] bytes, two
+   * indices per byte, coordinate 2k in the low nibble of byte k; k_scales / v_scales are
+   * [num_blocks][Hkv][block_size] fp32 norms; codebook is [16] fp32. The kernels rotate q
+   * the same way, attend in the rotated basis and un-rotate the output once per head. */
+  DA_KV_CB4 = 2
+};
+
+enum da_status {
+  DA_OK = 0,
+  DA_ERR_INVALID_ARG = -1,  /* a required pointer is NULL, a size is negative or inconsistent */
+  DA_ERR_UNSUPPORTED = -2,  /* valid arguments outside the built set (see da_params) */
+  DA_ERR_WORKSPACE = -3,    /* workspace NULL, misaligned, or smaller than decode_attn_workspace_bytes */
+  DA_ERR_LAUNCH = -4,       /* a kernel launch failed; see cudaGetLastError */
+  DA_ERR_CUDA = -5          /* another CUDA runtime call failed */
+};
+
+/* Bits of the device error word (decode_attn_get_device_error). */
+#define DA_DEVERR_BLOCK_ID 0x1u    /* a block-table entry used by the call was outside [0, num_blocks) */
+#define DA_DEVERR_CONTEXT_LEN 0x2u /* a context length was < 0 or above the limits in the header comment */
+
+typedef struct da_params {
+  int32_t batch;              /* B >= 0 sequences (B == 0: nothing to do) */
+  int32_t num_q_heads;        /* Hq >= 1 */
+  int32_t num_kv_heads;       /* Hkv >= 1, Hq % Hkv == 0; group size G = Hq / Hkv in {1, 2, 4, 8} */
+  int32_t head_dim;           /* D in {128, 256} */
+  int32_t block_size;         /* tokens per page; 16 */
+  int32_t num_blocks;         /* physical pages in the pool (>= 1) */
+  int32_t max_blocks_per_seq; /* row length of block_tables */
+  int32_t max_context_len;    /* upper bound on every context_lens[b]; sizes grid and workspace */
+  int32_t kv_format;          /* enum da_kv_format */
+  float softmax_scale;        /* scale applied to q . k (e.g. 1/sqrt(D)) */
+  float softcap;              /* 0 = off; else s <- softcap * tanh(s / softcap) after scaling */
+  int32_t window;             /* 0 = off; else attend only the last `window` tokens (t >= L - window) */
+  int32_t partition_size;     /* tokens per split-K partition (512); 0 = never split */
+  int32_t split_threshold;    /* split a sequence iff its attended length >= this (1024) */
+  void* workspace;            /* device memory, 256-byte aligned, decode_attn_workspace_bytes() long,
+                                 zeroed once by decode_attn_workspace_init before first use */
+  size_t workspace_bytes;     /* size of `workspace` in bytes */
+} da_params;
+
+/* Bytes of workspace a call with these parameters needs (0 if the parameters are invalid).
+ * The workspace holds the error word, the rotated queries of the codebook format
+ * ([B][Hq][D] f32) and the split-K partials: output [B][Hq][P][D] f32 (unnormalised),
+ * running max and running sum [B][Hq][P] f32, where P is the partition count of a
+ * sequence of length max_context_len (the page's partial buffers, sized for a batch). */
+size_t decode_attn_workspace_bytes(const da_params* p);
+
+/* Zero the workspace (in particular its error word) on `stream`. Call once after
+ * allocating it. Returns DA_OK, DA_ERR_WORKSPACE or DA_ERR_CUDA. */
+int decode_attn_workspace_init(const da_params* p, void* stream);
+
+/* Full decode attention: [codebook format: query rotation] -> partition kernel -> reduce.
+ *   q            [B][Hq][D] bf16, the single query token of each sequence.
+ *   k_cache,
+ *   v_cache      the paged caches, layout by format (enum da_kv_format).
+ *   k_scales,
+ *   v_scales     FP8: one float each; CB4: [num_blocks][Hkv][block_size] f32; BF16: ignored (may be NULL).
+ *   codebook     CB4: [16] f32; else ignored (may be NULL).
+ *   sign_pattern CB4: [D] f32 of +1/-1; else ignored (may be NULL).
+ *   block_tables [B][max_blocks_per_seq] int32: page i of sequence b lives in physical block
+ *                block_tables[b][i]; token t of sequence b is slot t % block_size of page
+ *                t / block_size. Only the pages holding attended tokens are read.
+ *   context_lens [B] int32: L_b, tokens in sequence b. L_b == 0 gives an all-zero output row.
+ *   out          [B][Hq][D] f32, fully written.
+ * Partitioning: with n_b = attended length (min(L_b, window) when window > 0, else L_b), the
+ * sequence is split iff partition_size > 0 and n_b >= split_threshold, into ceil(n_b /
+ * partition_size) partitions counted from the first attended token. */
+int decode_attn_paged(const void* q, const void* k_cache, const void* v_cache, const float* k_scales,
+                      const float* v_scales, const float* codebook, const float* sign_pattern,
+                      const int32_t* block_tables, const int32_t* context_lens, float* out, const da_params* p,
+                      void* stream);
+
+/* The phases of decode_attn_paged, for callers that schedule or time them one by one.
+ * Same arguments and checks as decode_attn_paged; they must run in this order on one stream:
+ *   decode_attn_rotate_q   CB4 only (returns DA_OK and does nothing for the other formats):
+ *                          q_rot = H diag(sign) q / sqrt(D) into the workspace.
+ *   decode_attn_partition  one CTA per (partition, kv head, sequence): partial output, max,
+ *                          sum of each partition into the workspace.
+ *   decode_attn_reduce     combines the partials of each (sequence, head) into out
+ *                          (and un-rotates it for CB4). */
+int decode_attn_rotate_q(const void* q, const void* k_cache, const void* v_cache, const float* k_scales,
+                         const float* v_scales, const float* codebook, const float* sign_pattern,
+                         const int32_t* block_tables, const int32_t* context_lens, float* out, const da_params* p,
+                         void* stream);
+int decode_attn_partition(const void* q, const void* k_cache, const void* v_cache, const float* k_scales,
+                          const float* v_scales, const float* codebook, const float* sign_pattern,
+                          const int32_t* block_tables, const int32_t* context_lens, float* out, const da_params* p,
+                          void* stream);
+int decode_attn_reduce(const void* q, const void* k_cache, const void* v_cache, const float* k_scales,
+                       const float* v_scales, const float* codebook, const float* sign_pattern,
+                       const int32_t* block_tables, const int32_t* context_lens, float* out, const da_params* p,
+                       void* stream);
+
+/* Synchronises `stream`, then reads the workspace's error word into *err_out (host
+ * pointer; DA_DEVERR_* bits, 0 = no bad input seen since the last read) and clears it. */
+int decode_attn_get_device_error(const da_params* p, void* stream, uint32_t* err_out);
+
+/* Static string describing a DA_* status code. */
+const char* decode_attn_strerror(int status);
+
+/* Partition count the grid is sized for: that of a sequence of length max_context_len. */
+int decode_attn_max_partitions(const da_params* p);
+
+/* ---- debug exports: the kernels' own device code, for bit-exact tests ---------------- */
+
+/* bounds [B][P][2] int32 (P = decode_attn_max_partitions): [start, end) of partition p of
+ * sequence b as the partition kernel computes it, or (-1, -1) where p is past the
+ * sequence's last partition. */
+int decode_attn_debug_partition_bounds(const int32_t* context_lens, int32_t* bounds, const da_params* p,
+                                       void* stream);
+
+/* out [n][Hkv][block_size][D] f32: the values the partition kernel computes from the cache
+ * blocks block_ids[0..n) (device int32): BF16 exact; FP8 scale * e4m3(code) with scales[0];
+ * CB4 scale_t * codebook[idx] in the rotated basis. */
+int decode_attn_debug_dequant_blocks(const void* cache, const float* scales, const float* codebook,
+                                     const int32_t* block_ids, int32_t n, float* out, const da_params* p,
+                                     void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DECODE_ATTN_H_ */

@@ -1,0 +1,419 @@
+#!/usr/bin/env python3
+"""Benchmark of single-token paged GQA decode attention on GB300.
+
+Metric: effective KV-read bandwidth, i.e. the algorithmic K/V bytes of the attended tokens
+divided by the device time of one call (and the same time as microseconds per call).
+One step = one pass of the whole hot path over the batch: [codebook format: query
+rotation] -> split-K partition kernel -> float reduce, through the C-ABI library.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Prints ONE JSON line. ``--impl reference`` times the fp64 CPU oracle (the only reference
+this method has here) on bounded samples of the same workload.
+Multi-GPU (torchrun, N > 1): every rank runs an independent replica of the batch (the path
+has no cross-GPU exchange), times are maxed over ranks and value sums all ranks' bytes.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import datetime as _dt
+import glob
+import hashlib
+import io
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode-attention effective KV-read GB/s (% of GB300 HBM peak); µs/call"
+UNIT = "GB/s"
+DEFAULT_WORKLOAD = "llama3_8b_bf16"
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 2 ** 20
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true", help="skip the nvidia-smi clock sampling and its soak")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------------- ranks
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- peaks / clocks
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, burst copy)"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, earlier GB300 measurement)"
+
+
+class ClockSampler:
+    """nvidia-smi samples (every 200 ms) over a window that contains the timed region."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.path = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.dev), "-lms", "200"], stdout=open(self.path, "w"),
+                                         stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def mark_begin(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for r in csv.reader(f):
+                if len(r) < 10:
+                    continue
+                try:
+                    ts = _dt.datetime.strptime(r[0].strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    rows.append((ts, float(r[2]), float(r[3]), float(r[4]), [x.strip() for x in r[5:]]))
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        win = [x for x in rows if self.t0 - 0.25 <= x[0] <= self.t1 + 0.25] or rows
+        if not win:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for x in win for i in range(4) if x[4][1 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(x[1] for x in win), "sm_max_mhz": max(x[2] for x in win),
+                "power_w_max": max(x[3] for x in win), "samples": len(win), "reasons": reasons}
+
+
+# ----------------------------------------------------------------------------- inputs
+def build_inputs(spec):
+    """Seeded inputs on the host (pinned) for the chosen workload. FP8 and codebook caches
+    are written by the library's own GPU encoders from the seeded fp32 source."""
+    import torch
+
+    from decode_attention_paged_gqa_gb300 import workloads as wl
+
+    lay = wl.make_layout(spec)
+    host = {"q": wl.make_query(spec), "bt": torch.from_numpy(lay.block_tables),
+            "lens": torch.from_numpy(lay.context_lens), "k_scales": None, "v_scales": None, "codebook": None,
+            "sign": None}
+    if spec.kv_format == "bf16":
+        host["k"] = wl.kv_bf16(spec, "k", lay.num_blocks)
+        host["v"] = wl.kv_bf16(spec, "v", lay.num_blocks)
+    else:
+        raise SystemExit(f"workload {spec.name}: the {spec.kv_format} cache needs the GPU encoders")
+    return lay, host
+
+
+def source_hash():
+    h = hashlib.sha1()
+    for f in sorted(glob.glob(os.path.join(ROOT, "decode_attention_paged_gqa_gb300", "csrc", "*"))):
+        with open(f, "rb") as fh:
+            h.update(os.path.basename(f).encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if taken on this kernel source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)[kernel]
+    except (OSError, KeyError, ValueError):
+        return None
+    if t.get("source_hash") != source_hash() or t.get("workload") != workload:
+        return None
+    return t.get("dram_bytes_per_launch")
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+def oracle_sample(spec, lay, host, target_s: float, max_seqs=None):
+    """Time the fp64 oracle on the first n sequences (all heads) of the workload, n chosen so
+    the timed sample takes about target_s. Returns (GB/s, seconds, n, threads)."""
+    import numpy as np
+
+    import oracle
+    from decode_attention_paged_gqa_gb300.metrics import algorithmic_kv_bytes
+
+    def u16(t):
+        return t.contiguous().view(__import__("torch").int16).numpy().view(np.uint16)
+
+    q, k, v = u16(host["q"]), u16(host["k"]), u16(host["v"])
+    bt, lens = host["bt"].numpy(), host["lens"].numpy()
+
+    def run(nseq):
+        sel = [(b, h) for b in range(nseq) for h in range(spec.num_q_heads)]
+        t0 = time.perf_counter()
+        _, thr = oracle.decode_attention(q, k, v, bt, lens, kv_format=spec.kv_format, num_kv_heads=spec.num_kv_heads,
+                                         softmax_scale=spec.scale, softcap=spec.softcap, window=spec.window,
+                                         partition_size=spec.partition_size, split_threshold=spec.split_threshold,
+                                         select=sel, return_threads=True)
+        return time.perf_counter() - t0, thr
+
+    t1, _ = run(1)
+    n = max(1, min(spec.batch, int(target_s / max(t1, 1e-3))))
+    if max_seqs:
+        n = min(n, max_seqs)
+    dt, thr = run(n)
+    nbytes = algorithmic_kv_bytes(lens[:n], spec.window, spec.num_kv_heads, spec.kv_format, spec.head_dim)
+    return nbytes / dt / 1e9, dt, n, thr
+
+
+def reference_arm(args, spec, rank, world):
+    if rank != 0:
+        return
+    import oracle
+
+    oracle.build()
+    lay, host = build_inputs(spec)
+    per_step = max(1.0, min(10.0, 150.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_sample(spec, lay, host, per_step / 4, max_seqs=1)
+    vals, secs, nseq, thr = [], 0.0, 0, 0
+    for _ in range(args.steps):
+        gbs, dt, n, thr = oracle_sample(spec, lay, host, per_step)
+        vals.append(gbs)
+        secs += dt
+        nseq = n
+    value = statistics.mean(vals)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * secs / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": spec.name, "sample_sequences_per_step": nseq},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": thr, "kind": "oracle",
+                             "sample": f"first {nseq} of {spec.batch} sequences, all {spec.num_q_heads} heads, "
+                                       f"per step"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def main():
+    args = parse_args()
+    from decode_attention_paged_gqa_gb300 import workloads as wl
+
+    spec = wl.WORKLOADS[args.workload]
+    rank, world, local = dist_setup()
+    if args.impl == "reference":
+        reference_arm(args, spec, rank, world)
+        return
+
+    import numpy as np
+    import torch
+
+    import decode_attention_paged_gqa_gb300 as da
+    from decode_attention_paged_gqa_gb300 import build as lib_build
+    from decode_attention_paged_gqa_gb300.metrics import algorithmic_kv_bytes
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (the product path has no CPU fallback)")
+    lib_build.build()
+    torch.cuda.set_device(local)
+    lay, host = build_inputs(spec)
+    dev = {k: (None if t is None else t.cuda()) for k, t in host.items()}
+    kv_bytes = algorithmic_kv_bytes(lay.context_lens, spec.window, spec.num_kv_heads, spec.kv_format, spec.head_dim)
+    cache_bytes = host["k"].numel() * host["k"].element_size() * 2
+    p = da.make_params(batch=spec.batch, num_q_heads=spec.num_q_heads, num_kv_heads=spec.num_kv_heads,
+                       head_dim=spec.head_dim, num_blocks=lay.num_blocks, max_blocks_per_seq=lay.block_tables.shape[1],
+                       max_context_len=spec.ctx_max, kv_format=spec.kv_format, softmax_scale=spec.scale,
+                       softcap=spec.softcap, window=spec.window, partition_size=spec.partition_size,
+                       split_threshold=spec.split_threshold)
+    ws = torch.empty(da.decode_attn_workspace_bytes(p), dtype=torch.uint8, device="cuda")
+    da.attach_workspace(p, ws)
+    da.decode_attn_workspace_init(p)
+    out = torch.empty((spec.batch, spec.num_q_heads, spec.head_dim), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    call = (dev["q"], dev["k"], dev["v"], dev["k_scales"], dev["v_scales"], dev["codebook"], dev["sign"], dev["bt"],
+            dev["lens"], out, p)
+    kernels_per_step = 3 if spec.kv_format == "cb4" else 2
+
+    def step(ev=None):
+        da.decode_attn_rotate_q(*call, stream=stream)
+        if ev is not None:
+            ev[0].record(stream)
+        da.decode_attn_partition(*call, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        da.decode_attn_reduce(*call, stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if da.decode_attn_get_device_error(p):
+        raise SystemExit("device reported bad input during warm-up")
+
+    clocks = None if args.no_clocks else ClockSampler(local)
+    if clocks:
+        clocks.start()
+        time.sleep(0.6)  # nvidia-smi start-up
+        soak_end = time.time() + 1.0
+        clocks.mark_begin()
+        while time.time() < soak_end:  # untimed load so the clock samples bracket the timed region
+            for _ in range(20):
+                step()
+            torch.cuda.synchronize()
+    K = args.steps
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    t_start.record(stream)
+    for k in range(K):
+        step(evs[k])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = None
+    if clocks:
+        time.sleep(0.3)
+        clocks.mark_end()
+        clk = clocks.stop()
+    step_ms = max_over_ranks(t_start.elapsed_time(t_end) / K, world)
+    part_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    if da.decode_attn_get_device_error(p):
+        raise SystemExit("device reported bad input during the timed steps")
+
+    # end to end through decode_attn_paged with host buffers: every step copies all inputs
+    # from pinned host memory and reads the output back
+    e2e = None
+    if not args.no_e2e:
+        pin = {k: (None if t is None else t.pin_memory()) for k, t in host.items()}
+        out_h = torch.empty(out.shape, dtype=torch.float32).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in pin.values() if t is not None)
+        d2h = out_h.numel() * 4
+
+        def e2e_step():
+            for k2, t in pin.items():
+                if t is not None:
+                    dev[k2].copy_(t, non_blocking=True)
+            da.decode_attn_paged(*call, stream=stream)
+            out_h.copy_(out, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        Ke = max(3, min(K, 20))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        a.record(stream)
+        for _ in range(Ke):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(a.elapsed_time(b) / Ke, world)
+        e2e = {"value": world * kv_bytes / (e2e_ms * 1e-3) / 1e9, "unit": UNIT, "ms_per_step": e2e_ms,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    peak, peak_src = hbm_peak()
+    gbs = world * kv_bytes / (step_ms * 1e-3) / 1e9
+    part_gbs = kv_bytes / (part_ms * 1e-3) / 1e9
+    traffic = recorded_traffic("partition", spec.name)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+
+        oracle.build()
+        cgbs, cdt, cn, cthr = oracle_sample(spec, lay, host, args.cpu_seconds)
+        cpu = {"value": cgbs, "unit": UNIT, "cores": cthr, "kind": "oracle",
+               "sample": f"first {cn} of {spec.batch} sequences, all {spec.num_q_heads} heads ({cdt:.1f} s)"}
+    line = {
+        "metric": METRIC, "value": gbs, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": step_ms, "us_per_call": step_ms * 1000, "pct_of_hbm_peak": 100 * gbs / world / peak,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": spec.kv_format, "data": "synthetic",
+        "config": {"workload": spec.name, "batch": spec.batch, "num_q_heads": spec.num_q_heads,
+                   "num_kv_heads": spec.num_kv_heads, "head_dim": spec.head_dim, "kv_format": spec.kv_format,
+                   "context": [spec.ctx_min, spec.ctx_max], "window": spec.window, "softcap": spec.softcap,
+                   "block_size": spec.block_size, "partition_size": spec.partition_size,
+                   "algorithmic_kv_bytes": kv_bytes, "cache_bytes": cache_bytes,
+                   "l2": "inputs larger than L2 (KV cache %.2f GB vs 129 MB L2), no flush" % (cache_bytes / 1e9)
+                   if cache_bytes > L2_BYTES else "inputs smaller than L2", "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "kernel": "partition", "achieved": part_gbs, "peak": peak, "unit": "GB/s",
+                     "frac": part_gbs / peak, "peak_source": peak_src, "traffic": traffic,
+                     "partition_us": part_ms * 1000, "bytes_per_launch": kv_bytes},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": K * kernels_per_step,
+        "clocks": clk,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -95,7 +95,7 @@ def make_layout(spec: WorkloadSpec, lens=None) -> PagedLayout:
     B, bs = spec.batch, spec.block_size
     if lens is not None:
         lens = torch.as_tensor(np.asarray(lens), dtype=torch.int64)
-        assert lens.shape == (B,) and int(lens.max(initial=0)) <= spec.ctx_max
+        assert lens.shape == (B,) and (B == 0 or int(lens.max()) <= spec.ctx_max)
     elif spec.ctx_min == spec.ctx_max:
         lens = torch.full((B,), spec.ctx_min, dtype=torch.int64)
     else:

@@ -152,7 +152,9 @@ cudaError_t ensure_dynamic_smem(Kernel kern, size_t bytes, DeviceFlags& done) {
 
 // Launchers (one translation unit each). They return cudaGetLastError() of their launch.
 cudaError_t launch_rotate_q(const Args& a, cudaStream_t s);
-cudaError_t launch_partition(const Args& a, cudaStream_t s);
+cudaError_t launch_partition(const Args& a, cudaStream_t s);     // dispatches on the format:
+cudaError_t launch_partition_tc(const Args& a, cudaStream_t s);  //   BF16, FP8: TMA + tensor cores
+cudaError_t launch_partition_simt(const Args& a, cudaStream_t s);  // CB4: CUDA cores
 cudaError_t launch_reduce(const Args& a, cudaStream_t s);
 cudaError_t launch_debug_bounds(const Args& a, int32_t* bounds, cudaStream_t s);
 cudaError_t launch_debug_dequant(const Args& a, const void* cache, const float* scales, const int32_t* ids, int n,

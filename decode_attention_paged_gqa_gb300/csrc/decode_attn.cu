@@ -32,6 +32,7 @@ int check_params(const da_params* p) {
   if (p->block_size != kBlockSize) return DA_ERR_UNSUPPORTED;
   if (p->batch > 65535 || p->num_kv_heads > 65535 || p->num_q_heads > 65535) return DA_ERR_UNSUPPORTED;
   if (host_max_partitions(*p) > kMaxPartitions) return DA_ERR_UNSUPPORTED;
+  if ((long long)p->num_blocks * p->num_kv_heads * p->block_size >= (1ll << 31)) return DA_ERR_UNSUPPORTED;
   return DA_OK;
 }
 
@@ -49,7 +50,7 @@ int check_tensors(const void* q, const void* k, const void* v, const float* ks, 
   if (p->kv_format != DA_KV_BF16 && (!ks || !vs)) return DA_ERR_INVALID_ARG;
   if (p->kv_format == DA_KV_CB4 && (!cb || !sign)) return DA_ERR_INVALID_ARG;
   // vector loads: caches on 16-byte boundaries, q / out / scales on their element size
-  if (!aligned(k, 16) || !aligned(v, 16) || !aligned(q, 2) || !aligned(out, 4) || !aligned(bt, 4) ||
+  if (!aligned(k, 16) || !aligned(v, 16) || !aligned(q, 16) || !aligned(out, 4) || !aligned(bt, 4) ||
       !aligned(lens, 4))
     return DA_ERR_INVALID_ARG;
   return DA_OK;

@@ -1,4 +1,5 @@
-// partition_simt.cu -- split-K partition kernel on the CUDA cores (fp32 throughout).
+// partition_simt.cu -- split-K partition kernel on the CUDA cores (fp32 throughout), used
+// for the 4-bit codebook cache.
 //
 // One CTA per (partition p, kv head g, sequence b). It walks the partition's tokens in
 // tiles of 32: the tile's K and V rows are gathered through the block table, dequantised
@@ -192,13 +193,13 @@ cudaError_t launch_d(const Args& a, cudaStream_t s) {
 
 }  // namespace
 
-cudaError_t launch_partition(const Args& a, cudaStream_t s) {
-  switch (a.fmt) {
-    case DA_KV_BF16: return launch_d<DA_KV_BF16>(a, s);
-    case DA_KV_FP8_E4M3: return launch_d<DA_KV_FP8_E4M3>(a, s);
-    case DA_KV_CB4: return launch_d<DA_KV_CB4>(a, s);
-  }
+cudaError_t launch_partition_simt(const Args& a, cudaStream_t s) {
+  if (a.fmt == DA_KV_CB4) return launch_d<DA_KV_CB4>(a, s);
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_partition(const Args& a, cudaStream_t s) {
+  return a.fmt == DA_KV_CB4 ? launch_partition_simt(a, s) : launch_partition_tc(a, s);
 }
 
 }  // namespace da

@@ -1,0 +1,471 @@
+// partition_tc.cu -- split-K partition kernel for the BF16 and FP8 E4M3 caches:
+// TMA page staging + warp-level tensor-core MMA for the GQA group's tiles.
+//
+// One CTA per (partition p, kv head g, sequence b), four warps. The partition's pages are
+// dealt round-robin to the warps; every warp runs its own pipeline of kStages shared-memory
+// stages, each holding one page (16 tokens) of K and of V for kv head g, loaded by TMA
+// (cp.async.bulk.tensor, 128-byte swizzle) and signalled on an mbarrier. Per page a warp
+// computes, on the tensor cores (mma.m16n8k16, fp32 accumulators):
+//   S^T[16 tokens x 8 cols] = K[16 x D] . Q^T[D x 8]      (the group's query heads as columns)
+//   O^T[D x 8 cols]       += V^T[D x 16]  . P^T[16 x 8]
+// Tokens are the MMA's M dimension, so a group of G = 4 heads uses 4 of the 8 columns for
+// its scores; the other 4 repeat the same heads and carry the low half of a hi/lo split of
+// the probabilities (p = hi + lo, both in the MMA's 16-bit type), which keeps P.V accurate
+// to ~2^-17 relative. The thread that owns a score column also owns that column of O^T, so
+// the online-softmax rescale needs no data exchange. At the end the four warps' (m, l, o)
+// are merged through shared memory and the partition's partial is written (or, for an
+// unsplit sequence, the normalised output directly).
+//
+// (attention.rs README: split-K decode kernels per KV format and m16n8k16 tensor-core MMA
+// with async copies on SM100-class GPUs; turboquant-rs 0.4.1, src/cache/cuda/attention.rs:
+// a partition kernel writing partial output, max and sum.)
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <cudaTypedefs.h>
+
+#include <cfloat>
+#include <cmath>
+#include <mutex>
+
+#include "da_internal.cuh"
+#include "ptx.cuh"
+
+namespace da {
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kThreads = 32 * kWarps;
+constexpr int kPage = 16;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr unsigned kFull = 0xffffffffu;
+
+template <int FMT, int D, int G>
+struct Tc {
+  static constexpr int kElemBytes = FMT == DA_KV_BF16 ? 2 : 1;
+  static constexpr int kSubs = D * kElemBytes / 128;       // 128-byte swizzled column slabs per row
+  static constexpr int kSubBytes = kPage * 128;             // one slab of one page: 2 KB
+  static constexpr int kPageBytes = kSubs * kSubBytes;      // one page of K (or V), one kv head
+  static constexpr int kStageBytes = 2 * kPageBytes;        // K + V
+  static constexpr int kStages = 16384 / kStageBytes > 0 ? 16384 / kStageBytes : 1;  // 64 KB of stages per CTA
+  static constexpr int kNT = G <= 4 ? 1 : 2;                // P.V column tiles (8 columns each)
+  static constexpr int kCols = 8 * kNT;
+  static constexpr int kMT = D / 16;                        // O^T row tiles
+  static constexpr int kKS = D / 16;                        // k-steps of S^T
+  static constexpr int kStageSmem = kWarps * kStages * kStageBytes;
+  static constexpr int kEpiSmem = (kWarps * kCols * D + 2 * kWarps * 8) * 4;
+  static constexpr int kSmem = (kStageSmem > kEpiSmem ? kStageSmem : kEpiSmem) + 1024;
+};
+
+__device__ __forceinline__ uint32_t swz(uint32_t slab, int row, int chunk) {
+  return slab + row * 128 + ((chunk ^ (row & 7)) << 4);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+// p = hi + lo with hi, lo in the MMA's 16-bit type
+template <int FMT>
+__device__ __forceinline__ float hi_part(float p) {
+  return FMT == DA_KV_BF16 ? __bfloat162float(__float2bfloat16_rn(p)) : __half2float(__float2half_rn(p));
+}
+template <int FMT>
+__device__ __forceinline__ uint32_t pack16(float lo, float hi) {
+  return FMT == DA_KV_BF16 ? pack_bf16(lo, hi) : pack_f16(lo, hi);
+}
+// two E4M3 codes (low 16 bits) -> f16x2, exact
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
+  __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two & 0xffffu), __NV_E4M3);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+template <int FMT>
+__device__ __forceinline__ void mma(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  if constexpr (FMT == DA_KV_BF16)
+    ptx::mma_bf16(d, a, b0, b1);
+  else
+    ptx::mma_f16(d, a, b0, b1);
+}
+
+template <int FMT, int D, int G>
+__global__ void __launch_bounds__(kThreads, 2)
+    partition_tc_kernel(const Args a, const __grid_constant__ CUtensorMap kmap,
+                        const __grid_constant__ CUtensorMap vmap) {
+  using T = Tc<FMT, D, G>;
+  const int p = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int gid = lane >> 2, tig = lane & 3;
+  const int L = load_len(a, b, p == 0 && g == 0 && tid == 0);
+  const Range r = partition_range(L, p, a.window, a.psize, a.thresh);
+  if (r.start >= r.end) return;
+  const int np = num_partitions(L - attended_start(L, a.window), a.psize, a.thresh);
+
+  extern __shared__ unsigned char smem_raw[];
+  __shared__ __align__(8) uint64_t bars[kWarps * T::kStages];
+  const uint32_t smem = (ptx::smem_u32(smem_raw) + 1023u) & ~1023u;
+  unsigned char* smem_gen = smem_raw + (smem - ptx::smem_u32(smem_raw));
+  const uint32_t bar0 = ptx::smem_u32(bars) + w * T::kStages * 8;
+  const uint32_t stage0 = smem + w * T::kStages * T::kStageBytes;
+
+  if (lane == 0) {
+    ptx::prefetch_tensor_map(&kmap);
+    ptx::prefetch_tensor_map(&vmap);
+    for (int s = 0; s < T::kStages; ++s) ptx::mbar_init(bar0 + 8 * s, 1);
+    ptx::fence_mbar_init();
+  }
+  __syncwarp();
+
+  // ---- pages of this partition and this warp's share of them
+  const int first_page = r.start / kPage, npages = (r.end - 1) / kPage - first_page + 1;
+  const int nw = npages > w ? (npages - w + kWarps - 1) / kWarps : 0;
+  int bid = -1;  // lane l: physical block of local page 32*chunk + l
+  auto load_bids = [&](int chunk) {
+    const int i = 32 * chunk + lane;
+    bid = i < nw ? load_block(a, b, first_page + w + kWarps * i) : -1;
+  };
+  load_bids(0);
+  uint32_t valid_mask = 0;  // bit s: the page in stage s has a valid block (warp-uniform)
+  auto issue = [&](int k) {  // all lanes; lane 0 issues the copies of local page k
+    if (k > 0 && (k & 31) == 0) load_bids(k >> 5);
+    const int phys = __shfl_sync(kFull, bid, k & 31);
+    const int s = k % T::kStages;
+    valid_mask = phys >= 0 ? (valid_mask | (1u << s)) : (valid_mask & ~(1u << s));
+    if (lane == 0) {
+      const uint32_t bar = bar0 + 8 * s, dst = stage0 + s * T::kStageBytes;
+      if (phys < 0) {
+        ptx::mbar_arrive(bar);  // completes the phase with nothing loaded
+      } else {
+        ptx::fence_proxy_async();
+        ptx::mbar_arrive_expect_tx(bar, T::kStageBytes);
+        const int y = (phys * a.Hkv + g) * kPage;
+#pragma unroll
+        for (int u = 0; u < T::kSubs; ++u) {
+          ptx::tma_load_2d(dst + u * T::kSubBytes, &kmap, u * (128 / T::kElemBytes), y, bar);
+          ptx::tma_load_2d(dst + T::kPageBytes + u * T::kSubBytes, &vmap, u * (128 / T::kElemBytes), y, bar);
+        }
+      }
+    }
+  };
+  for (int k = 0; k < T::kStages && k < nw; ++k) issue(k);
+
+  // ---- query fragments (B operand of S^T): column n holds head n % G of the group
+  const int qhead = g * G + (gid % G);
+  const uint16_t* qrow = a.q + ((size_t)b * a.Hq + qhead) * D;
+  uint32_t qf[T::kKS][2];
+  float score_scale = a.scale * kLog2e;  // applied to the MMA result (log2 domain)
+  if constexpr (FMT == DA_KV_BF16) {
+#pragma unroll
+    for (int ks = 0; ks < T::kKS; ++ks) {
+      qf[ks][0] = *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * tig);
+      qf[ks][1] = *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 8 + 2 * tig);
+    }
+  } else {
+    // f16 operands: scale q by a power of two so that max|q| fits f16 (exact), undo in the score scale
+    float qv[T::kKS][4];
+    float mx = 0.0f;
+#pragma unroll
+    for (int ks = 0; ks < T::kKS; ++ks)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        qv[ks][e] = bf16_to_f32(qrow[16 * ks + 4 * tig + e]);
+        mx = fmaxf(mx, fabsf(qv[ks][e]));
+      }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+    int ex = 0;
+    frexpf(mx, &ex);
+    const int e2 = ex > 14 ? 14 - ex : 0;
+    const float qs = ldexpf(1.0f, e2);
+#pragma unroll
+    for (int ks = 0; ks < T::kKS; ++ks) {
+      qf[ks][0] = pack_f16(qv[ks][0] * qs, qv[ks][1] * qs);
+      qf[ks][1] = pack_f16(qv[ks][2] * qs, qv[ks][3] * qs);
+    }
+    score_scale = a.scale * __ldg(a.k_scales) * ldexpf(1.0f, -e2) * kLog2e;
+  }
+  const float cap = a.softcap;
+  const float cap_pre = cap > 0.0f ? score_scale / (cap * kLog2e) : 0.0f;  // s_nat / cap
+  const float cap_post = cap * kLog2e;
+
+  // ---- running state: column c = 2*tig + j of S^T and of every O^T column tile
+  float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.0f, 0.0f};
+  float o[T::kNT][T::kMT][4];
+#pragma unroll
+  for (int t = 0; t < T::kNT; ++t)
+#pragma unroll
+    for (int mt = 0; mt < T::kMT; ++mt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) o[t][mt][e] = 0.0f;
+  // hi/lo role of this thread's two columns (G <= 4: column c carries part c / G)
+  int part[2];
+#pragma unroll
+  for (int j = 0; j < 2; ++j) part[j] = G <= 4 ? (2 * tig + j) / G : 0;
+
+  const int mi = lane >> 3, ri = lane & 7;  // ldmatrix: matrix index and row of this lane's address
+  int stalled_at = -1;  // local page whose copy never arrived (never expected)
+  for (int i = 0; i < nw; ++i) {
+    const int s = i % T::kStages;
+    if (!ptx::mbar_wait(bar0 + 8 * s, (i / T::kStages) & 1)) {
+      stalled_at = i;
+      break;
+    }
+    if (valid_mask & (1u << s)) {
+      const uint32_t kb = stage0 + s * T::kStageBytes, vb = kb + T::kPageBytes;
+      const int tok0 = (first_page + w + kWarps * i) * kPage;
+      // -- S^T = K . Q^T
+      float sc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      if constexpr (FMT == DA_KV_BF16) {
+#pragma unroll
+        for (int ks = 0; ks < T::kKS; ++ks) {
+          const int row = ri + 8 * (mi & 1), chunk = 2 * ks + (mi >> 1);
+          uint32_t af[4];
+          ptx::ldmatrix_x4(af, swz(kb + (chunk >> 3) * T::kSubBytes, row, chunk & 7));
+          mma<FMT>(sc, af, qf[ks][0], qf[ks][1]);
+        }
+      } else {
+#pragma unroll
+        for (int j2 = 0; j2 < T::kKS / 2; ++j2) {
+          const int row = ri + 8 * (mi & 1), chunk = 2 * j2 + (mi >> 1);
+          uint32_t rr[4];
+          ptx::ldmatrix_x4(rr, swz(kb + (chunk >> 3) * T::kSubBytes, row, chunk & 7));
+          const uint32_t a0[4] = {e4m3x2_to_f16x2(rr[0]), e4m3x2_to_f16x2(rr[1]), e4m3x2_to_f16x2(rr[0] >> 16),
+                                  e4m3x2_to_f16x2(rr[1] >> 16)};
+          mma<FMT>(sc, a0, qf[2 * j2][0], qf[2 * j2][1]);
+          const uint32_t a1[4] = {e4m3x2_to_f16x2(rr[2]), e4m3x2_to_f16x2(rr[3]), e4m3x2_to_f16x2(rr[2] >> 16),
+                                  e4m3x2_to_f16x2(rr[3] >> 16)};
+          mma<FMT>(sc, a1, qf[2 * j2 + 1][0], qf[2 * j2 + 1][1]);
+        }
+      }
+      // -- scale, softcap, mask; sc[0], sc[1]: token gid; sc[2], sc[3]: token gid + 8
+      const bool ok0 = tok0 + gid >= r.start && tok0 + gid < r.end;
+      const bool ok1 = tok0 + gid + 8 >= r.start && tok0 + gid + 8 < r.end;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float x = cap > 0.0f ? cap_post * tanhf(sc[e] * cap_pre) : sc[e] * score_scale;
+        sc[e] = (e < 2 ? ok0 : ok1) ? x : -INFINITY;
+      }
+      // -- online softmax per column
+      float alpha[2], pr[4];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        float mx = fmaxf(sc[j], sc[j + 2]);
+        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 4));
+        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
+        const float mn = fmaxf(m_run[j], mx);
+        const bool none = mn == -INFINITY;
+        alpha[j] = none ? 1.0f : exp2f(m_run[j] - mn);
+        pr[j] = none ? 0.0f : exp2f(sc[j] - mn);
+        pr[j + 2] = none ? 0.0f : exp2f(sc[j + 2] - mn);
+        l_run[j] = l_run[j] * alpha[j] + pr[j] + pr[j + 2];
+        m_run[j] = mn;
+      }
+      if (__any_sync(kFull, alpha[0] != 1.0f || alpha[1] != 1.0f)) {
+#pragma unroll
+        for (int t = 0; t < T::kNT; ++t)
+#pragma unroll
+          for (int mt = 0; mt < T::kMT; ++mt) {
+            o[t][mt][0] *= alpha[0];
+            o[t][mt][1] *= alpha[1];
+            o[t][mt][2] *= alpha[0];
+            o[t][mt][3] *= alpha[1];
+          }
+      }
+      // -- P^T as the B operand: hi/lo parts in C layout, transposed with movmatrix
+      uint32_t pb[T::kNT][2];
+      if constexpr (G <= 4) {
+        float x[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int pt = part[e & 1];
+          const float h = hi_part<FMT>(pr[e]);
+          x[e] = pt == 0 ? h : (pt == 1 ? pr[e] - h : 0.0f);
+        }
+        pb[0][0] = ptx::movmatrix_trans(pack16<FMT>(x[0], x[1]));
+        pb[0][1] = ptx::movmatrix_trans(pack16<FMT>(x[2], x[3]));
+      } else {
+        float hi[4], lo[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          hi[e] = hi_part<FMT>(pr[e]);
+          lo[e] = pr[e] - hi[e];
+        }
+        pb[0][0] = ptx::movmatrix_trans(pack16<FMT>(hi[0], hi[1]));
+        pb[0][1] = ptx::movmatrix_trans(pack16<FMT>(hi[2], hi[3]));
+        pb[T::kNT - 1][0] = ptx::movmatrix_trans(pack16<FMT>(lo[0], lo[1]));
+        pb[T::kNT - 1][1] = ptx::movmatrix_trans(pack16<FMT>(lo[2], lo[3]));
+      }
+      // -- O^T += V^T . P^T
+      if constexpr (FMT == DA_KV_BF16) {
+#pragma unroll
+        for (int mt = 0; mt < T::kMT; ++mt) {
+          const int row = ri + 8 * (mi >> 1), chunk = 2 * mt + (mi & 1);
+          uint32_t af[4];
+          ptx::ldmatrix_x4_trans(af, swz(vb + (chunk >> 3) * T::kSubBytes, row, chunk & 7));
+#pragma unroll
+          for (int t = 0; t < T::kNT; ++t) mma<FMT>(o[t][mt], af, pb[t][0], pb[t][1]);
+        }
+      } else {
+#pragma unroll
+        for (int j2 = 0; j2 < T::kMT / 2; ++j2) {
+          const int row = ri + 8 * (mi >> 1), chunk = 2 * j2 + (mi & 1);
+          uint32_t rr[4];
+          ptx::ldmatrix_x4_trans(rr, swz(vb + (chunk >> 3) * T::kSubBytes, row, chunk & 7));
+          const uint32_t x0 = __byte_perm(rr[0], 0, 0x3120), x1 = __byte_perm(rr[1], 0, 0x3120);
+          const uint32_t x2 = __byte_perm(rr[2], 0, 0x3120), x3 = __byte_perm(rr[3], 0, 0x3120);
+          const uint32_t a0[4] = {e4m3x2_to_f16x2(x0), e4m3x2_to_f16x2(x0 >> 16), e4m3x2_to_f16x2(x2),
+                                  e4m3x2_to_f16x2(x2 >> 16)};
+          const uint32_t a1[4] = {e4m3x2_to_f16x2(x1), e4m3x2_to_f16x2(x1 >> 16), e4m3x2_to_f16x2(x3),
+                                  e4m3x2_to_f16x2(x3 >> 16)};
+#pragma unroll
+          for (int t = 0; t < T::kNT; ++t) {
+            mma<FMT>(o[t][2 * j2], a0, pb[t][0], pb[t][1]);
+            mma<FMT>(o[t][2 * j2 + 1], a1, pb[t][0], pb[t][1]);
+          }
+        }
+      }
+    }
+    __syncwarp();
+    if (i + T::kStages < nw) issue(i + T::kStages);
+  }
+  if (stalled_at >= 0) {
+    if (lane == 0) atomicOr(a.err, DA_DEVERR_TIMEOUT);
+    // give the copies still in flight into this warp's stages a bounded chance to land
+    for (int k = stalled_at; k < nw && k < stalled_at + T::kStages; ++k)
+      ptx::mbar_wait(bar0 + 8 * (k % T::kStages), (k / T::kStages) & 1);
+  }
+
+  // ---- merge the four warps through shared memory (the stage buffers are free now)
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    l_run[j] += __shfl_xor_sync(kFull, l_run[j], 4);
+    l_run[j] += __shfl_xor_sync(kFull, l_run[j], 8);
+    l_run[j] += __shfl_xor_sync(kFull, l_run[j], 16);
+  }
+  __syncthreads();
+  float* ep_o = reinterpret_cast<float*>(smem_gen);  // [kWarps][kCols][D]
+  float* ep_m = ep_o + kWarps * T::kCols * D;          // [kWarps][8]
+  float* ep_l = ep_m + kWarps * 8;                     // [kWarps][8]
+#pragma unroll
+  for (int t = 0; t < T::kNT; ++t)
+#pragma unroll
+    for (int mt = 0; mt < T::kMT; ++mt) {
+      const int d0 = FMT == DA_KV_BF16 ? 16 * mt + gid : 16 * mt + 2 * gid;
+      const int d1 = FMT == DA_KV_BF16 ? d0 + 8 : d0 + 1;
+      float* base = ep_o + (w * T::kCols + 8 * t + 2 * tig) * D;
+      base[d0] = o[t][mt][0];
+      base[D + d0] = o[t][mt][1];
+      base[d1] = o[t][mt][2];
+      base[D + d1] = o[t][mt][3];
+    }
+  if (gid == 0) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      ep_m[w * 8 + 2 * tig + j] = m_run[j];
+      ep_l[w * 8 + 2 * tig + j] = l_run[j];
+    }
+  }
+  __syncthreads();
+  const bool direct = np == 1;
+  const float out_scale = FMT == DA_KV_FP8_E4M3 ? __ldg(a.v_scales) : 1.0f;
+  for (int idx = tid; idx < G * D; idx += kThreads) {
+    const int h = idx / D, d = idx % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int ww = 0; ww < kWarps; ++ww) M = fmaxf(M, ep_m[ww * 8 + h]);
+    float acc = 0.0f, l = 0.0f;
+#pragma unroll
+    for (int ww = 0; ww < kWarps; ++ww) {
+      const float mw = ep_m[ww * 8 + h];
+      const float wt = mw == -INFINITY ? 0.0f : exp2f(mw - M);
+      const float* ow = ep_o + ww * T::kCols * D;
+      acc += wt * (ow[h * D + d] + ow[(h + G) * D + d]);
+      l += wt * ep_l[ww * 8 + h];
+    }
+    const size_t bh = (size_t)b * a.Hq + g * G + h;
+    if (direct) {
+      a.out[bh * D + d] = l > 0.0f ? acc * out_scale / l : 0.0f;
+    } else {
+      const size_t pi = bh * a.P + p;
+      a.part_o[pi * D + d] = acc;
+      if (d == 0) {
+        a.part_m[pi] = M;
+        a.part_l[pi] = l;
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// 2-D view of a paged cache: rows = (block, kv head, slot), columns = the row's D elements;
+// boxes of 16 rows x 128 bytes with the 128-byte swizzle.
+bool encode_cache_map(CUtensorMap* map, const void* base, int elem_bytes, int D, long long rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)D * elem_bytes};
+  const cuuint32_t box[2] = {(cuuint32_t)(128 / elem_bytes), (cuuint32_t)kPage};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+            const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int FMT, int D, int G>
+cudaError_t launch_fixed(const Args& a, cudaStream_t s) {
+  using T = Tc<FMT, D, G>;
+  CUtensorMap km, vm;
+  const long long rows = (long long)a.num_blocks * a.Hkv * kPage;
+  if (!encode_cache_map(&km, a.k_cache, T::kElemBytes, D, rows) ||
+      !encode_cache_map(&vm, a.v_cache, T::kElemBytes, D, rows))
+    return cudaErrorInvalidValue;
+  auto kern = partition_tc_kernel<FMT, D, G>;
+  static DeviceFlags attr;
+  cudaError_t e = ensure_dynamic_smem(kern, T::kSmem, attr);
+  if (e != cudaSuccess) return e;
+  kern<<<dim3(a.P, a.Hkv, a.B), kThreads, T::kSmem, s>>>(a, km, vm);
+  return cudaGetLastError();
+}
+
+template <int FMT, int D>
+cudaError_t launch_g(const Args& a, cudaStream_t s) {
+  switch (a.Hq / a.Hkv) {
+    case 1: return launch_fixed<FMT, D, 1>(a, s);
+    case 2: return launch_fixed<FMT, D, 2>(a, s);
+    case 4: return launch_fixed<FMT, D, 4>(a, s);
+    case 8: return launch_fixed<FMT, D, 8>(a, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t launch_partition_tc(const Args& a, cudaStream_t s) {
+  if (a.fmt == DA_KV_BF16) return a.D == 128 ? launch_g<DA_KV_BF16, 128>(a, s) : launch_g<DA_KV_BF16, 256>(a, s);
+  if (a.fmt == DA_KV_FP8_E4M3)
+    return a.D == 128 ? launch_g<DA_KV_FP8_E4M3, 128>(a, s) : launch_g<DA_KV_FP8_E4M3, 256>(a, s);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace da

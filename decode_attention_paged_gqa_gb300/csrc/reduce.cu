@@ -5,8 +5,10 @@
 //
 // For sequence b, head h with partials (o_p, m_p, l_p), p < P_b (m in log2 units):
 //   M = max_p m_p,  w_p = 2^(m_p - M),  out = sum_p w_p o_p / sum_p w_p l_p.
-// An empty sequence gets an all-zero row. For the codebook format the result is still in
-// the rotated basis and is un-rotated here: out <- diag(sign) H out / sqrt(D).
+// An empty sequence gets an all-zero row. An unsplit BF16/FP8 sequence was written by the
+// partition kernel and is skipped here. For the codebook format the result is still in the
+// rotated basis and is un-rotated here: out <- diag(sign) H out / sqrt(D). For FP8 the
+// per-tensor V scale is applied once, to the result.
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -31,6 +33,7 @@ __global__ void __launch_bounds__(128) reduce_kernel(const Args a) {
     for (int d = tid; d < D; d += blockDim.x) out[d] = 0.0f;
     return;
   }
+  if (np == 1 && !kUnrotate) return;
   const size_t base = ((size_t)b * a.Hq + h) * a.P;
   if (tid < 32) {
     float M = -INFINITY;
@@ -48,7 +51,7 @@ __global__ void __launch_bounds__(128) reduce_kernel(const Args a) {
     if (lane == 0) inv_l_s = lsum > 0.0f ? 1.0f / lsum : 0.0f;
   }
   __syncthreads();
-  const float inv_l = inv_l_s;
+  const float inv_l = inv_l_s * (a.fmt == DA_KV_FP8_E4M3 ? __ldg(a.v_scales) : 1.0f);
   for (int d = tid; d < D; d += blockDim.x) {
     float acc = 0.0f;
     for (int p = 0; p < np; ++p) acc = fmaf(w_s[p], a.part_o[(base + p) * D + d], acc);

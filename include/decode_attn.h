@@ -73,6 +73,7 @@ enum da_status {
 /* Bits of the device error word (decode_attn_get_device_error). */
 #define DA_DEVERR_BLOCK_ID 0x1u    /* a block-table entry used by the call was outside [0, num_blocks) */
 #define DA_DEVERR_CONTEXT_LEN 0x2u /* a context length was < 0 or above the limits in the header comment */
+#define DA_DEVERR_TIMEOUT 0x4u     /* a wait for a page copy gave up after its iteration bound (never expected) */
 
 typedef struct da_params {
   int32_t batch;              /* B >= 0 sequences (B == 0: nothing to do) */
@@ -106,9 +107,10 @@ size_t decode_attn_workspace_bytes(const da_params* p);
 int decode_attn_workspace_init(const da_params* p, void* stream);
 
 /* Full decode attention: [codebook format: query rotation] -> partition kernel -> reduce.
- *   q            [B][Hq][D] bf16, the single query token of each sequence.
+ *   q            [B][Hq][D] bf16, the single query token of each sequence (16-byte aligned).
  *   k_cache,
- *   v_cache      the paged caches, layout by format (enum da_kv_format).
+ *   v_cache      the paged caches, layout by format (enum da_kv_format), 16-byte aligned;
+ *                num_blocks * Hkv * block_size must stay below 2^31.
  *   k_scales,
  *   v_scales     FP8: one float each; CB4: [num_blocks][Hkv][block_size] f32; BF16: ignored (may be NULL).
  *   codebook     CB4: [16] f32; else ignored (may be NULL).

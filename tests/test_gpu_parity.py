@@ -79,3 +79,15 @@ def test_full_size_workloads_sampled(name, n):
     assert_close(got, ref, name)
     # every output row is finite and the empty-context rule never fires here
     assert np.all(np.isfinite(out))
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "fp8"])
+@pytest.mark.parametrize("qscale", [1e-3, 3e2, 1e5])
+def test_query_magnitudes(fmt, qscale):
+    """The FP8 path computes q.k with f16 operands: queries far outside the f16 range must
+    still give the right answer (they are rescaled by a power of two, exactly)."""
+    spec, lay = small_spec(fmt, 128, 4, lens=[1, 600, 1500], seed=11)
+    c = make_case(spec, lay)
+    c["q"] = (c["q"].float() * qscale).to(torch.bfloat16)
+    assert_close(run_gpu(c, softmax_scale=1.0 / (qscale * math.sqrt(128))), run_oracle(
+        c, softmax_scale=1.0 / (qscale * math.sqrt(128))), f"{fmt} q x{qscale}")

@@ -157,11 +157,16 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------- inputs
-def build_inputs(spec):
-    """Seeded inputs on the host (pinned) for the chosen workload. FP8 and codebook caches
-    are written by the library's own GPU encoders from the seeded fp32 source."""
+def build_inputs(spec, encode_on_gpu=True):
+    """Seeded inputs on the host for the chosen workload. BF16 caches come straight from the
+    generator; FP8 and codebook caches are written on the GPU by the library's own encoders
+    from the seeded fp32 source (and copied back to the host for the end-to-end leg).
+    Returns (layout, host tensors, fp32 sources or None)."""
+    import math
+
     import torch
 
+    import decode_attention_paged_gqa_gb300 as da
     from decode_attention_paged_gqa_gb300 import workloads as wl
 
     lay = wl.make_layout(spec)
@@ -171,9 +176,30 @@ def build_inputs(spec):
     if spec.kv_format == "bf16":
         host["k"] = wl.kv_bf16(spec, "k", lay.num_blocks)
         host["v"] = wl.kv_bf16(spec, "v", lay.num_blocks)
-    else:
-        raise SystemExit(f"workload {spec.name}: the {spec.kv_format} cache needs the GPU encoders")
-    return lay, host
+        return lay, host, None
+    src = {w: wl.kv_source(spec, w, lay.num_blocks) for w in ("k", "v")}
+    D = spec.head_dim
+    if spec.kv_format == "cb4":
+        host["sign"] = wl.sign_pattern(spec)
+    if not encode_on_gpu:  # the CPU reference arm encodes with the oracle from `src`
+        return lay, host, src
+    if spec.kv_format == "cb4":
+        host["codebook"] = torch.tensor(da.decode_attn_codebook_lloyd_max(16, 1.0 / math.sqrt(D)))
+        cb_d, sg_d = host["codebook"].cuda(), host["sign"].cuda()
+    for w in ("k", "v"):
+        x = src[w].cuda()
+        if spec.kv_format == "fp8":
+            codes = torch.empty(x.shape, dtype=torch.uint8, device="cuda")
+            sc = torch.empty(1, dtype=torch.float32, device="cuda")
+            da.decode_attn_encode_fp8(x, x.numel(), codes, sc)
+        else:
+            codes = torch.empty(x.shape[:-1] + (D // 2,), dtype=torch.uint8, device="cuda")
+            sc = torch.empty(x.shape[:-1], dtype=torch.float32, device="cuda")
+            da.decode_attn_encode_cb4(x, x.numel() // D, D, sg_d, cb_d, codes, sc)
+        torch.cuda.synchronize()
+        host[w], host[w + "_scales"] = codes.cpu(), sc.cpu()
+        del x
+    return lay, host, src
 
 
 def source_hash():
@@ -198,35 +224,58 @@ def recorded_traffic(kernel: str, workload: str):
 
 
 # ----------------------------------------------------------------------------- CPU oracle
-def oracle_sample(spec, lay, host, target_s: float, max_seqs=None):
-    """Time the fp64 oracle on the first n sequences (all heads) of the workload, n chosen so
-    the timed sample takes about target_s. Returns (GB/s, seconds, n, threads)."""
+def oracle_inputs(spec, host, src, nseq):
+    """The oracle's inputs for the first nseq sequences: a compact cache holding only their
+    blocks (renumbered), encoded by the oracle's own encoders for FP8 and the codebook."""
     import numpy as np
 
     import oracle
+
+    bt, lens = host["bt"].numpy()[:nseq], host["lens"].numpy()[:nseq]
+    pages = -(-lens // spec.block_size)
+    used = np.unique(np.concatenate([bt[b, :pages[b]] for b in range(nseq)] + [np.zeros(0, np.int32)]))
+    remap = np.full(max(int(host["bt"].max()) + 1, 1), -1, np.int64)
+    remap[used] = np.arange(len(used))
+    sub_bt = np.where(bt >= 0, remap[np.maximum(bt, 0)], -1).astype(np.int32)
+    q = host["q"][:nseq].contiguous().view(__import__("torch").int16).numpy().view(np.uint16)
+    kw = {}
+    if spec.kv_format == "bf16":
+        k = host["k"].view(__import__("torch").int16).numpy().view(np.uint16)[used]
+        v = host["v"].view(__import__("torch").int16).numpy().view(np.uint16)[used]
+    elif spec.kv_format == "fp8":
+        kc, ks = oracle.fp8_quantize(src["k"].numpy())
+        vc, vs = oracle.fp8_quantize(src["v"].numpy())
+        k, v, kw = kc[used], vc[used], dict(k_scales=ks, v_scales=vs)
+    else:
+        cb = oracle.lloyd_max(16, 1.0 / np.sqrt(spec.head_dim))[1]
+        sg = host["sign"].numpy()
+        k, ks = oracle.cb4_encode(src["k"].numpy()[used], sg, cb)
+        v, vs = oracle.cb4_encode(src["v"].numpy()[used], sg, cb)
+        kw = dict(k_scales=ks, v_scales=vs, codebook=cb, sign_pattern=sg)
+    return q, k, v, sub_bt, lens, kw
+
+
+def oracle_sample(spec, host, src, target_s: float, max_seqs=None):
+    """Time the fp64 oracle on the first n sequences (all heads) of the workload, n chosen so
+    that the timed sample takes about target_s. Returns (GB/s, seconds, n, threads)."""
+    import oracle
     from decode_attention_paged_gqa_gb300.metrics import algorithmic_kv_bytes
 
-    def u16(t):
-        return t.contiguous().view(__import__("torch").int16).numpy().view(np.uint16)
-
-    q, k, v = u16(host["q"]), u16(host["k"]), u16(host["v"])
-    bt, lens = host["bt"].numpy(), host["lens"].numpy()
-
     def run(nseq):
-        sel = [(b, h) for b in range(nseq) for h in range(spec.num_q_heads)]
+        q, k, v, bt, lens, kw = oracle_inputs(spec, host, src, nseq)
         t0 = time.perf_counter()
         _, thr = oracle.decode_attention(q, k, v, bt, lens, kv_format=spec.kv_format, num_kv_heads=spec.num_kv_heads,
                                          softmax_scale=spec.scale, softcap=spec.softcap, window=spec.window,
                                          partition_size=spec.partition_size, split_threshold=spec.split_threshold,
-                                         select=sel, return_threads=True)
-        return time.perf_counter() - t0, thr
+                                         return_threads=True, **kw)
+        return time.perf_counter() - t0, thr, lens
 
-    t1, _ = run(1)
+    t1, _, _ = run(1)
     n = max(1, min(spec.batch, int(target_s / max(t1, 1e-3))))
     if max_seqs:
         n = min(n, max_seqs)
-    dt, thr = run(n)
-    nbytes = algorithmic_kv_bytes(lens[:n], spec.window, spec.num_kv_heads, spec.kv_format, spec.head_dim)
+    dt, thr, lens = run(n)
+    nbytes = algorithmic_kv_bytes(lens, spec.window, spec.num_kv_heads, spec.kv_format, spec.head_dim)
     return nbytes / dt / 1e9, dt, n, thr
 
 
@@ -236,13 +285,13 @@ def reference_arm(args, spec, rank, world):
     import oracle
 
     oracle.build()
-    lay, host = build_inputs(spec)
+    lay, host, src = build_inputs(spec, encode_on_gpu=False)
     per_step = max(1.0, min(10.0, 150.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
-        oracle_sample(spec, lay, host, per_step / 4, max_seqs=1)
+        oracle_sample(spec, host, src, per_step / 4, max_seqs=1)
     vals, secs, nseq, thr = [], 0.0, 0, 0
     for _ in range(args.steps):
-        gbs, dt, n, thr = oracle_sample(spec, lay, host, per_step)
+        gbs, dt, n, thr = oracle_sample(spec, host, src, per_step)
         vals.append(gbs)
         secs += dt
         nseq = n
@@ -280,7 +329,7 @@ def main():
         raise SystemExit("bench.py needs a CUDA GPU (the product path has no CPU fallback)")
     lib_build.build()
     torch.cuda.set_device(local)
-    lay, host = build_inputs(spec)
+    lay, host, src = build_inputs(spec)
     dev = {k: (None if t is None else t.cuda()) for k, t in host.items()}
     kv_bytes = algorithmic_kv_bytes(lay.context_lens, spec.window, spec.num_kv_heads, spec.kv_format, spec.head_dim)
     cache_bytes = host["k"].numel() * host["k"].element_size() * 2
@@ -384,7 +433,7 @@ def main():
         import oracle
 
         oracle.build()
-        cgbs, cdt, cn, cthr = oracle_sample(spec, lay, host, args.cpu_seconds)
+        cgbs, cdt, cn, cthr = oracle_sample(spec, host, src, args.cpu_seconds)
         cpu = {"value": cgbs, "unit": UNIT, "cores": cthr, "kind": "oracle",
                "sample": f"first {cn} of {spec.batch} sequences, all {spec.num_q_heads} heads ({cdt:.1f} s)"}
     line = {

@@ -7,6 +7,7 @@ ctypes binding (``_binding``) plus the seeded synthetic input generators (``work
 from ._binding import (  # noqa: F401
     DA_DEVERR_BLOCK_ID,
     DA_DEVERR_CONTEXT_LEN,
+    DA_DEVERR_TIMEOUT,
     DA_KV_BF16,
     DA_KV_CB4,
     DA_KV_FP8_E4M3,
@@ -16,7 +17,10 @@ from ._binding import (  # noqa: F401
     attach_workspace,
     da_params,
     decode_attn_debug_dequant_blocks,
+    decode_attn_codebook_lloyd_max,
     decode_attn_debug_partition_bounds,
+    decode_attn_encode_cb4,
+    decode_attn_encode_fp8,
     decode_attn_get_device_error,
     decode_attn_max_partitions,
     decode_attn_paged,

@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(_HERE, "_build", "libdecode_attn.so")
 DA_KV_BF16, DA_KV_FP8_E4M3, DA_KV_CB4 = 0, 1, 2
 KV_FORMATS = {"bf16": DA_KV_BF16, "fp8": DA_KV_FP8_E4M3, "cb4": DA_KV_CB4}
 DA_OK, DA_ERR_INVALID_ARG, DA_ERR_UNSUPPORTED, DA_ERR_WORKSPACE, DA_ERR_LAUNCH, DA_ERR_CUDA = 0, -1, -2, -3, -4, -5
-DA_DEVERR_BLOCK_ID, DA_DEVERR_CONTEXT_LEN = 0x1, 0x2
+DA_DEVERR_BLOCK_ID, DA_DEVERR_CONTEXT_LEN, DA_DEVERR_TIMEOUT = 0x1, 0x2, 0x4
 
 
 class DecodeAttnError(RuntimeError):
@@ -94,6 +94,9 @@ def _load():
                 "decode_attn_get_device_error": (I, [PP, P, ctypes.POINTER(ctypes.c_uint32)]),
                 "decode_attn_strerror": (ctypes.c_char_p, [I]),
                 "decode_attn_max_partitions": (I, [PP]),
+                "decode_attn_encode_fp8": (I, [P, ctypes.c_int64, P, P, P]),
+                "decode_attn_encode_cb4": (I, [P, ctypes.c_int64, ctypes.c_int32, P, P, P, P, P]),
+                "decode_attn_codebook_lloyd_max": (I, [ctypes.c_int32, ctypes.c_double, P]),
                 "decode_attn_debug_partition_bounds": (I, [P, P, PP, P]),
                 "decode_attn_debug_dequant_blocks": (I, [P, P, P, P, ctypes.c_int32, P, PP, P]),
             }
@@ -188,6 +191,24 @@ def decode_attn_get_device_error(params: da_params, stream=None) -> int:
     _check(_load().decode_attn_get_device_error(ctypes.byref(params), _stream(stream), ctypes.byref(v)),
            "decode_attn_get_device_error")
     return int(v.value)
+
+
+def decode_attn_encode_fp8(x, n, codes, scale_out, stream=None) -> None:
+    _check(_load().decode_attn_encode_fp8(_ptr(x), int(n), _ptr(codes), _ptr(scale_out), _stream(stream)),
+           "decode_attn_encode_fp8")
+
+
+def decode_attn_encode_cb4(x, num_vectors, head_dim, sign_pattern, codebook, packed, scales, stream=None) -> None:
+    _check(_load().decode_attn_encode_cb4(_ptr(x), int(num_vectors), int(head_dim), _ptr(sign_pattern),
+                                          _ptr(codebook), _ptr(packed), _ptr(scales), _stream(stream)),
+           "decode_attn_encode_cb4")
+
+
+def decode_attn_codebook_lloyd_max(levels: int, sigma: float):
+    """Host call: the Lloyd-Max codebook as a list of `levels` floats (ascending)."""
+    buf = (ctypes.c_float * int(levels))()
+    _check(_load().decode_attn_codebook_lloyd_max(int(levels), float(sigma), buf), "decode_attn_codebook_lloyd_max")
+    return [float(v) for v in buf]
 
 
 def decode_attn_debug_partition_bounds(context_lens, bounds, params: da_params, stream=None) -> None:

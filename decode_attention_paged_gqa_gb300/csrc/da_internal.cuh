@@ -156,6 +156,10 @@ cudaError_t launch_partition(const Args& a, cudaStream_t s);     // dispatches o
 cudaError_t launch_partition_tc(const Args& a, cudaStream_t s);  //   BF16, FP8: TMA + tensor cores
 cudaError_t launch_partition_simt(const Args& a, cudaStream_t s);  // CB4: CUDA cores
 cudaError_t launch_reduce(const Args& a, cudaStream_t s);
+cudaError_t launch_encode_fp8(const float* x, long long n, uint8_t* codes, float* scale, cudaStream_t s);
+cudaError_t launch_encode_cb4(const float* x, long long nvec, int D, const float* sign, const float* codebook,
+                              uint8_t* packed, float* scales, cudaStream_t s);
+int lloyd_max_codebook(int levels, double sigma, float* out);
 cudaError_t launch_debug_bounds(const Args& a, int32_t* bounds, cudaStream_t s);
 cudaError_t launch_debug_dequant(const Args& a, const void* cache, const float* scales, const int32_t* ids, int n,
                                  float* out, cudaStream_t s);

@@ -195,6 +195,30 @@ int decode_attn_max_partitions(const da_params* p) {
   return host_max_partitions(*p);
 }
 
+int decode_attn_encode_fp8(const float* x, int64_t n, uint8_t* codes, float* scale_out, void* stream) {
+  if (n < 0 || !scale_out || (n > 0 && (!x || !codes)) || !aligned(scale_out, 4) || !aligned(x, 4))
+    return DA_ERR_INVALID_ARG;
+  return launch_encode_fp8(x, n, codes, scale_out, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? DA_OK
+             : DA_ERR_LAUNCH;
+}
+
+int decode_attn_encode_cb4(const float* x, int64_t num_vectors, int32_t head_dim, const float* sign_pattern,
+                           const float* codebook, uint8_t* packed, float* scales, void* stream) {
+  if (num_vectors < 0 || (num_vectors > 0 && (!x || !sign_pattern || !codebook || !packed || !scales)))
+    return DA_ERR_INVALID_ARG;
+  if (head_dim != 128 && head_dim != 256) return DA_ERR_UNSUPPORTED;
+  return launch_encode_cb4(x, num_vectors, head_dim, sign_pattern, codebook, packed, scales,
+                           static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? DA_OK
+             : DA_ERR_LAUNCH;
+}
+
+int decode_attn_codebook_lloyd_max(int32_t levels, double sigma, float* codebook_host) {
+  if (!codebook_host) return DA_ERR_INVALID_ARG;
+  return lloyd_max_codebook(levels, sigma, codebook_host) == 0 ? DA_OK : DA_ERR_INVALID_ARG;
+}
+
 int decode_attn_debug_partition_bounds(const int32_t* context_lens, int32_t* bounds, const da_params* p,
                                        void* stream) {
   int rc = check_params(p);

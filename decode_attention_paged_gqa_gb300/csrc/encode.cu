@@ -1,0 +1,169 @@
+// encode.cu -- cache writers for the quantised KV formats (the step before the hot path),
+// and the Lloyd-Max codebook of the 4-bit format.
+//
+// FP8 E4M3 with one scale per tensor (attention.rs README, KV Cache Formats table, "FP8
+// (E4M3)"): scale = amax|x| / 448 in binary32, code = round-to-nearest-even E4M3 of the
+// binary32 quotient x / scale, saturating at +-448.
+//
+// 4-bit codebook on a random-sign Walsh-Hadamard basis (same table, "Turbo4";
+// turboquant-rs 0.4.1, src/cache/cuda/attention.rs: codebook + sign_pattern inputs):
+//   r = H diag(sign) x / sqrt(D), scale = ||x||_2 (stored as binary32),
+//   idx_d = nearest codebook value to r_d / scale (ties to the lower index),
+//   two indices per byte, coordinate 2k in the low nibble of byte k.
+// The norm and the rotation are computed in fp64 with the sums taken in index order, so
+// every code decision is made on the same fp64 value a plain sequential evaluation gives.
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "da_internal.cuh"
+
+namespace da {
+namespace {
+
+__global__ void amax_kernel(const float* __restrict__ x, long long n, unsigned* __restrict__ amax_bits) {
+  float m = 0.0f;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x)
+    m = fmaxf(m, fabsf(x[i]));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  // non-negative floats order like their bit patterns
+  if ((threadIdx.x & 31) == 0) atomicMax(amax_bits, __float_as_uint(m));
+}
+
+__global__ void fp8_scale_kernel(float* scale) {
+  const float amax = *scale;  // holds the amax bits written by amax_kernel
+  *scale = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+}
+
+__global__ void fp8_cast_kernel(const float* __restrict__ x, long long n, const float* __restrict__ scale,
+                                uint8_t* __restrict__ codes) {
+  const float s = *scale;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x)
+    codes[i] = (uint8_t)__nv_cvt_float_to_fp8(__fdiv_rn(x[i], s), __NV_SATFINITE, __NV_E4M3);
+}
+
+// One warp per vector; lane l produces coordinates l, l + 32, ...
+template <int D>
+__global__ void __launch_bounds__(128) cb4_encode_kernel(const float* __restrict__ x, long long nvec,
+                                                         const float* __restrict__ sign,
+                                                         const float* __restrict__ codebook,
+                                                         uint8_t* __restrict__ packed, float* __restrict__ scales) {
+  __shared__ double xs_all[4][D];
+  __shared__ float cb[16];
+  if (threadIdx.x < 16) cb[threadIdx.x] = codebook[threadIdx.x];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  double* xs = xs_all[w];
+  __syncthreads();
+  for (long long v = blockIdx.x * 4ll + w; v < nvec; v += gridDim.x * 4ll) {
+    const float* xv = x + v * D;
+    for (int k = lane; k < D; k += 32) xs[k] = (double)sign[k] * (double)xv[k];
+    __syncwarp();
+    // ||x||^2 in index order (exact squares, fp64 sums)
+    double n2 = 0.0;
+    for (int k = 0; k < D; ++k) n2 += xs[k] * xs[k];
+    const float scale = (float)sqrt(n2);
+    const double inv = 1.0 / sqrt((double)D);
+    uint8_t idx[D / 32];
+#pragma unroll
+    for (int j = 0; j < D / 32; ++j) {
+      const int i = lane + 32 * j;
+      double acc = 0.0;
+      for (int k = 0; k < D; ++k) acc += (__popc(i & k) & 1) ? -xs[k] : xs[k];  // H[i][k] sign[k] x[k]
+      const double r = acc * inv;
+      const double u = scale > 0.0f ? r / (double)scale : 0.0;
+      int best = 0;
+      double bd = fabs(u - (double)cb[0]);
+      for (int c = 1; c < 16; ++c) {
+        const double dd = fabs(u - (double)cb[c]);
+        if (dd < bd) {
+          bd = dd;
+          best = c;
+        }
+      }
+      idx[j] = (uint8_t)best;
+    }
+    // pack: coordinate 2k (even lane) low nibble, 2k + 1 (odd lane) high nibble
+#pragma unroll
+    for (int j = 0; j < D / 32; ++j) {
+      const unsigned other = __shfl_xor_sync(0xffffffffu, (unsigned)idx[j], 1);
+      if ((lane & 1) == 0) packed[v * (D / 2) + (lane + 32 * j) / 2] = (uint8_t)(idx[j] | (other << 4));
+    }
+    if (lane == 0) scales[v] = scale;
+    __syncwarp();
+  }
+}
+
+int grid_for(long long n, int threads) {
+  long long g = (n + threads - 1) / threads;
+  return (int)(g < 4096 ? (g < 1 ? 1 : g) : 4096);
+}
+
+// ---------------------------------------------------------------- Lloyd-Max (host)
+double phi(double z) { return exp(-0.5 * z * z) / sqrt(2.0 * M_PI); }
+// standard normal mass of (a, b], from erfc so both tails keep their precision
+double mass(double a, double b) {
+  if (a >= 0.0) return 0.5 * (erfc(a / M_SQRT2) - erfc(b / M_SQRT2));
+  if (b <= 0.0) return 0.5 * (erfc(-b / M_SQRT2) - erfc(-a / M_SQRT2));
+  return 1.0 - 0.5 * erfc(-a / M_SQRT2) - 0.5 * erfc(b / M_SQRT2);
+}
+
+}  // namespace
+
+cudaError_t launch_encode_fp8(const float* x, long long n, uint8_t* codes, float* scale, cudaStream_t s) {
+  cudaError_t e = cudaMemsetAsync(scale, 0, sizeof(float), s);
+  if (e != cudaSuccess) return e;
+  if (n > 0) amax_kernel<<<grid_for(n, 256), 256, 0, s>>>(x, n, reinterpret_cast<unsigned*>(scale));
+  fp8_scale_kernel<<<1, 1, 0, s>>>(scale);
+  if (n > 0) fp8_cast_kernel<<<grid_for(n, 256), 256, 0, s>>>(x, n, scale, codes);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_encode_cb4(const float* x, long long nvec, int D, const float* sign, const float* codebook,
+                              uint8_t* packed, float* scales, cudaStream_t s) {
+  if (nvec == 0) return cudaSuccess;
+  const int grid = (int)((nvec + 3) / 4 < 8192 ? (nvec + 3) / 4 : 8192);
+  if (D == 128)
+    cb4_encode_kernel<128><<<grid, 128, 0, s>>>(x, nvec, sign, codebook, packed, scales);
+  else
+    cb4_encode_kernel<256><<<grid, 128, 0, s>>>(x, nvec, sign, codebook, packed, scales);
+  return cudaGetLastError();
+}
+
+// Lloyd-Max quantiser of `levels` output levels for N(0, sigma^2): thresholds at the
+// midpoints of neighbouring levels, each level at the conditional mean of its cell,
+// repeated from evenly spaced levels on [-3 sigma, 3 sigma] until no level moves by more
+// than 1e-14 sigma; then made exactly symmetric and rounded to binary32.
+int lloyd_max_codebook(int levels, double sigma, float* out) {
+  if (levels < 2 || levels > 64 || !(sigma > 0.0)) return -1;
+  double c[64], t[65];
+  const int L = levels;
+  for (int i = 0; i < L; ++i) c[i] = -3.0 + 6.0 * (i + 0.5) / L;
+  int it = 0;
+  for (; it < 1000000; ++it) {
+    double moved = 0.0;
+    t[0] = -INFINITY;
+    t[L] = INFINITY;
+    for (int i = 1; i < L; ++i) t[i] = 0.5 * (c[i - 1] + c[i]);
+    for (int i = 0; i < L; ++i) {
+      const double pa = std::isinf(t[i]) ? 0.0 : phi(t[i]), pb = std::isinf(t[i + 1]) ? 0.0 : phi(t[i + 1]);
+      const double nc = (pa - pb) / mass(t[i], t[i + 1]);
+      moved = fmax(moved, fabs(nc - c[i]));
+      c[i] = nc;
+    }
+    if (moved < 1e-14) break;
+  }
+  if (it == 1000000) return -1;
+  for (int i = 0; i < L / 2; ++i) {
+    const double m = 0.5 * (c[L - 1 - i] - c[i]);
+    c[i] = -m;
+    c[L - 1 - i] = m;
+  }
+  if (L % 2) c[L / 2] = 0.0;
+  for (int i = 0; i < L; ++i) out[i] = (float)(sigma * c[i]);
+  return 0;
+}
+
+}  // namespace da

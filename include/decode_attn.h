@@ -159,6 +159,30 @@ const char* decode_attn_strerror(int status);
 /* Partition count the grid is sized for: that of a sequence of length max_context_len. */
 int decode_attn_max_partitions(const da_params* p);
 
+/* ---- cache writers: the step that fills the quantised caches ------------------------- */
+
+/* FP8 E4M3 encoding of one cache tensor (attention.rs README, KV Cache Formats table):
+ * scale = max|x| / 448 (binary32; 1 for an all-zero tensor) is written to *scale_out
+ * (device float), and codes[i] = round-to-nearest-even E4M3 of the binary32 quotient
+ * x[i] / scale, saturating at +-448 (NaN stays NaN). x: n device floats, in the cache's
+ * layout; codes: n device bytes. Three kernels on `stream`. */
+int decode_attn_encode_fp8(const float* x, int64_t n, uint8_t* codes, float* scale_out, void* stream);
+
+/* 4-bit codebook encoding of num_vectors vectors of head_dim floats (128 or 256), e.g. the
+ * rows [num_blocks][Hkv][block_size] of a cache: r = H diag(sign) x / sqrt(D); scale =
+ * ||x||_2 as binary32; idx_d = nearest codebook[16] value to r_d / scale (ties to the lower
+ * index); packed[v][k] = idx_{2k} | idx_{2k+1} << 4; scales[v] = scale. The norm and the
+ * rotation are evaluated in fp64 with index-ordered sums, so the codes do not depend on
+ * the thread layout. All pointers are device pointers. */
+int decode_attn_encode_cb4(const float* x, int64_t num_vectors, int32_t head_dim, const float* sign_pattern,
+                           const float* codebook, uint8_t* packed, float* scales, void* stream);
+
+/* Host-side: the `levels`-level Lloyd-Max quantiser of N(0, sigma^2) (alternate midpoint
+ * thresholds and conditional-mean levels until no level moves by 1e-14 sigma, then make it
+ * exactly symmetric), written ascending as binary32 to codebook_host[levels]. The
+ * codebook format uses levels = 16, sigma = 1/sqrt(D). Returns DA_OK or DA_ERR_INVALID_ARG. */
+int decode_attn_codebook_lloyd_max(int32_t levels, double sigma, float* codebook_host);
+
 /* ---- debug exports: the kernels' own device code, for bit-exact tests ---------------- */
 
 /* bounds [B][P][2] int32 (P = decode_attn_max_partitions): [start, end) of partition p of

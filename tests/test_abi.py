@@ -121,3 +121,18 @@ def test_strerror():
     for s in range(-5, 1):
         assert da.decode_attn_strerror(s) != "unknown status"
     assert da.decode_attn_strerror(-99) == "unknown status"
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+def test_library_codebook_equals_oracle_codebook(D):
+    import math
+
+    import numpy as np
+
+    import oracle
+
+    ours = np.array(da.decode_attn_codebook_lloyd_max(16, 1.0 / math.sqrt(D)), np.float32)
+    ref = oracle.lloyd_max(16, 1.0 / math.sqrt(D))[1]
+    assert np.array_equal(ours, ref)
+    with pytest.raises(da.DecodeAttnError):
+        da.decode_attn_codebook_lloyd_max(1, 1.0)

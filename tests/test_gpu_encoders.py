@@ -1,0 +1,73 @@
+"""The library's cache writers on the GPU against the oracle's encoders: FP8 scale and
+codes, 4-bit codebook norms and packed indices, all bit for bit."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import decode_attention_paged_gqa_gb300 as da
+from decode_attention_paged_gqa_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from decode_attention_paged_gqa_gb300 import build
+
+    build.build()
+
+
+@pytest.mark.parametrize("n,scale", [(1, 1.0), (1000, 3.0), (1 << 20, 1.0), (3_000_001, 1e-3)])
+def test_fp8_encoder_bit_exact(n, scale):
+    g = torch.Generator().manual_seed(n)
+    x = torch.randn(n, generator=g) * scale
+    x[::97] *= 50.0
+    if n > 10:
+        x[3] = 0.0
+        x[5] = -0.0
+    codes_ref, s_ref = oracle.fp8_quantize(x.numpy())
+    xd = x.cuda()
+    codes = torch.empty(n, dtype=torch.uint8, device="cuda")
+    s = torch.empty(1, dtype=torch.float32, device="cuda")
+    da.decode_attn_encode_fp8(xd, n, codes, s)
+    assert s.item() == s_ref
+    assert np.array_equal(codes.cpu().numpy(), codes_ref)
+
+
+def test_fp8_encoder_zero_tensor_and_repeat():
+    x = torch.zeros(4096, device="cuda")
+    codes = torch.full((4096,), 7, dtype=torch.uint8, device="cuda")
+    s = torch.full((1,), 5.0, device="cuda")
+    da.decode_attn_encode_fp8(x, 4096, codes, s)
+    assert s.item() == 1.0 and int(codes.max()) == 0
+    y = torch.randn(4096, device="cuda")
+    da.decode_attn_encode_fp8(y, 4096, codes, s)  # the scale slot is reset each call
+    ref_codes, ref_s = oracle.fp8_quantize(y.cpu().numpy())
+    assert s.item() == ref_s and np.array_equal(codes.cpu().numpy(), ref_codes)
+
+
+@pytest.mark.parametrize("D", [128, 256])
+def test_cb4_encoder_bit_exact(D):
+    spec = wl.WorkloadSpec("enc", 2, 8, 4, D, "cb4", 100, 300, seed=D)
+    lay = wl.make_layout(spec)
+    x = wl.kv_source(spec, "k", lay.num_blocks)
+    x[0, 0, 0] = 0.0  # a zero vector
+    sg = wl.sign_pattern(spec)
+    cb = oracle.lloyd_max(16, 1.0 / math.sqrt(D))[1]
+    packed_ref, scales_ref = oracle.cb4_encode(x.numpy(), sg.numpy(), cb)
+    nvec = x.numel() // D
+    packed = torch.empty(x.shape[:-1] + (D // 2,), dtype=torch.uint8, device="cuda")
+    scales = torch.empty(x.shape[:-1], dtype=torch.float32, device="cuda")
+    da.decode_attn_encode_cb4(x.cuda(), nvec, D, sg.cuda(), torch.from_numpy(cb).cuda(), packed, scales)
+    assert np.array_equal(scales.cpu().numpy(), scales_ref)
+    assert np.array_equal(packed.cpu().numpy(), packed_ref)
+
+
+def test_cb4_encoder_rejects_bad_head_dim():
+    with pytest.raises(da.DecodeAttnError):
+        da.decode_attn_encode_cb4(256, 1, 96, 256, 256, 256, 256)

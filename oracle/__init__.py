@@ -14,6 +14,7 @@ Every function here is pinned by the ``-m "not gpu"`` tests in ``tests/test_orac
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import subprocess
@@ -33,50 +34,73 @@ _lib = None
 _lock = threading.Lock()
 
 
+def compile_source(src: str, out: str) -> str:
+    """gcc -O2 without FMA contraction or fast-math; used for oracle.c (and, by the mutation
+    test, for deliberately broken copies of it)."""
+    tmp = out + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=gnu11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared", "-pthread",
+           src, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
 def build(force: bool = False) -> str:
-    """Compile oracle.c into oracle/_build/liboracle.so (gcc, -O2, no FMA contraction)."""
+    """Compile oracle.c into oracle/_build/liboracle.so."""
     os.makedirs(_BUILD_DIR, exist_ok=True)
     if not force and os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC):
         return _LIB_PATH
-    tmp = _LIB_PATH + f".tmp{os.getpid()}"
-    cmd = ["gcc", "-O2", "-std=gnu11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared", "-pthread",
-           _SRC, "-o", tmp, "-lm"]
-    subprocess.run(cmd, check=True)
-    os.replace(tmp, _LIB_PATH)
-    return _LIB_PATH
+    return compile_source(_SRC, _LIB_PATH)
+
+
+@contextlib.contextmanager
+def library_override(path: str):
+    """Run the oracle's Python functions against another build of oracle.c (tests only)."""
+    global _lib
+    with _lock:
+        saved = _lib
+        _lib = _open(path)
+    try:
+        yield
+    finally:
+        with _lock:
+            _lib = saved
 
 
 def _load():
     global _lib
     with _lock:
-        if _lib is not None:
-            return _lib
-        lib = ctypes.CDLL(build())
-        P, I, I64, D, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_double, ctypes.c_float
-        sig = {
-            "or_bf16_decode": (D, [ctypes.c_uint16]),
-            "or_e4m3_decode": (D, [ctypes.c_uint8]),
-            "or_e4m3_encode": (ctypes.c_uint8, [F]),
-            "or_e4m3_decode_array": (None, [P, I64, P]),
-            "or_e4m3_encode_array": (None, [P, I64, P]),
-            "or_fp8_quantize": (F, [P, I64, P, I]),
-            "or_hadamard": (None, [I, P]),
-            "or_lloyd_max": (I, [I, D, D, I, P, P]),
-            "or_cb_nearest": (I, [D, P, I]),
-            "or_cb4_encode": (I, [P, I64, I, P, P, P, P, I]),
-            "or_cb4_dequant_rotated": (None, [P, P, I64, I, P, P]),
-            "or_cb4_dequant": (None, [P, P, I64, I, P, P, P]),
-            "or_partition_bounds": (I, [I, I, I, I, P, P, I]),
-            "or_default_threads": (I, []),
-            "or_decode_attention": (I, [I, I, I, I, I, I, I, I, P, P, P, P, P, P, P, P, P, D, D, I, I, I, P, P, I,
-                                        ctypes.POINTER(ctypes.c_int)]),
-        }
-        for name, (res, args) in sig.items():
-            fn = getattr(lib, name)
-            fn.restype = res
-            fn.argtypes = args
-        _lib = lib
-        return lib
+        if _lib is None:
+            _lib = _open(build())
+        return _lib
+
+
+def _open(path: str):
+    lib = ctypes.CDLL(path)
+    P, I, I64, D, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_double, ctypes.c_float
+    sig = {
+        "or_bf16_decode": (D, [ctypes.c_uint16]),
+        "or_e4m3_decode": (D, [ctypes.c_uint8]),
+        "or_e4m3_encode": (ctypes.c_uint8, [F]),
+        "or_e4m3_decode_array": (None, [P, I64, P]),
+        "or_e4m3_encode_array": (None, [P, I64, P]),
+        "or_fp8_quantize": (F, [P, I64, P, I]),
+        "or_hadamard": (None, [I, P]),
+        "or_lloyd_max": (I, [I, D, D, I, P, P]),
+        "or_cb_nearest": (I, [D, P, I]),
+        "or_cb4_encode": (I, [P, I64, I, P, P, P, P, I]),
+        "or_cb4_dequant_rotated": (None, [P, P, I64, I, P, P]),
+        "or_cb4_dequant": (None, [P, P, I64, I, P, P, P]),
+        "or_partition_bounds": (I, [I, I, I, I, P, P, I]),
+        "or_default_threads": (I, []),
+        "or_decode_attention": (I, [I, I, I, I, I, I, I, I, P, P, P, P, P, P, P, P, P, D, D, I, I, I, P, P, I,
+                                    ctypes.POINTER(ctypes.c_int)]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
 
 
 def _ptr(a):

@@ -177,25 +177,30 @@ def build_inputs(spec, encode_on_gpu=True):
         host["k"] = wl.kv_bf16(spec, "k", lay.num_blocks)
         host["v"] = wl.kv_bf16(spec, "v", lay.num_blocks)
         return lay, host, None
+    sides = {"fp8": ("fp8", "fp8"), "cb4": ("cb4", "cb4"), "fp8k_cb4v": ("fp8", "cb4"),
+             "cb3k_cb4v": ("cb3", "cb4")}[spec.kv_format]
     src = {w: wl.kv_source(spec, w, lay.num_blocks) for w in ("k", "v")}
     D = spec.head_dim
-    if spec.kv_format == "cb4":
+    if "cb3" in sides or "cb4" in sides:
         host["sign"] = wl.sign_pattern(spec)
     if not encode_on_gpu:  # the CPU reference arm encodes with the oracle from `src`
         return lay, host, src
-    if spec.kv_format == "cb4":
-        host["codebook"] = torch.tensor(da.decode_attn_codebook_lloyd_max(16, 1.0 / math.sqrt(D)))
-        cb_d, sg_d = host["codebook"].cuda(), host["sign"].cuda()
-    for w in ("k", "v"):
+    cbs = {}
+    if "cb3" in sides or "cb4" in sides:
+        cbs = {b: torch.tensor(da.decode_attn_codebook_lloyd_max(1 << b, 1.0 / math.sqrt(D))) for b in (3, 4)}
+        host["codebook"] = torch.cat([cbs[3], cbs[4]]) if sides[0] == "cb3" else cbs[4]
+        sg_d = host["sign"].cuda()
+    for w, side in zip(("k", "v"), sides):
         x = src[w].cuda()
-        if spec.kv_format == "fp8":
+        if side == "fp8":
             codes = torch.empty(x.shape, dtype=torch.uint8, device="cuda")
             sc = torch.empty(1, dtype=torch.float32, device="cuda")
             da.decode_attn_encode_fp8(x, x.numel(), codes, sc)
         else:
-            codes = torch.empty(x.shape[:-1] + (D // 2,), dtype=torch.uint8, device="cuda")
+            bits = 3 if side == "cb3" else 4
+            codes = torch.empty(x.shape[:-1] + (D * bits // 8,), dtype=torch.uint8, device="cuda")
             sc = torch.empty(x.shape[:-1], dtype=torch.float32, device="cuda")
-            da.decode_attn_encode_cb4(x, x.numel() // D, D, sg_d, cb_d, codes, sc)
+            da.decode_attn_encode_codebook(x, x.numel() // D, D, bits, sg_d, cbs[bits].cuda(), codes, sc)
         torch.cuda.synchronize()
         host[w], host[w + "_scales"] = codes.cpu(), sc.cpu()
         del x
@@ -242,16 +247,24 @@ def oracle_inputs(spec, host, src, nseq):
     if spec.kv_format == "bf16":
         k = host["k"].view(__import__("torch").int16).numpy().view(np.uint16)[used]
         v = host["v"].view(__import__("torch").int16).numpy().view(np.uint16)[used]
-    elif spec.kv_format == "fp8":
-        kc, ks = oracle.fp8_quantize(src["k"].numpy())
-        vc, vs = oracle.fp8_quantize(src["v"].numpy())
-        k, v, kw = kc[used], vc[used], dict(k_scales=ks, v_scales=vs)
     else:
-        cb = oracle.lloyd_max(16, 1.0 / np.sqrt(spec.head_dim))[1]
-        sg = host["sign"].numpy()
-        k, ks = oracle.cb4_encode(src["k"].numpy()[used], sg, cb)
-        v, vs = oracle.cb4_encode(src["v"].numpy()[used], sg, cb)
-        kw = dict(k_scales=ks, v_scales=vs, codebook=cb, sign_pattern=sg)
+        sides = oracle.SIDES[spec.kv_format]
+        D = spec.head_dim
+        cb = {b: oracle.lloyd_max(1 << b, 1.0 / np.sqrt(D))[1] for b in (3, 4)}
+        sg = host["sign"].numpy() if host["sign"] is not None else None
+        enc = {}
+        for w, side in zip(("k", "v"), sides):
+            if side == "fp8":
+                codes, sc = oracle.fp8_quantize(src[w].numpy())
+                enc[w] = (codes[used], sc)
+            else:
+                bits = 3 if side == "cb3" else 4
+                enc[w] = oracle.cb_encode(bits, src[w].numpy()[used], sg, cb[bits])
+        k, v = enc["k"][0], enc["v"][0]
+        kw = dict(k_scales=enc["k"][1], v_scales=enc["v"][1])
+        if sg is not None:
+            kw["codebook"] = np.concatenate([cb[3], cb[4]]) if sides[0] == "cb3" else cb[4]
+            kw["sign_pattern"] = sg
     return q, k, v, sub_bt, lens, kw
 
 

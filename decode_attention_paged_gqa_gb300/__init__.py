@@ -9,8 +9,10 @@ from ._binding import (  # noqa: F401
     DA_DEVERR_CONTEXT_LEN,
     DA_DEVERR_TIMEOUT,
     DA_KV_BF16,
+    DA_KV_CB3K_CB4V,
     DA_KV_CB4,
     DA_KV_FP8_E4M3,
+    DA_KV_FP8K_CB4V,
     KV_FORMATS,
     LIB_PATH,
     DecodeAttnError,
@@ -20,6 +22,7 @@ from ._binding import (  # noqa: F401
     decode_attn_codebook_lloyd_max,
     decode_attn_debug_partition_bounds,
     decode_attn_encode_cb4,
+    decode_attn_encode_codebook,
     decode_attn_encode_fp8,
     decode_attn_get_device_error,
     decode_attn_max_partitions,

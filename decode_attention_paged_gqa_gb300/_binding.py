@@ -15,8 +15,9 @@ import threading
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libdecode_attn.so")
 
-DA_KV_BF16, DA_KV_FP8_E4M3, DA_KV_CB4 = 0, 1, 2
-KV_FORMATS = {"bf16": DA_KV_BF16, "fp8": DA_KV_FP8_E4M3, "cb4": DA_KV_CB4}
+DA_KV_BF16, DA_KV_FP8_E4M3, DA_KV_CB4, DA_KV_FP8K_CB4V, DA_KV_CB3K_CB4V = 0, 1, 2, 3, 4
+KV_FORMATS = {"bf16": DA_KV_BF16, "fp8": DA_KV_FP8_E4M3, "cb4": DA_KV_CB4, "fp8k_cb4v": DA_KV_FP8K_CB4V,
+              "cb3k_cb4v": DA_KV_CB3K_CB4V}
 DA_OK, DA_ERR_INVALID_ARG, DA_ERR_UNSUPPORTED, DA_ERR_WORKSPACE, DA_ERR_LAUNCH, DA_ERR_CUDA = 0, -1, -2, -3, -4, -5
 DA_DEVERR_BLOCK_ID, DA_DEVERR_CONTEXT_LEN, DA_DEVERR_TIMEOUT = 0x1, 0x2, 0x4
 
@@ -96,9 +97,11 @@ def _load():
                 "decode_attn_max_partitions": (I, [PP]),
                 "decode_attn_encode_fp8": (I, [P, ctypes.c_int64, P, P, P]),
                 "decode_attn_encode_cb4": (I, [P, ctypes.c_int64, ctypes.c_int32, P, P, P, P, P]),
+                "decode_attn_encode_codebook": (I, [P, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, P, P, P, P,
+                                                    P]),
                 "decode_attn_codebook_lloyd_max": (I, [ctypes.c_int32, ctypes.c_double, P]),
                 "decode_attn_debug_partition_bounds": (I, [P, P, PP, P]),
-                "decode_attn_debug_dequant_blocks": (I, [P, P, P, P, ctypes.c_int32, P, PP, P]),
+                "decode_attn_debug_dequant_blocks": (I, [P, P, P, P, ctypes.c_int32, ctypes.c_int32, P, PP, P]),
             }
             for name, (res, args) in sigs.items():
                 fn = getattr(lib, name)
@@ -204,6 +207,13 @@ def decode_attn_encode_cb4(x, num_vectors, head_dim, sign_pattern, codebook, pac
            "decode_attn_encode_cb4")
 
 
+def decode_attn_encode_codebook(x, num_vectors, head_dim, bits, sign_pattern, codebook, packed, scales,
+                                stream=None) -> None:
+    _check(_load().decode_attn_encode_codebook(_ptr(x), int(num_vectors), int(head_dim), int(bits),
+                                               _ptr(sign_pattern), _ptr(codebook), _ptr(packed), _ptr(scales),
+                                               _stream(stream)), "decode_attn_encode_codebook")
+
+
 def decode_attn_codebook_lloyd_max(levels: int, sigma: float):
     """Host call: the Lloyd-Max codebook as a list of `levels` floats (ascending)."""
     buf = (ctypes.c_float * int(levels))()
@@ -216,8 +226,8 @@ def decode_attn_debug_partition_bounds(context_lens, bounds, params: da_params, 
                                                       _stream(stream)), "decode_attn_debug_partition_bounds")
 
 
-def decode_attn_debug_dequant_blocks(cache, scales, codebook, block_ids, n, out, params: da_params,
+def decode_attn_debug_dequant_blocks(cache, scales, codebook, block_ids, n, which, out, params: da_params,
                                      stream=None) -> None:
     _check(_load().decode_attn_debug_dequant_blocks(_ptr(cache), _ptr(scales), _ptr(codebook), _ptr(block_ids),
-                                                    int(n), _ptr(out), ctypes.byref(params), _stream(stream)),
-           "decode_attn_debug_dequant_blocks")
+                                                    int(n), int(which), _ptr(out), ctypes.byref(params),
+                                                    _stream(stream)), "decode_attn_debug_dequant_blocks")

@@ -36,7 +36,7 @@ struct Args {
   int P;                      // partitions the grid and the workspace are sized for
   // workspace pieces
   uint32_t* err;              // device error word (DA_DEVERR_* bits)
-  float* q_rot;               // [B][Hq][D] (cb4)
+  float* q_rot;               // [B][Hq][D] (formats whose keys are on the rotated basis)
   float* part_o;              // [B][Hq][P][D], unnormalised partial outputs
   float* part_m;              // [B][Hq][P], running max in log2 units
   float* part_l;              // [B][Hq][P], running sum of 2^(s - m)
@@ -121,7 +121,8 @@ inline Layout workspace_layout(const da_params& p) {
   l.err = off;
   off = align256(off + sizeof(uint32_t));
   l.q_rot = off;
-  off = align256(off + (p.kv_format == DA_KV_CB4 ? BH * p.head_dim * sizeof(float) : 0));
+  const bool rotated_keys = p.kv_format == DA_KV_CB4 || p.kv_format == DA_KV_CB3K_CB4V;
+  off = align256(off + (rotated_keys ? BH * p.head_dim * sizeof(float) : 0));
   l.part_o = off;
   off = align256(off + BH * P * p.head_dim * sizeof(float));
   l.part_m = off;
@@ -157,11 +158,11 @@ cudaError_t launch_partition_tc(const Args& a, cudaStream_t s);  //   BF16, FP8:
 cudaError_t launch_partition_simt(const Args& a, cudaStream_t s);  // CB4: CUDA cores
 cudaError_t launch_reduce(const Args& a, cudaStream_t s);
 cudaError_t launch_encode_fp8(const float* x, long long n, uint8_t* codes, float* scale, cudaStream_t s);
-cudaError_t launch_encode_cb4(const float* x, long long nvec, int D, const float* sign, const float* codebook,
-                              uint8_t* packed, float* scales, cudaStream_t s);
+cudaError_t launch_encode_codebook(const float* x, long long nvec, int D, int bits, const float* sign,
+                                   const float* codebook, uint8_t* packed, float* scales, cudaStream_t s);
 int lloyd_max_codebook(int levels, double sigma, float* out);
 cudaError_t launch_debug_bounds(const Args& a, int32_t* bounds, cudaStream_t s);
 cudaError_t launch_debug_dequant(const Args& a, const void* cache, const float* scales, const int32_t* ids, int n,
-                                 float* out, cudaStream_t s);
+                                 int which, float* out, cudaStream_t s);
 
 }  // namespace da

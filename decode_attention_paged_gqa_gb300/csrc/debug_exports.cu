@@ -21,11 +21,11 @@ __global__ void debug_bounds_kernel(const Args a, int32_t* bounds) {
 }
 
 // One CTA per listed block; each thread dequantises 8-element chunks of its rows.
-template <int FMT>
+template <int S>
 __global__ void debug_dequant_kernel(const Args a, const void* cache, const float* scales, const int32_t* ids,
-                                     float* out) {
+                                     const float* codebook, float* out) {
   __shared__ float cb_s[16];
-  if (FMT == DA_KV_CB4 && threadIdx.x < 16) cb_s[threadIdx.x] = a.codebook[threadIdx.x];
+  if (is_codebook(S) && threadIdx.x < (S == kSideCB3 ? 8 : 16)) cb_s[threadIdx.x] = codebook[threadIdx.x];
   __syncthreads();
   const int i = blockIdx.x;
   const int phys = ids[i];
@@ -35,7 +35,7 @@ __global__ void debug_dequant_kernel(const Args a, const void* cache, const floa
     float x[8];
     if (phys >= 0 && phys < a.num_blocks) {
       const size_t crow = (size_t)phys * rows + rr;
-      KvFormat<FMT>::load8(cache, crow, a.D, col, row_scale<FMT>(scales, crow), cb_s, x);
+      SideFormat<S>::load8(cache, crow, a.D, col, side_scale<S>(scales, crow), cb_s, x);
     } else {
       if (c == 0) atomicOr(a.err, DA_DEVERR_BLOCK_ID);
 #pragma unroll
@@ -55,13 +55,15 @@ cudaError_t launch_debug_bounds(const Args& a, int32_t* bounds, cudaStream_t s) 
 }
 
 cudaError_t launch_debug_dequant(const Args& a, const void* cache, const float* scales, const int32_t* ids, int n,
-                                 float* out, cudaStream_t s) {
+                                 int which, float* out, cudaStream_t s) {
   if (n == 0) return cudaSuccess;
-  switch (a.fmt) {
-    case DA_KV_BF16: debug_dequant_kernel<DA_KV_BF16><<<n, 128, 0, s>>>(a, cache, scales, ids, out); break;
-    case DA_KV_FP8_E4M3: debug_dequant_kernel<DA_KV_FP8_E4M3><<<n, 128, 0, s>>>(a, cache, scales, ids, out); break;
-    case DA_KV_CB4: debug_dequant_kernel<DA_KV_CB4><<<n, 128, 0, s>>>(a, cache, scales, ids, out); break;
-    default: return cudaErrorInvalidValue;
+  const int side = which ? v_side(a.fmt) : k_side(a.fmt);
+  const float* cb = a.codebook + ((which && a.fmt == DA_KV_CB3K_CB4V) ? 8 : 0);
+  switch (side) {
+    case kSideBF16: debug_dequant_kernel<kSideBF16><<<n, 128, 0, s>>>(a, cache, scales, ids, cb, out); break;
+    case kSideFP8: debug_dequant_kernel<kSideFP8><<<n, 128, 0, s>>>(a, cache, scales, ids, cb, out); break;
+    case kSideCB3: debug_dequant_kernel<kSideCB3><<<n, 128, 0, s>>>(a, cache, scales, ids, cb, out); break;
+    default: debug_dequant_kernel<kSideCB4><<<n, 128, 0, s>>>(a, cache, scales, ids, cb, out); break;
   }
   return cudaGetLastError();
 }

@@ -12,6 +12,7 @@
 #include <cstdint>
 
 #include "da_internal.cuh"
+#include "kv_formats.cuh"
 
 using namespace da;
 
@@ -25,7 +26,7 @@ int check_params(const da_params* p) {
     return DA_ERR_INVALID_ARG;
   if (p->num_q_heads % p->num_kv_heads) return DA_ERR_INVALID_ARG;
   if (!std::isfinite(p->softmax_scale) || !std::isfinite(p->softcap) || p->softcap < 0.0f) return DA_ERR_INVALID_ARG;
-  if (p->kv_format < DA_KV_BF16 || p->kv_format > DA_KV_CB4) return DA_ERR_INVALID_ARG;
+  if (p->kv_format < DA_KV_BF16 || p->kv_format > DA_KV_CB3K_CB4V) return DA_ERR_INVALID_ARG;
   const int G = p->num_q_heads / p->num_kv_heads;
   if (G != 1 && G != 2 && G != 4 && G != 8) return DA_ERR_UNSUPPORTED;
   if (p->head_dim != 128 && p->head_dim != 256) return DA_ERR_UNSUPPORTED;
@@ -48,7 +49,8 @@ int check_tensors(const void* q, const void* k, const void* v, const float* ks, 
                   const float* sign, const int32_t* bt, const int32_t* lens, const float* out, const da_params* p) {
   if (!q || !k || !v || !bt || !lens || !out) return DA_ERR_INVALID_ARG;
   if (p->kv_format != DA_KV_BF16 && (!ks || !vs)) return DA_ERR_INVALID_ARG;
-  if (p->kv_format == DA_KV_CB4 && (!cb || !sign)) return DA_ERR_INVALID_ARG;
+  if ((is_codebook(k_side(p->kv_format)) || is_codebook(v_side(p->kv_format))) && (!cb || !sign))
+    return DA_ERR_INVALID_ARG;
   // vector loads: caches on 16-byte boundaries, q / out / scales on their element size
   if (!aligned(k, 16) || !aligned(v, 16) || !aligned(q, 16) || !aligned(out, 4) || !aligned(bt, 4) ||
       !aligned(lens, 4))
@@ -105,7 +107,8 @@ int run(int phases, const void* q, const void* k, const void* v, const float* ks
   if (p->batch == 0) return DA_OK;
   const Args a = make_args(q, k, v, ks, vs, cb, sign, bt, lens, out, p);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if ((phases & kRotate) && a.fmt == DA_KV_CB4 && launch_rotate_q(a, s) != cudaSuccess) return DA_ERR_LAUNCH;
+  if ((phases & kRotate) && is_codebook(k_side(a.fmt)) && launch_rotate_q(a, s) != cudaSuccess)
+    return DA_ERR_LAUNCH;
   if ((phases & kPartition) && launch_partition(a, s) != cudaSuccess) return DA_ERR_LAUNCH;
   if ((phases & kReduce) && launch_reduce(a, s) != cudaSuccess) return DA_ERR_LAUNCH;
   return DA_OK;
@@ -203,15 +206,21 @@ int decode_attn_encode_fp8(const float* x, int64_t n, uint8_t* codes, float* sca
              : DA_ERR_LAUNCH;
 }
 
-int decode_attn_encode_cb4(const float* x, int64_t num_vectors, int32_t head_dim, const float* sign_pattern,
-                           const float* codebook, uint8_t* packed, float* scales, void* stream) {
+int decode_attn_encode_codebook(const float* x, int64_t num_vectors, int32_t head_dim, int32_t bits,
+                                const float* sign_pattern, const float* codebook, uint8_t* packed, float* scales,
+                                void* stream) {
   if (num_vectors < 0 || (num_vectors > 0 && (!x || !sign_pattern || !codebook || !packed || !scales)))
     return DA_ERR_INVALID_ARG;
-  if (head_dim != 128 && head_dim != 256) return DA_ERR_UNSUPPORTED;
-  return launch_encode_cb4(x, num_vectors, head_dim, sign_pattern, codebook, packed, scales,
-                           static_cast<cudaStream_t>(stream)) == cudaSuccess
+  if ((head_dim != 128 && head_dim != 256) || (bits != 3 && bits != 4)) return DA_ERR_UNSUPPORTED;
+  return launch_encode_codebook(x, num_vectors, head_dim, bits, sign_pattern, codebook, packed, scales,
+                                static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? DA_OK
              : DA_ERR_LAUNCH;
+}
+
+int decode_attn_encode_cb4(const float* x, int64_t num_vectors, int32_t head_dim, const float* sign_pattern,
+                           const float* codebook, uint8_t* packed, float* scales, void* stream) {
+  return decode_attn_encode_codebook(x, num_vectors, head_dim, 4, sign_pattern, codebook, packed, scales, stream);
 }
 
 int decode_attn_codebook_lloyd_max(int32_t levels, double sigma, float* codebook_host) {
@@ -230,16 +239,19 @@ int decode_attn_debug_partition_bounds(const int32_t* context_lens, int32_t* bou
 }
 
 int decode_attn_debug_dequant_blocks(const void* cache, const float* scales, const float* codebook,
-                                     const int32_t* block_ids, int32_t n, float* out, const da_params* p,
-                                     void* stream) {
+                                     const int32_t* block_ids, int32_t n, int32_t which, float* out,
+                                     const da_params* p, void* stream) {
   int rc = check_params(p);
   if (rc) return rc;
   if ((rc = check_workspace(p))) return rc;
-  if (!cache || !block_ids || !out || n < 0 || !aligned(cache, 16)) return DA_ERR_INVALID_ARG;
-  if (p->kv_format != DA_KV_BF16 && !scales) return DA_ERR_INVALID_ARG;
-  if (p->kv_format == DA_KV_CB4 && !codebook) return DA_ERR_INVALID_ARG;
+  if (!cache || !block_ids || !out || n < 0 || !aligned(cache, 16) || (which != 0 && which != 1))
+    return DA_ERR_INVALID_ARG;
+  const int side = which ? v_side(p->kv_format) : k_side(p->kv_format);
+  if (side != kSideBF16 && !scales) return DA_ERR_INVALID_ARG;
+  if (is_codebook(side) && !codebook) return DA_ERR_INVALID_ARG;
   Args a = make_args(nullptr, nullptr, nullptr, nullptr, nullptr, codebook, nullptr, nullptr, nullptr, nullptr, p);
-  return launch_debug_dequant(a, cache, scales, block_ids, n, out, static_cast<cudaStream_t>(stream)) == cudaSuccess
+  return launch_debug_dequant(a, cache, scales, block_ids, n, which, out, static_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
              ? DA_OK
              : DA_ERR_LAUNCH;
 }

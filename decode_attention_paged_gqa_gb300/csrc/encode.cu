@@ -5,11 +5,11 @@
 // (E4M3)"): scale = amax|x| / 448 in binary32, code = round-to-nearest-even E4M3 of the
 // binary32 quotient x / scale, saturating at +-448.
 //
-// 4-bit codebook on a random-sign Walsh-Hadamard basis (same table, "Turbo4";
-// turboquant-rs 0.4.1, src/cache/cuda/attention.rs: codebook + sign_pattern inputs):
+// 4-bit and 3-bit codebooks on a random-sign Walsh-Hadamard basis (same table, "Turbo4" /
+// "Turbo3"; turboquant-rs 0.4.1, src/cache/cuda/attention.rs: codebook + sign_pattern):
 //   r = H diag(sign) x / sqrt(D), scale = ||x||_2 (stored as binary32),
 //   idx_d = nearest codebook value to r_d / scale (ties to the lower index),
-//   two indices per byte, coordinate 2k in the low nibble of byte k.
+//   codes packed as a little-endian bit stream (4 bits: coordinate 2k in the low nibble).
 // The norm and the rotation are computed in fp64 with the sums taken in index order, so
 // every code decision is made on the same fp64 value a plain sequential evaluation gives.
 #include <cuda_fp8.h>
@@ -45,17 +45,24 @@ __global__ void fp8_cast_kernel(const float* __restrict__ x, long long n, const 
     codes[i] = (uint8_t)__nv_cvt_float_to_fp8(__fdiv_rn(x[i], s), __NV_SATFINITE, __NV_E4M3);
 }
 
-// One warp per vector; lane l produces coordinates l, l + 32, ...
+// One warp per vector; lane l produces coordinates l, l + 32, ... Codes are gathered in
+// shared memory and packed as a little-endian bit stream of `bits`-bit codes (for 4 bits:
+// coordinate 2k in the low nibble of byte k).
 template <int D>
-__global__ void __launch_bounds__(128) cb4_encode_kernel(const float* __restrict__ x, long long nvec,
-                                                         const float* __restrict__ sign,
-                                                         const float* __restrict__ codebook,
-                                                         uint8_t* __restrict__ packed, float* __restrict__ scales) {
+__global__ void __launch_bounds__(128) codebook_encode_kernel(const float* __restrict__ x, long long nvec, int bits,
+                                                              const float* __restrict__ sign,
+                                                              const float* __restrict__ codebook,
+                                                              uint8_t* __restrict__ packed,
+                                                              float* __restrict__ scales) {
   __shared__ double xs_all[4][D];
+  __shared__ uint8_t codes_all[4][D];
   __shared__ float cb[16];
-  if (threadIdx.x < 16) cb[threadIdx.x] = codebook[threadIdx.x];
+  const int levels = 1 << bits;
+  if (threadIdx.x < levels) cb[threadIdx.x] = codebook[threadIdx.x];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   double* xs = xs_all[w];
+  uint8_t* codes = codes_all[w];
+  const int row_bytes = D * bits / 8;
   __syncthreads();
   for (long long v = blockIdx.x * 4ll + w; v < nvec; v += gridDim.x * 4ll) {
     const float* xv = x + v * D;
@@ -66,30 +73,30 @@ __global__ void __launch_bounds__(128) cb4_encode_kernel(const float* __restrict
     for (int k = 0; k < D; ++k) n2 += xs[k] * xs[k];
     const float scale = (float)sqrt(n2);
     const double inv = 1.0 / sqrt((double)D);
-    uint8_t idx[D / 32];
-#pragma unroll
-    for (int j = 0; j < D / 32; ++j) {
-      const int i = lane + 32 * j;
+    for (int i = lane; i < D; i += 32) {
       double acc = 0.0;
       for (int k = 0; k < D; ++k) acc += (__popc(i & k) & 1) ? -xs[k] : xs[k];  // H[i][k] sign[k] x[k]
       const double r = acc * inv;
       const double u = scale > 0.0f ? r / (double)scale : 0.0;
       int best = 0;
       double bd = fabs(u - (double)cb[0]);
-      for (int c = 1; c < 16; ++c) {
+      for (int c = 1; c < levels; ++c) {
         const double dd = fabs(u - (double)cb[c]);
         if (dd < bd) {
           bd = dd;
           best = c;
         }
       }
-      idx[j] = (uint8_t)best;
+      codes[i] = (uint8_t)best;
     }
-    // pack: coordinate 2k (even lane) low nibble, 2k + 1 (odd lane) high nibble
-#pragma unroll
-    for (int j = 0; j < D / 32; ++j) {
-      const unsigned other = __shfl_xor_sync(0xffffffffu, (unsigned)idx[j], 1);
-      if ((lane & 1) == 0) packed[v * (D / 2) + (lane + 32 * j) / 2] = (uint8_t)(idx[j] | (other << 4));
+    __syncwarp();
+    for (int byte = lane; byte < row_bytes; byte += 32) {
+      unsigned out = 0;
+      for (int bit = 0; bit < 8; ++bit) {
+        const int s = 8 * byte + bit;
+        out |= ((codes[s / bits] >> (s % bits)) & 1u) << bit;
+      }
+      packed[v * row_bytes + byte] = (uint8_t)out;
     }
     if (lane == 0) scales[v] = scale;
     __syncwarp();
@@ -121,14 +128,14 @@ cudaError_t launch_encode_fp8(const float* x, long long n, uint8_t* codes, float
   return cudaGetLastError();
 }
 
-cudaError_t launch_encode_cb4(const float* x, long long nvec, int D, const float* sign, const float* codebook,
-                              uint8_t* packed, float* scales, cudaStream_t s) {
+cudaError_t launch_encode_codebook(const float* x, long long nvec, int D, int bits, const float* sign,
+                                   const float* codebook, uint8_t* packed, float* scales, cudaStream_t s) {
   if (nvec == 0) return cudaSuccess;
   const int grid = (int)((nvec + 3) / 4 < 8192 ? (nvec + 3) / 4 : 8192);
   if (D == 128)
-    cb4_encode_kernel<128><<<grid, 128, 0, s>>>(x, nvec, sign, codebook, packed, scales);
+    codebook_encode_kernel<128><<<grid, 128, 0, s>>>(x, nvec, bits, sign, codebook, packed, scales);
   else
-    cb4_encode_kernel<256><<<grid, 128, 0, s>>>(x, nvec, sign, codebook, packed, scales);
+    codebook_encode_kernel<256><<<grid, 128, 0, s>>>(x, nvec, bits, sign, codebook, packed, scales);
   return cudaGetLastError();
 }
 

@@ -1,9 +1,9 @@
-// kv_formats.cuh -- in-register dequantisation of the three KV cache formats
-// (attention.rs README, KV Cache Formats table: BF16, FP8 E4M3, 4-bit Walsh-Hadamard
-// codebook). The codebook format is dequantised in its rotated basis only: the value of
-// coordinate d is scale_t * codebook[idx_d] (turboquant-rs 0.4.1, src/cache/cuda/
-// attention.rs: the fused kernel "reads directly from the compressed KV-cache (no full
-// dequantization needed)").
+// kv_formats.cuh -- in-register dequantisation of one side (K or V) of a KV cache
+// (attention.rs README, KV Cache Formats table: BF16, FP8 E4M3, and the 4-bit / 3-bit
+// Walsh-Hadamard codebook formats, alone or mixed as FP8 K + 4-bit V and 3-bit K +
+// 4-bit V). Codebook sides are dequantised in their rotated basis only: coordinate d is
+// scale_t * codebook[idx_d] (turboquant-rs 0.4.1, src/cache/cuda/attention.rs: the fused
+// kernel "reads directly from the compressed KV-cache (no full dequantization needed)").
 #pragma once
 
 #include <cuda_fp16.h>
@@ -13,13 +13,30 @@
 
 namespace da {
 
-template <int FMT>
-struct KvFormat;
+// storage of one side
+enum Side { kSideBF16 = 0, kSideFP8 = 1, kSideCB3 = 2, kSideCB4 = 3 };
+
+__host__ __device__ constexpr int k_side(int fmt) {
+  return fmt == DA_KV_BF16 ? kSideBF16
+         : fmt == DA_KV_FP8_E4M3 || fmt == DA_KV_FP8K_CB4V ? kSideFP8
+         : fmt == DA_KV_CB3K_CB4V ? kSideCB3
+                                  : kSideCB4;
+}
+__host__ __device__ constexpr int v_side(int fmt) {
+  return fmt == DA_KV_BF16 ? kSideBF16 : fmt == DA_KV_FP8_E4M3 ? kSideFP8 : kSideCB4;
+}
+__host__ __device__ constexpr bool is_codebook(int side) { return side == kSideCB3 || side == kSideCB4; }
+// bytes of one stored row (one token of one kv head)
+__host__ __device__ constexpr int row_bytes(int side, int D) {
+  return side == kSideBF16 ? 2 * D : side == kSideFP8 ? D : side == kSideCB3 ? 3 * D / 8 : D / 2;
+}
+
+template <int S>
+struct SideFormat;
 
 // bf16: the upper half of a binary32 word, converted exactly.
 template <>
-struct KvFormat<DA_KV_BF16> {
-  static constexpr int kBitsPerElem = 16;
+struct SideFormat<kSideBF16> {
   // 8 consecutive elements of cache row `row`, starting at column `col` (a multiple of 8).
   __device__ static __forceinline__ void load8(const void* cache, size_t row, int D, int col, float /*scale*/,
                                                const float* /*cb*/, float* x) {
@@ -34,10 +51,9 @@ struct KvFormat<DA_KV_BF16> {
 };
 
 // E4M3 -> f16 is exact (3 mantissa bits, exponents 2^-9 .. 2^8 fit f16); then one fp32
-// multiply by the tensor's dequant scale.
+// multiply by `scale` (the caller passes 1 to keep the values in code units).
 template <>
-struct KvFormat<DA_KV_FP8_E4M3> {
-  static constexpr int kBitsPerElem = 8;
+struct SideFormat<kSideFP8> {
   __device__ static __forceinline__ float2 e4m3x2_to_float2(uint32_t two_codes) {
     const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two_codes & 0xffffu), __NV_E4M3);
     return __half22float2(*reinterpret_cast<const __half2*>(&h));
@@ -61,8 +77,7 @@ struct KvFormat<DA_KV_FP8_E4M3> {
 // 4-bit codebook: byte k of a row holds coordinate 2k in its low nibble, 2k+1 in its high
 // nibble; value = scale_t * codebook[idx] (rotated basis).
 template <>
-struct KvFormat<DA_KV_CB4> {
-  static constexpr int kBitsPerElem = 4;
+struct SideFormat<kSideCB4> {
   __device__ static __forceinline__ void load8(const void* cache, size_t row, int D, int col, float scale,
                                                const float* cb, float* x) {
     const uint32_t v = __ldg(reinterpret_cast<const uint32_t*>(static_cast<const uint8_t*>(cache) + row * (D / 2) +
@@ -72,11 +87,25 @@ struct KvFormat<DA_KV_CB4> {
   }
 };
 
-// Per-row scale: fp8 has one per tensor, cb4 one per (block, kv head, slot), bf16 none.
-template <int FMT>
-__device__ __forceinline__ float row_scale(const float* scales, size_t row) {
-  if constexpr (FMT == DA_KV_FP8_E4M3) return __ldg(scales);
-  else if constexpr (FMT == DA_KV_CB4) return __ldg(scales + row);
+// 3-bit codebook: the codes form a little-endian bit stream, coordinate d at stream bits
+// [3d, 3d + 3); 8 coordinates starting at a multiple of 8 are the 3 bytes at 3 * col / 8.
+template <>
+struct SideFormat<kSideCB3> {
+  __device__ static __forceinline__ void load8(const void* cache, size_t row, int D, int col, float scale,
+                                               const float* cb, float* x) {
+    const uint8_t* p = static_cast<const uint8_t*>(cache) + row * (3 * D / 8) + 3 * (col / 8);
+    const uint32_t v = (uint32_t)__ldg(p) | ((uint32_t)__ldg(p + 1) << 8) | ((uint32_t)__ldg(p + 2) << 16);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) x[i] = scale * cb[(v >> (3 * i)) & 7u];
+  }
+};
+
+// Per-row scale: an FP8 side has one per tensor, a codebook side one per (block, kv head,
+// slot), bf16 none.
+template <int S>
+__device__ __forceinline__ float side_scale(const float* scales, size_t row) {
+  if constexpr (S == kSideFP8) return __ldg(scales);
+  else if constexpr (S == kSideCB3 || S == kSideCB4) return __ldg(scales + row);
   else return 1.0f;
 }
 

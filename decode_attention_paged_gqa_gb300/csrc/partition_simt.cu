@@ -1,5 +1,5 @@
 // partition_simt.cu -- split-K partition kernel on the CUDA cores (fp32 throughout), used
-// for the 4-bit codebook cache.
+// for the formats with a codebook side: 4-bit K and V, FP8 K + 4-bit V, 3-bit K + 4-bit V.
 //
 // One CTA per (partition p, kv head g, sequence b). It walks the partition's tokens in
 // tiles of 32: the tile's K and V rows are gathered through the block table, dequantised
@@ -48,16 +48,21 @@ __global__ void __launch_bounds__(kThreads) partition_simt_kernel(const Args a) 
   float* v_s = k_s + kTile * (D + 1);       // [kTile][D]
   float* p_s = v_s + kTile * D;             // [G][kTile]
   float* alpha_s = p_s + G * kTile;         // [G]
-  float* cb_s = alpha_s + G;                // [16]
-  int* ok_s = reinterpret_cast<int*>(cb_s + 16);  // [kTile]
+  float* cbk_s = alpha_s + G;               // [16] key codebook
+  float* cbv_s = cbk_s + 16;                // [16] value codebook
+  int* ok_s = reinterpret_cast<int*>(cbv_s + 16);  // [kTile]
+  constexpr int KS = k_side(FMT), VS = v_side(FMT);
 
-  // queries of the group (rotated ones for the codebook format)
+  // queries of the group (rotated ones when the keys are stored on the rotated basis)
   for (int i = tid; i < G * D; i += kThreads) {
     const int h = g * G + i / D, d = i % D;
     const size_t qi = ((size_t)b * a.Hq + h) * D + d;
-    q_s[i] = FMT == DA_KV_CB4 ? a.q_rot[qi] : bf16_to_f32(a.q[qi]);
+    q_s[i] = is_codebook(KS) ? a.q_rot[qi] : bf16_to_f32(a.q[qi]);
   }
-  if (FMT == DA_KV_CB4 && tid < 16) cb_s[tid] = __ldg(a.codebook + tid);
+  if (tid < 16) {
+    if (is_codebook(KS)) cbk_s[tid] = tid < (KS == kSideCB3 ? 8 : 16) ? __ldg(a.codebook + tid) : 0.0f;
+    if (is_codebook(VS)) cbv_s[tid] = __ldg(a.codebook + (KS == kSideCB3 ? 8 : 0) + tid);
+  }
 
   constexpr int kHeadsPerWarp = (G + 3) / 4;
   float m_run[kHeadsPerWarp], l_run[kHeadsPerWarp];
@@ -75,7 +80,7 @@ __global__ void __launch_bounds__(kThreads) partition_simt_kernel(const Args a) 
 
   constexpr int kChunks = D / 8;  // 8-element chunks per row
   for (int t0 = r.start; t0 < r.end; t0 += kTile) {
-    __syncthreads();  // previous tile fully consumed (and q_s / cb_s written on the first pass)
+    __syncthreads();  // previous tile fully consumed (and q_s / codebooks written on the first pass)
     for (int c = tid; c < kTile * kChunks; c += kThreads) {
       const int row = c / kChunks, col = (c % kChunks) * 8, t = t0 + row;
       float xk[8], xv[8];
@@ -85,8 +90,10 @@ __global__ void __launch_bounds__(kThreads) partition_simt_kernel(const Args a) 
         if (phys >= 0) {
           ok = true;
           const size_t crow = ((size_t)phys * a.Hkv + g) * a.bs + t % a.bs;
-          KvFormat<FMT>::load8(a.k_cache, crow, D, col, row_scale<FMT>(a.k_scales, crow), cb_s, xk);
-          KvFormat<FMT>::load8(a.v_cache, crow, D, col, row_scale<FMT>(a.v_scales, crow), cb_s, xv);
+          SideFormat<KS>::load8(a.k_cache, crow, D, col, side_scale<KS>(a.k_scales, crow), cbk_s, xk);
+          // an FP8 value side stays in code units; the reduce applies its scale once
+          SideFormat<VS>::load8(a.v_cache, crow, D, col, VS == kSideFP8 ? 1.0f : side_scale<VS>(a.v_scales, crow),
+                                cbv_s, xv);
         }
       }
       if (!ok) {
@@ -165,7 +172,8 @@ __global__ void __launch_bounds__(kThreads) partition_simt_kernel(const Args a) 
 
 template <int FMT, int D, int G>
 cudaError_t launch_fixed(const Args& a, cudaStream_t s) {
-  const size_t smem = sizeof(float) * (G * D + kTile * (D + 1) + kTile * D + G * kTile + G + 16) + sizeof(int) * kTile;
+  const size_t smem =
+      sizeof(float) * (G * D + kTile * (D + 1) + kTile * D + G * kTile + G + 32) + sizeof(int) * kTile;
   auto kern = partition_simt_kernel<FMT, D, G>;
   static DeviceFlags attr_set;
   cudaError_t e = ensure_dynamic_smem(kern, smem, attr_set);
@@ -194,12 +202,16 @@ cudaError_t launch_d(const Args& a, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_partition_simt(const Args& a, cudaStream_t s) {
-  if (a.fmt == DA_KV_CB4) return launch_d<DA_KV_CB4>(a, s);
+  switch (a.fmt) {
+    case DA_KV_CB4: return launch_d<DA_KV_CB4>(a, s);
+    case DA_KV_FP8K_CB4V: return launch_d<DA_KV_FP8K_CB4V>(a, s);
+    case DA_KV_CB3K_CB4V: return launch_d<DA_KV_CB3K_CB4V>(a, s);
+  }
   return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_partition(const Args& a, cudaStream_t s) {
-  return a.fmt == DA_KV_CB4 ? launch_partition_simt(a, s) : launch_partition_tc(a, s);
+  return a.fmt == DA_KV_BF16 || a.fmt == DA_KV_FP8_E4M3 ? launch_partition_tc(a, s) : launch_partition_simt(a, s);
 }
 
 }  // namespace da

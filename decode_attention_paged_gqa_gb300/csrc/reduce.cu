@@ -7,14 +7,15 @@
 //   M = max_p m_p,  w_p = 2^(m_p - M),  out = sum_p w_p o_p / sum_p w_p l_p.
 // An empty sequence gets an all-zero row. An unsplit BF16/FP8 sequence was written by the
 // partition kernel and is skipped here. For the codebook format the result is still in the
-// rotated basis and is un-rotated here: out <- diag(sign) H out / sqrt(D). For FP8 the
-// per-tensor V scale is applied once, to the result.
+// rotated basis and is un-rotated here when the values are stored on it: out <- diag(sign)
+// H out / sqrt(D). For an FP8 value side the per-tensor V scale is applied once, here.
 #include <cuda_runtime.h>
 
 #include <cmath>
 
 #include "da_internal.cuh"
 #include "fwht.cuh"
+#include "kv_formats.cuh"
 
 namespace da {
 namespace {
@@ -51,7 +52,7 @@ __global__ void __launch_bounds__(128) reduce_kernel(const Args a) {
     if (lane == 0) inv_l_s = lsum > 0.0f ? 1.0f / lsum : 0.0f;
   }
   __syncthreads();
-  const float inv_l = inv_l_s * (a.fmt == DA_KV_FP8_E4M3 ? __ldg(a.v_scales) : 1.0f);
+  const float inv_l = inv_l_s * (v_side(a.fmt) == kSideFP8 ? __ldg(a.v_scales) : 1.0f);
   for (int d = tid; d < D; d += blockDim.x) {
     float acc = 0.0f;
     for (int p = 0; p < np; ++p) acc = fmaf(w_s[p], a.part_o[(base + p) * D + d], acc);
@@ -71,7 +72,7 @@ template <int D>
 cudaError_t launch_d(const Args& a, cudaStream_t s) {
   dim3 grid(a.Hq, a.B);
   const size_t smem = sizeof(float) * (size_t)a.P;  // P <= kMaxPartitions: within the default 48 KB
-  if (a.fmt == DA_KV_CB4)
+  if (is_codebook(v_side(a.fmt)))
     reduce_kernel<D, true><<<grid, 128, smem, s>>>(a);
   else
     reduce_kernel<D, false><<<grid, 128, smem, s>>>(a);

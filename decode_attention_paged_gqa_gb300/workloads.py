@@ -33,7 +33,7 @@ class WorkloadSpec:
     num_q_heads: int
     num_kv_heads: int
     head_dim: int
-    kv_format: str             # "bf16" | "fp8" | "cb4"
+    kv_format: str             # "bf16" | "fp8" | "cb4" | "fp8k_cb4v" | "cb3k_cb4v"
     ctx_min: int               # context lengths are uniform integers in [ctx_min, ctx_max]
     ctx_max: int
     seed: int
@@ -66,6 +66,9 @@ WORKLOADS = {
                                          window=4096, softcap=50.0, softmax_scale=1.0 / 16.0),
     # 4-bit rotated-codebook cache, 32 sequences of 32768 tokens, 32/8 heads, D 128
     "cb4_long_32k": WorkloadSpec("cb4_long_32k", 32, 32, 8, 128, "cb4", 32768, 32768, seed=1005),
+    # the same batch with FP8 keys + 4-bit values, and with 3-bit keys + 4-bit values
+    "fp8k_cb4v_long_32k": WorkloadSpec("fp8k_cb4v_long_32k", 32, 32, 8, 128, "fp8k_cb4v", 32768, 32768, seed=1006),
+    "cb3k_cb4v_long_32k": WorkloadSpec("cb3k_cb4v_long_32k", 32, 32, 8, 128, "cb3k_cb4v", 32768, 32768, seed=1007),
 }
 
 

@@ -58,7 +58,15 @@ enum da_kv_format {
    * indices per byte, coordinate 2k in the low nibble of byte k; k_scales / v_scales are
    * [num_blocks][Hkv][block_size] fp32 norms; codebook is [16] fp32. The kernels rotate q
    * the same way, attend in the rotated basis and un-rotate the output once per head. */
-  DA_KV_CB4 = 2
+  DA_KV_CB4 = 2,
+  /* "Turbo8": keys as DA_KV_FP8_E4M3 (k_scales: one float), values as DA_KV_CB4 (v_scales:
+   * per-token norms; codebook: the 16 value levels). */
+  DA_KV_FP8K_CB4V = 3,
+  /* "Turbo3": keys as a 3-bit codebook on the same rotated basis (8 levels; the codes of a
+   * row form a little-endian bit stream, coordinate d at stream bits [3d, 3d+3), i.e. 3D/8
+   * bytes per row; k_scales: per-token norms), values as DA_KV_CB4. codebook holds the 8 key
+   * levels followed by the 16 value levels ([24] f32). */
+  DA_KV_CB3K_CB4V = 4
 };
 
 enum da_status {
@@ -112,9 +120,10 @@ int decode_attn_workspace_init(const da_params* p, void* stream);
  *   v_cache      the paged caches, layout by format (enum da_kv_format), 16-byte aligned;
  *                num_blocks * Hkv * block_size must stay below 2^31.
  *   k_scales,
- *   v_scales     FP8: one float each; CB4: [num_blocks][Hkv][block_size] f32; BF16: ignored (may be NULL).
- *   codebook     CB4: [16] f32; else ignored (may be NULL).
- *   sign_pattern CB4: [D] f32 of +1/-1; else ignored (may be NULL).
+ *   v_scales     per side: FP8 one float; codebook [num_blocks][Hkv][block_size] f32 norms;
+ *                BF16: ignored (may be NULL).
+ *   codebook     formats with a codebook side: [16] f32 (DA_KV_CB3K_CB4V: [8 + 16]); else ignored.
+ *   sign_pattern formats with a codebook side: [D] f32 of +1/-1; else ignored (may be NULL).
  *   block_tables [B][max_blocks_per_seq] int32: page i of sequence b lives in physical block
  *                block_tables[b][i]; token t of sequence b is slot t % block_size of page
  *                t / block_size. Only the pages holding attended tokens are read.
@@ -177,6 +186,13 @@ int decode_attn_encode_fp8(const float* x, int64_t n, uint8_t* codes, float* sca
 int decode_attn_encode_cb4(const float* x, int64_t num_vectors, int32_t head_dim, const float* sign_pattern,
                            const float* codebook, uint8_t* packed, float* scales, void* stream);
 
+/* The same for `bits`-bit codes (3 or 4) with a [2^bits] codebook; packed rows are
+ * head_dim * bits / 8 bytes holding the codes as a little-endian bit stream (coordinate d
+ * at stream bits [bits*d, bits*d + bits)). bits == 4 is decode_attn_encode_cb4. */
+int decode_attn_encode_codebook(const float* x, int64_t num_vectors, int32_t head_dim, int32_t bits,
+                                const float* sign_pattern, const float* codebook, uint8_t* packed, float* scales,
+                                void* stream);
+
 /* Host-side: the `levels`-level Lloyd-Max quantiser of N(0, sigma^2) (alternate midpoint
  * thresholds and conditional-mean levels until no level moves by 1e-14 sigma, then make it
  * exactly symmetric), written ascending as binary32 to codebook_host[levels]. The
@@ -192,11 +208,12 @@ int decode_attn_debug_partition_bounds(const int32_t* context_lens, int32_t* bou
                                        void* stream);
 
 /* out [n][Hkv][block_size][D] f32: the values the partition kernel computes from the cache
- * blocks block_ids[0..n) (device int32): BF16 exact; FP8 scale * e4m3(code) with scales[0];
- * CB4 scale_t * codebook[idx] in the rotated basis. */
+ * blocks block_ids[0..n) (device int32) of the K side (which == 0) or V side (which == 1) of
+ * the format: BF16 exact; FP8 scale * e4m3(code) with scales[0]; codebook sides
+ * scale_t * codebook[idx] in the rotated basis (codebook as in decode_attn_paged). */
 int decode_attn_debug_dequant_blocks(const void* cache, const float* scales, const float* codebook,
-                                     const int32_t* block_ids, int32_t n, float* out, const da_params* p,
-                                     void* stream);
+                                     const int32_t* block_ids, int32_t n, int32_t which, float* out,
+                                     const da_params* p, void* stream);
 
 #ifdef __cplusplus
 }

@@ -27,7 +27,10 @@ _SRC = os.path.join(_HERE, "oracle.c")
 _BUILD_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
 
-FMT = {"bf16": 0, "fp8": 1, "cb4": 2}
+FMT = {"bf16": 0, "fp8": 1, "cb4": 2, "fp8k_cb4v": 3, "cb3k_cb4v": 4}
+# (K side, V side) storage of each format
+SIDES = {"bf16": ("bf16", "bf16"), "fp8": ("fp8", "fp8"), "cb4": ("cb4", "cb4"), "fp8k_cb4v": ("fp8", "cb4"),
+         "cb3k_cb4v": ("cb3", "cb4")}
 ERRORS = {0: "ok", -1: "invalid argument", -2: "block-table entry out of range", -3: "out of memory"}
 
 _lib = None
@@ -91,6 +94,9 @@ def _open(path: str):
         "or_cb4_encode": (I, [P, I64, I, P, P, P, P, I]),
         "or_cb4_dequant_rotated": (None, [P, P, I64, I, P, P]),
         "or_cb4_dequant": (None, [P, P, I64, I, P, P, P]),
+        "or_cb_encode": (I, [I, P, I64, I, P, P, P, P, I]),
+        "or_cb_dequant_rotated": (None, [I, P, P, I64, I, P, P]),
+        "or_cb_dequant": (None, [I, P, P, I64, I, P, P, P]),
         "or_partition_bounds": (I, [I, I, I, I, P, P, I]),
         "or_default_threads": (I, []),
         "or_decode_attention": (I, [I, I, I, I, I, I, I, I, P, P, P, P, P, P, P, P, P, D, D, I, I, I, P, P, I,
@@ -182,6 +188,39 @@ def cb4_encode(x, sign, codebook, threads: int = 0):
     return packed, scales
 
 
+def cb_encode(bits, x, sign, codebook, threads: int = 0):
+    """b-bit codebook encoding of vectors x[..., D] -> (packed uint8 [..., D*bits/8], scales fp32)."""
+    a = _c(x, np.float32)
+    D = a.shape[-1]
+    nvec = a.size // D
+    packed = np.empty(a.shape[:-1] + (D * bits // 8,), dtype=np.uint8)
+    scales = np.empty(a.shape[:-1], dtype=np.float32)
+    rc = _load().or_cb_encode(int(bits), _ptr(a), nvec, D, _ptr(_c(sign, np.float32)),
+                              _ptr(_c(codebook, np.float32)), _ptr(packed), _ptr(scales), threads)
+    if rc:
+        raise ValueError(ERRORS.get(rc, rc))
+    return packed, scales
+
+
+def cb_dequant_rotated(bits, packed, scales, codebook) -> np.ndarray:
+    p = _c(packed, np.uint8)
+    s = _c(scales, np.float32)
+    D = p.shape[-1] * 8 // bits
+    out = np.empty(p.shape[:-1] + (D,), dtype=np.float64)
+    _load().or_cb_dequant_rotated(int(bits), _ptr(p), _ptr(s), s.size, D, _ptr(_c(codebook, np.float32)), _ptr(out))
+    return out
+
+
+def cb_dequant(bits, packed, scales, codebook, sign) -> np.ndarray:
+    p = _c(packed, np.uint8)
+    s = _c(scales, np.float32)
+    D = p.shape[-1] * 8 // bits
+    out = np.empty(p.shape[:-1] + (D,), dtype=np.float64)
+    _load().or_cb_dequant(int(bits), _ptr(p), _ptr(s), s.size, D, _ptr(_c(codebook, np.float32)),
+                          _ptr(_c(sign, np.float32)), _ptr(out))
+    return out
+
+
 def cb4_dequant_rotated(packed, scales, codebook) -> np.ndarray:
     """scale * codebook[idx] per coordinate, in the rotated basis (fp64)."""
     p = _c(packed, np.uint8)
@@ -231,6 +270,8 @@ def decode_attention(q_bits, k_cache, v_cache, block_tables, context_lens, *, kv
     kf = FMT[kv_format]
     kc = _c(k_cache, np.uint16 if kf == 0 else np.uint8)
     vc = _c(v_cache, np.uint16 if kf == 0 else np.uint8)
+    if k_scales is not None and SIDES[kv_format][0] == "fp8":
+        k_scales = np.atleast_1d(k_scales)
     num_blocks, hkv, bs = kc.shape[:3]
     if hkv != num_kv_heads:
         raise ValueError("cache head count does not match num_kv_heads")

@@ -33,6 +33,31 @@
 #define OR_FMT_BF16 0
 #define OR_FMT_FP8 1
 #define OR_FMT_CB4 2
+#define OR_FMT_FP8K_CB4V 3  /* "Turbo8": FP8 keys, 4-bit codebook values */
+#define OR_FMT_CB3K_CB4V 4  /* "Turbo3": 3-bit codebook keys, 4-bit codebook values */
+
+/* How one side (K or V) of a cache format is stored. */
+enum { OR_SIDE_BF16, OR_SIDE_FP8, OR_SIDE_CB3, OR_SIDE_CB4 };
+
+static int or_side(int fmt, int which) {
+  switch (fmt) {
+    case OR_FMT_BF16: return OR_SIDE_BF16;
+    case OR_FMT_FP8: return OR_SIDE_FP8;
+    case OR_FMT_CB4: return OR_SIDE_CB4;
+    case OR_FMT_FP8K_CB4V: return which ? OR_SIDE_CB4 : OR_SIDE_FP8;
+    default: return which ? OR_SIDE_CB4 : OR_SIDE_CB3;
+  }
+}
+
+/* Bytes of one stored row (one token of one kv head) of a side. */
+static int64_t or_side_row_bytes(int side, int D) {
+  switch (side) {
+    case OR_SIDE_BF16: return 2 * (int64_t)D;
+    case OR_SIDE_FP8: return D;
+    case OR_SIDE_CB3: return 3 * (int64_t)D / 8;
+    default: return D / 2;
+  }
+}
 
 #define OR_OK 0
 #define OR_ERR_ARG -1
@@ -259,6 +284,30 @@ int or_cb_nearest(double u, const float* codebook, int levels) {
   return best;
 }
 
+/* b-bit codes are packed as a little-endian bit stream: the code of coordinate d occupies
+ * stream bits [b*d, b*d + b), stream bit s being bit (s mod 8) of byte s / 8. For b = 4
+ * this puts coordinate 2k in the low nibble of byte k and 2k + 1 in the high nibble (the
+ * 4-bit config, step (4)). Reading for b = 3 (attention.rs README, "Turbo3": 3-bit K):
+ * the pages give no packing; this is the plainest one. */
+static int or_code_get(const uint8_t* vec, int bits, int d) {
+  int v = 0;
+  for (int i = 0; i < bits; ++i) {
+    int s = bits * d + i;
+    v |= ((vec[s >> 3] >> (s & 7)) & 1) << i;
+  }
+  return v;
+}
+
+static void or_code_put(uint8_t* vec, int bits, int d, int code) {
+  for (int i = 0; i < bits; ++i) {
+    int s = bits * d + i;
+    if ((code >> i) & 1)
+      vec[s >> 3] = (uint8_t)(vec[s >> 3] | (1u << (s & 7)));
+    else
+      vec[s >> 3] = (uint8_t)(vec[s >> 3] & ~(1u << (s & 7)));
+  }
+}
+
 typedef struct {
   const float* x;
   const float* sign;
@@ -266,19 +315,18 @@ typedef struct {
   const double* H;
   uint8_t* packed;
   float* scales;
-  int D;
-} or_cb4_job;
+  int D, bits;
+} or_cb_job;
 
 /* One vector: (1) r = H * diag(sign) * x / sqrt(D); (2) scale = ||x||_2 stored as
- * binary32; (3) idx_d = nearest codebook value to r_d / scale; (4) two indices per
- * byte, the even coordinate in the low nibble. A zero vector codes as r / scale = 0. */
-static void or_cb4_task(void* ctx, int64_t v) {
-  or_cb4_job* j = (or_cb4_job*)ctx;
-  int D = j->D, i, k;
+ * binary32; (3) idx_d = nearest of the 2^bits codebook values to r_d / scale; (4) the
+ * codes packed as a bit stream. A zero vector codes as r / scale = 0. */
+static void or_cb_task(void* ctx, int64_t v) {
+  or_cb_job* j = (or_cb_job*)ctx;
+  int D = j->D, bits = j->bits, i, k;
   const float* x = j->x + v * D;
   double norm2 = 0.0, r[1024], inv = 1.0 / sqrt((double)D);
   float scale;
-  uint8_t idx[1024];
   for (k = 0; k < D; ++k) norm2 += (double)x[k] * (double)x[k];
   scale = (float)sqrt(norm2);
   for (i = 0; i < D; ++i) {
@@ -286,16 +334,18 @@ static void or_cb4_task(void* ctx, int64_t v) {
     for (k = 0; k < D; ++k) acc += j->H[(int64_t)i * D + k] * (double)j->sign[k] * (double)x[k];
     r[i] = acc * inv;
   }
-  for (i = 0; i < D; ++i) idx[i] = (uint8_t)or_cb_nearest(scale > 0.0f ? r[i] / (double)scale : 0.0, j->codebook, 16);
-  for (k = 0; k < D / 2; ++k) j->packed[v * (D / 2) + k] = (uint8_t)(idx[2 * k] | (idx[2 * k + 1] << 4));
+  for (i = 0; i < D; ++i) {
+    double u = scale > 0.0f ? r[i] / (double)scale : 0.0;
+    or_code_put(j->packed + v * (D * bits / 8), bits, i, or_cb_nearest(u, j->codebook, 1 << bits));
+  }
   j->scales[v] = scale;
 }
 
-int or_cb4_encode(const float* x, int64_t nvec, int D, const float* sign, const float* codebook, uint8_t* packed,
-                  float* scales, int threads) {
-  or_cb4_job j;
+int or_cb_encode(int bits, const float* x, int64_t nvec, int D, const float* sign, const float* codebook,
+                 uint8_t* packed, float* scales, int threads) {
+  or_cb_job j;
   double* H;
-  if (D <= 0 || D > 1024 || (D & (D - 1))) return OR_ERR_ARG;
+  if (D <= 0 || D > 1024 || (D & (D - 1)) || D % 8 || bits < 1 || bits > 8) return OR_ERR_ARG;
   H = (double*)malloc(sizeof(double) * D * D);
   if (!H) return OR_ERR_NOMEM;
   or_hadamard(D, H);
@@ -306,24 +356,33 @@ int or_cb4_encode(const float* x, int64_t nvec, int D, const float* sign, const 
   j.packed = packed;
   j.scales = scales;
   j.D = D;
-  or_parallel_for(or_cb4_task, &j, nvec, threads);
+  j.bits = bits;
+  or_parallel_for(or_cb_task, &j, nvec, threads);
   free(H);
   return OR_OK;
 }
 
-/* Codebook value of coordinate d of a packed vector, times its scale: the
- * rotated-basis value scale * codebook[idx_d]. */
-static double or_cb4_rot_value(const uint8_t* packed_vec, int d, float scale, const float* codebook) {
-  uint8_t b = packed_vec[d >> 1];
-  int idx = (d & 1) ? (b >> 4) : (b & 15);
-  return (double)scale * (double)codebook[idx];
+int or_cb4_encode(const float* x, int64_t nvec, int D, const float* sign, const float* codebook, uint8_t* packed,
+                  float* scales, int threads) {
+  return or_cb_encode(4, x, nvec, D, sign, codebook, packed, scales, threads);
+}
+
+/* Rotated-basis value of coordinate d of a packed vector: scale * codebook[idx_d]. */
+static double or_cb_rot_value(const uint8_t* packed_vec, int bits, int d, float scale, const float* codebook) {
+  return (double)scale * (double)codebook[or_code_get(packed_vec, bits, d)];
 }
 
 /* Rotated-basis dequantisation of n packed vectors: out[v][d] = scale_v * cb[idx]. */
+void or_cb_dequant_rotated(int bits, const uint8_t* packed, const float* scales, int64_t nvec, int D,
+                           const float* codebook, double* out) {
+  for (int64_t v = 0; v < nvec; ++v)
+    for (int d = 0; d < D; ++d)
+      out[v * D + d] = or_cb_rot_value(packed + v * (D * bits / 8), bits, d, scales[v], codebook);
+}
+
 void or_cb4_dequant_rotated(const uint8_t* packed, const float* scales, int64_t nvec, int D, const float* codebook,
                             double* out) {
-  for (int64_t v = 0; v < nvec; ++v)
-    for (int d = 0; d < D; ++d) out[v * D + d] = or_cb4_rot_value(packed + v * (D / 2), d, scales[v], codebook);
+  or_cb_dequant_rotated(4, packed, scales, nvec, D, codebook, out);
 }
 
 /* Back to the original basis: x = diag(sign) * H * r / sqrt(D) (H * H = D * I). */
@@ -336,17 +395,22 @@ static void or_unrotate(const double* r, int D, const double* H, const float* si
   }
 }
 
-void or_cb4_dequant(const uint8_t* packed, const float* scales, int64_t nvec, int D, const float* codebook,
-                    const float* sign, double* out) {
+void or_cb_dequant(int bits, const uint8_t* packed, const float* scales, int64_t nvec, int D, const float* codebook,
+                   const float* sign, double* out) {
   double* H = (double*)malloc(sizeof(double) * D * D);
   double r[1024];
   if (!H) return;
   or_hadamard(D, H);
   for (int64_t v = 0; v < nvec; ++v) {
-    for (int d = 0; d < D; ++d) r[d] = or_cb4_rot_value(packed + v * (D / 2), d, scales[v], codebook);
+    for (int d = 0; d < D; ++d) r[d] = or_cb_rot_value(packed + v * (D * bits / 8), bits, d, scales[v], codebook);
     or_unrotate(r, D, H, sign, out + v * D);
   }
   free(H);
+}
+
+void or_cb4_dequant(const uint8_t* packed, const float* scales, int64_t nvec, int D, const float* codebook,
+                    const float* sign, double* out) {
+  or_cb_dequant(4, packed, scales, nvec, D, codebook, sign, out);
 }
 
 /* ------------------------------------------------------------------------- */
@@ -388,12 +452,12 @@ int or_partition_bounds(int L, int window, int partition_size, int split_thresho
 typedef struct {
   int B, Hq, Hkv, D, bs, fmt, num_blocks, max_blocks;
   const uint16_t* q;      /* bf16 bits [B][Hq][D] */
-  const void* k_cache;    /* [num_blocks][Hkv][bs][D] bf16 bits or e4m3 codes; cb4: [..][D/2] bytes */
+  const void* k_cache;    /* [num_blocks][Hkv][bs][row bytes of the side] */
   const void* v_cache;
-  const float* k_scales;  /* fp8: [1]; cb4: [num_blocks][Hkv][bs] */
+  const float* k_scales;  /* fp8 side: [1]; codebook side: [num_blocks][Hkv][bs] */
   const float* v_scales;
-  const float* codebook;  /* cb4: [16] */
-  const float* sign;      /* cb4: [D] of +-1 */
+  const float* codebook;  /* 4-bit: [16]; 3-bit keys: [8] key levels then [16] value levels */
+  const float* sign;      /* codebook formats: [D] of +-1 */
   const int32_t* block_tables; /* [B][max_blocks] */
   const int32_t* context_lens; /* [B] */
   double scale, softcap;
@@ -407,25 +471,30 @@ typedef struct {
 } or_attn_job;
 
 /* Dequantise token `t` of kv head g of sequence b (K if which == 0, else V) into x[D],
- * gathered through the block table: page t / bs, slot t % bs. */
+ * gathered through the block table: page t / bs, slot t % bs. Codebook sides are
+ * decoded in their rotated basis and taken back to the original one with the dense H.
+ * Codebooks: 4-bit formats use codebook[0..15]; the 3-bit-key format stores its 8 key
+ * levels first and the 16 value levels after them. */
 static int or_token(const or_attn_job* j, int b, int g, int t, int which, double* x) {
-  int D = j->D, bs = j->bs, d;
+  int D = j->D, bs = j->bs, d, side = or_side(j->fmt, which);
   int32_t phys = j->block_tables[(int64_t)b * j->max_blocks + t / bs];
   int64_t row;
+  const uint8_t* base = (const uint8_t*)(which ? j->v_cache : j->k_cache);
   if (phys < 0 || phys >= j->num_blocks) return OR_ERR_BLOCK;
   row = ((int64_t)phys * j->Hkv + g) * bs + t % bs; /* layout [num_blocks][Hkv][bs][...] */
-  if (j->fmt == OR_FMT_BF16) {
-    const uint16_t* c = (const uint16_t*)(which ? j->v_cache : j->k_cache) + row * D;
+  base += row * or_side_row_bytes(side, D);
+  if (side == OR_SIDE_BF16) {
+    const uint16_t* c = (const uint16_t*)base;
     for (d = 0; d < D; ++d) x[d] = or_bf16_decode(c[d]);
-  } else if (j->fmt == OR_FMT_FP8) {
-    const uint8_t* c = (const uint8_t*)(which ? j->v_cache : j->k_cache) + row * D;
+  } else if (side == OR_SIDE_FP8) {
     double s = (double)(which ? j->v_scales[0] : j->k_scales[0]);
-    for (d = 0; d < D; ++d) x[d] = s * or_e4m3_decode(c[d]);
+    for (d = 0; d < D; ++d) x[d] = s * or_e4m3_decode(base[d]);
   } else {
-    const uint8_t* c = (const uint8_t*)(which ? j->v_cache : j->k_cache) + row * (D / 2);
+    int bits = side == OR_SIDE_CB3 ? 3 : 4;
+    const float* cb = j->codebook + ((j->fmt == OR_FMT_CB3K_CB4V && which) ? 8 : 0);
     float sc = (which ? j->v_scales : j->k_scales)[row];
     double r[1024];
-    for (d = 0; d < D; ++d) r[d] = or_cb4_rot_value(c, d, sc, j->codebook);
+    for (d = 0; d < D; ++d) r[d] = or_cb_rot_value(base, bits, d, sc, cb);
     or_unrotate(r, D, j->H, j->sign, x);
   }
   return OR_OK;
@@ -542,7 +611,8 @@ int or_decode_attention(int B, int Hq, int Hkv, int D, int block_size, int fmt, 
   int64_t nu = 0, b, g, hh;
   int used;
   if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || D <= 0 || D > 1024 || block_size <= 0) return OR_ERR_ARG;
-  if (fmt == OR_FMT_CB4 && (D & (D - 1))) return OR_ERR_ARG;
+  if (fmt < OR_FMT_BF16 || fmt > OR_FMT_CB3K_CB4V) return OR_ERR_ARG;
+  if (fmt >= OR_FMT_CB4 && (D & (D - 1))) return OR_ERR_ARG;
   memset(&j, 0, sizeof j);
   if (!out_row) {
     rows = (int32_t*)malloc(sizeof(int32_t) * (size_t)(B * Hq + 1));
@@ -552,11 +622,11 @@ int or_decode_attention(int B, int Hq, int Hkv, int D, int block_size, int fmt, 
   }
   j.unit_b = (int32_t*)malloc(sizeof(int32_t) * (size_t)(B * Hkv + 1));
   j.unit_g = (int32_t*)malloc(sizeof(int32_t) * (size_t)(B * Hkv + 1));
-  if (fmt == OR_FMT_CB4) {
+  if (fmt >= OR_FMT_CB4) {
     H = (double*)malloc(sizeof(double) * D * D);
     if (H) or_hadamard(D, H);
   }
-  if (!j.unit_b || !j.unit_g || (fmt == OR_FMT_CB4 && !H)) {
+  if (!j.unit_b || !j.unit_g || (fmt >= OR_FMT_CB4 && !H)) {
     free(rows);
     free(j.unit_b);
     free(j.unit_g);

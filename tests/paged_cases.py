@@ -26,21 +26,25 @@ def make_case(spec: wl.WorkloadSpec, layout: wl.PagedLayout | None = None) -> di
     nb = lay.num_blocks
     c = dict(spec=spec, lens=lay.context_lens, bt=lay.block_tables, num_blocks=nb, q=wl.make_query(spec),
              k_scales=None, v_scales=None, codebook=None, sign=None)
-    if spec.kv_format == "bf16":
-        c["k"] = wl.kv_bf16(spec, "k", nb)
-        c["v"] = wl.kv_bf16(spec, "v", nb)
-    elif spec.kv_format == "fp8":
-        for w in ("k", "v"):
-            codes, s = oracle.fp8_quantize(wl.kv_source(spec, w, nb).numpy())
+    k_side, v_side = oracle.SIDES[spec.kv_format]
+    if "cb3" in (k_side, v_side) or "cb4" in (k_side, v_side):
+        D = spec.head_dim
+        cb16 = oracle.lloyd_max(16, 1.0 / math.sqrt(D))[1]
+        cb8 = oracle.lloyd_max(8, 1.0 / math.sqrt(D))[1]
+        c["codebook"] = torch.from_numpy(np.concatenate([cb8, cb16]) if k_side == "cb3" else cb16)
+        c["sign"] = wl.sign_pattern(spec)
+    for w, side in (("k", k_side), ("v", v_side)):
+        if side == "bf16":
+            c[w] = wl.kv_bf16(spec, w, nb)
+            continue
+        src = wl.kv_source(spec, w, nb).numpy()
+        if side == "fp8":
+            codes, s = oracle.fp8_quantize(src)
             c[w] = torch.from_numpy(codes)
             c[w + "_scales"] = torch.tensor([s], dtype=torch.float32)
-    else:
-        _, cb, _ = oracle.lloyd_max(16, 1.0 / math.sqrt(spec.head_dim))
-        sg = wl.sign_pattern(spec)
-        c["codebook"] = torch.from_numpy(cb)
-        c["sign"] = sg
-        for w in ("k", "v"):
-            packed, scales = oracle.cb4_encode(wl.kv_source(spec, w, nb).numpy(), sg.numpy(), cb)
+        else:
+            bits = 3 if side == "cb3" else 4
+            packed, scales = oracle.cb_encode(bits, src, c["sign"].numpy(), cb8 if bits == 3 else cb16)
             c[w] = torch.from_numpy(packed)
             c[w + "_scales"] = torch.from_numpy(scales)
     return c
@@ -91,8 +95,8 @@ def run_oracle(c: dict, select=None, **override) -> np.ndarray:
     kw = dict(kv_format=s.kv_format, num_kv_heads=s.num_kv_heads, softmax_scale=s.scale, softcap=s.softcap,
               window=s.window, partition_size=s.partition_size, split_threshold=s.split_threshold)
     kw.update(override)
-    k = u16(c["k"]) if s.kv_format == "bf16" else c["k"].numpy()
-    v = u16(c["v"]) if s.kv_format == "bf16" else c["v"].numpy()
+    k = u16(c["k"]) if c["k"].dtype == torch.bfloat16 else c["k"].numpy()
+    v = u16(c["v"]) if c["v"].dtype == torch.bfloat16 else c["v"].numpy()
 
     def np_or_none(t):
         return None if t is None else t.numpy()

@@ -55,7 +55,7 @@ def test_partition_bounds_match_oracle(window, psize, thresh):
             assert tuple(got[b, i]) == exp, (int(L), i)
 
 
-@pytest.mark.parametrize("fmt", ["bf16", "fp8", "cb4"])
+@pytest.mark.parametrize("fmt", ["bf16", "fp8", "cb4", "fp8k_cb4v", "cb3k_cb4v"])
 @pytest.mark.parametrize("D", [128, 256])
 def test_dequant_blocks_bitwise(fmt, D):
     spec = wl.WorkloadSpec("deq", 3, 8, 4, D, fmt, 200, 300, seed=D)
@@ -65,19 +65,23 @@ def test_dequant_blocks_bitwise(fmt, D):
     ws = _ws(p)
     ids = torch.tensor([0, 5, c["num_blocks"] - 1, 2], dtype=torch.int32, device="cuda")
     out = torch.empty((4, spec.num_kv_heads, 16, D), dtype=torch.float32, device="cuda")
-    for which in ("k", "v"):
-        da.decode_attn_debug_dequant_blocks(dev[which], dev[which + "_scales"], dev["codebook"], ids, 4, out, p)
+    sides = oracle.SIDES[fmt]
+    for which, w in enumerate(("k", "v")):
+        da.decode_attn_debug_dequant_blocks(dev[w], dev[w + "_scales"], dev["codebook"], ids, 4, which, out, p)
         got = out.cpu().numpy()
         sel = ids.cpu().numpy()
-        if fmt == "bf16":
-            ref = oracle.bf16_decode(u16(c[which])[sel])
-        elif fmt == "fp8":
-            ref = oracle.e4m3_decode(c[which].numpy()[sel]) * float(c[which + "_scales"][0])
+        side = sides[which]
+        if side == "bf16":
+            ref = oracle.bf16_decode(u16(c[w])[sel])
+        elif side == "fp8":
+            ref = oracle.e4m3_decode(c[w].numpy()[sel]) * float(c[w + "_scales"][0])
         else:
-            ref = oracle.cb4_dequant_rotated(c[which].numpy()[sel], c[which + "_scales"].numpy()[sel],
-                                             c["codebook"].numpy())
+            bits = 3 if side == "cb3" else 4
+            cb = c["codebook"].numpy()
+            cb = cb[8:] if (fmt == "cb3k_cb4v" and which == 1) else cb
+            ref = oracle.cb_dequant_rotated(bits, c[w].numpy()[sel], c[w + "_scales"].numpy()[sel], cb)
         # one fp32 rounding of an exact product on both sides
-        assert np.array_equal(got, ref.astype(np.float32)), which
+        assert np.array_equal(got, ref.astype(np.float32)), w
     assert da.decode_attn_get_device_error(p) == 0
 
 

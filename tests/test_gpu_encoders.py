@@ -71,3 +71,19 @@ def test_cb4_encoder_bit_exact(D):
 def test_cb4_encoder_rejects_bad_head_dim():
     with pytest.raises(da.DecodeAttnError):
         da.decode_attn_encode_cb4(256, 1, 96, 256, 256, 256, 256)
+
+
+@pytest.mark.parametrize("D", [128, 256])
+def test_three_bit_encoder_bit_exact(D):
+    spec = wl.WorkloadSpec("enc3", 2, 8, 4, D, "cb3k_cb4v", 100, 300, seed=D + 1)
+    lay = wl.make_layout(spec)
+    x = wl.kv_source(spec, "k", lay.num_blocks)
+    sg = wl.sign_pattern(spec)
+    cb8 = oracle.lloyd_max(8, 1.0 / math.sqrt(D))[1]
+    packed_ref, scales_ref = oracle.cb_encode(3, x.numpy(), sg.numpy(), cb8)
+    nvec = x.numel() // D
+    packed = torch.empty(x.shape[:-1] + (3 * D // 8,), dtype=torch.uint8, device="cuda")
+    scales = torch.empty(x.shape[:-1], dtype=torch.float32, device="cuda")
+    da.decode_attn_encode_codebook(x.cuda(), nvec, D, 3, sg.cuda(), torch.from_numpy(cb8).cuda(), packed, scales)
+    assert np.array_equal(scales.cpu().numpy(), scales_ref)
+    assert np.array_equal(packed.cpu().numpy(), packed_ref)

@@ -42,7 +42,7 @@ def test_tiny_bf16_unsplit_and_split():
     assert_close(run_gpu(c, partition_size=512, split_threshold=1), ref, "tiny split forced")
 
 
-@pytest.mark.parametrize("fmt", ["bf16", "fp8", "cb4"])
+@pytest.mark.parametrize("fmt", ["bf16", "fp8", "cb4", "fp8k_cb4v", "cb3k_cb4v"])
 @pytest.mark.parametrize("D", [128, 256])
 @pytest.mark.parametrize("G", [1, 2, 4, 8])
 def test_edge_lengths(fmt, D, G):
@@ -51,7 +51,7 @@ def test_edge_lengths(fmt, D, G):
     assert_close(run_gpu(c), run_oracle(c), f"{fmt} D{D} G{G}")
 
 
-@pytest.mark.parametrize("fmt", ["bf16", "fp8", "cb4"])
+@pytest.mark.parametrize("fmt", ["bf16", "fp8", "cb4", "fp8k_cb4v", "cb3k_cb4v"])
 @pytest.mark.parametrize("window,softcap", [(100, 0.0), (1000, 0.0), (1024, 30.0), (0, 5.0), (4096, 50.0)])
 def test_window_and_softcap(fmt, window, softcap):
     spec, lay = small_spec(fmt, 128, 4, window=window, softcap=softcap, lens=EDGE_LENS + [4097, 5000], seed=window)

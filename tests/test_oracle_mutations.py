@@ -20,8 +20,8 @@ MUTATIONS = [
      "int start = (j->window > 0 && L > j->window) ? L - j->window + 1 : 0;"),
     ("page slot off by one", "row = ((int64_t)phys * j->Hkv + g) * bs + t % bs;",
      "row = ((int64_t)phys * j->Hkv + g) * bs + (t + 1) % bs;"),
-    ("K and V swapped", "const uint16_t* c = (const uint16_t*)(which ? j->v_cache : j->k_cache) + row * D;",
-     "const uint16_t* c = (const uint16_t*)(which ? j->k_cache : j->v_cache) + row * D;"),
+    ("K and V swapped", "const uint8_t* base = (const uint8_t*)(which ? j->v_cache : j->k_cache);",
+     "const uint8_t* base = (const uint8_t*)(which ? j->k_cache : j->v_cache);"),
     ("partition weights dropped from the sum", "Lsum += lp[i] * w;", "Lsum += lp[i];"),
     ("partition outputs not rescaled", "out[d] += o[(int64_t)i * D + d] * w;", "out[d] += o[(int64_t)i * D + d];"),
     ("partition boundary off by one",
@@ -31,11 +31,13 @@ MUTATIONS = [
     ("e4m3 rounding half up", "r = nearbyint(q);", "r = floor(q + 0.5);"),
     ("e4m3 subnormal step", "v = ldexp((double)m, -9);", "v = ldexp((double)m, -10);"),
     ("fp8 scale not applied", "double s = (double)(which ? j->v_scales[0] : j->k_scales[0]);", "double s = 1.0;"),
-    ("nibble order swapped", "int idx = (d & 1) ? (b >> 4) : (b & 15);", "int idx = (d & 1) ? (b & 15) : (b >> 4);"),
+    ("bit order within a byte reversed", "v |= ((vec[s >> 3] >> (s & 7)) & 1) << i;",
+     "v |= ((vec[s >> 3] >> (7 - (s & 7))) & 1) << i;"),
     ("un-rotation without the signs", "x[i] = (double)sign[i] * acc * inv;", "x[i] = acc * inv;"),
     ("hadamard transposed sign", "? -1.0 : 1.0;", "? 1.0 : -1.0;"),
     ("codebook ties to the upper index", "    if (d < bd) {", "    if (d <= bd) {"),
-    ("cb4 coordinates not normalised", "scale > 0.0f ? r[i] / (double)scale : 0.0", "r[i]"),
+    ("codebook coordinates not normalised", "double u = scale > 0.0f ? r[i] / (double)scale : 0.0;",
+     "double u = r[i];"),
     ("lloyd-max threshold not the midpoint", "for (i = 1; i < L; ++i) t[i] = 0.5 * (c[i - 1] + c[i]);",
      "for (i = 1; i < L; ++i) t[i] = c[i];"),
     ("bf16 decoded from the wrong half", "uint32_t w = (uint32_t)bits << 16;", "uint32_t w = (uint32_t)bits << 15;"),

@@ -98,8 +98,9 @@ def _open(path: str):
         "or_cb_dequant_rotated": (None, [I, P, P, I64, I, P, P]),
         "or_cb_dequant": (None, [I, P, P, I64, I, P, P, P]),
         "or_partition_bounds": (I, [I, I, I, I, P, P, I]),
+        "or_partition_bounds_multi": (I, [I, I, I, I, I, P, P, I]),
         "or_default_threads": (I, []),
-        "or_decode_attention": (I, [I, I, I, I, I, I, I, I, P, P, P, P, P, P, P, P, P, D, D, I, I, I, P, P, I,
+        "or_decode_attention": (I, [I, I, I, I, I, I, I, I, I, P, P, P, P, P, P, P, P, P, D, D, I, I, I, P, P, I,
                                     ctypes.POINTER(ctypes.c_int)]),
     }
     for name, (res, args) in sig.items():
@@ -243,13 +244,19 @@ def cb4_dequant(packed, scales, codebook, sign) -> np.ndarray:
 
 
 # ---------------------------------------------------------------- attention
-def partition_bounds(L: int, window: int = 0, partition_size: int = 512, split_threshold: int = 1024):
-    """[(start, end), ...] of the partitions of one sequence of length L."""
+def partition_bounds(L: int, window: int = 0, partition_size: int = 512, split_threshold: int = 1024,
+                     query_len: int = 1):
+    """[(start, end), ...] of the partitions of one sequence of length L with query_len
+    query tokens (the last query_len positions)."""
     cap = 1 << 16
     st = np.empty(cap, dtype=np.int32)
     en = np.empty(cap, dtype=np.int32)
-    n = _load().or_partition_bounds(int(L), int(window), int(partition_size), int(split_threshold), _ptr(st),
-                                    _ptr(en), cap)
+    if query_len == 1:
+        n = _load().or_partition_bounds(int(L), int(window), int(partition_size), int(split_threshold), _ptr(st),
+                                        _ptr(en), cap)
+    else:
+        n = _load().or_partition_bounds_multi(int(L), int(query_len), int(window), int(partition_size),
+                                              int(split_threshold), _ptr(st), _ptr(en), cap)
     return [(int(st[i]), int(en[i])) for i in range(n)]
 
 
@@ -259,14 +266,19 @@ def decode_attention(q_bits, k_cache, v_cache, block_tables, context_lens, *, kv
                      select=None, threads: int = 0, return_threads: bool = False):
     """fp64 paged GQA decode attention.
 
-    q_bits: uint16 bf16 bit patterns [B, Hq, D]. Caches: [num_blocks, Hkv, bs, D] uint16
+    q_bits: uint16 bf16 bit patterns [B, Hq, D], or [B, T, Hq, D] for T query tokens per
+    sequence (positions L-T .. L-1, causal). Caches: [num_blocks, Hkv, bs, D] uint16
     (bf16 bits) or uint8 (E4M3 codes), or [num_blocks, Hkv, bs, D/2] uint8 (packed 4-bit).
     k_scales/v_scales: fp8 -> one value each; cb4 -> [num_blocks, Hkv, bs] fp32.
-    select: optional list of (b, h); then the result is [len(select), D] in that order,
-    else [B, Hq, D]. partition_size 0 computes without partitions.
+    select: optional list of (b, h) (or (b, j, h) with T query tokens); then the result is
+    [len(select), D] in that order, else [B, Hq, D] (or [B, T, Hq, D]). partition_size 0
+    computes without partitions.
     """
     q = _c(q_bits, np.uint16)
-    B, Hq, D = q.shape
+    multi = q.ndim == 4
+    if not multi:
+        q = q[:, None]
+    B, T, Hq, D = q.shape
     kf = FMT[kv_format]
     kc = _c(k_cache, np.uint16 if kf == 0 else np.uint8)
     vc = _c(v_cache, np.uint16 if kf == 0 else np.uint8)
@@ -281,20 +293,24 @@ def decode_attention(q_bits, k_cache, v_cache, block_tables, context_lens, *, kv
     vs = _c(np.atleast_1d(v_scales), np.float32) if v_scales is not None else None
     if select is None:
         rows = None
-        out = np.zeros((B, Hq, D), dtype=np.float64)
+        out = np.zeros((B, T, Hq, D), dtype=np.float64)
     else:
-        rows = np.full(B * Hq, -1, dtype=np.int32)
-        for i, (b, h) in enumerate(select):
-            if rows[b * Hq + h] >= 0:
-                raise ValueError("duplicate (b, h) in select")
-            rows[b * Hq + h] = i
+        rows = np.full(B * T * Hq, -1, dtype=np.int32)
+        for i, key in enumerate(select):
+            b, jq, h = key if len(key) == 3 else (key[0], 0, key[1])
+            r = (b * T + jq) * Hq + h
+            if rows[r] >= 0:
+                raise ValueError("duplicate entry in select")
+            rows[r] = i
         out = np.zeros((len(select), D), dtype=np.float64)
     used = ctypes.c_int(0)
     rc = _load().or_decode_attention(
-        B, Hq, num_kv_heads, D, bs, kf, num_blocks, bt.shape[1], _ptr(q), _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs),
+        B, T, Hq, num_kv_heads, D, bs, kf, num_blocks, bt.shape[1], _ptr(q), _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs),
         _ptr(_c(codebook, np.float32)), _ptr(_c(sign_pattern, np.float32)), _ptr(bt), _ptr(cl),
         float(softmax_scale), float(softcap), int(window), int(partition_size), int(split_threshold), _ptr(rows),
         _ptr(out), int(threads), ctypes.byref(used))
     if rc:
         raise ValueError(f"oracle: {ERRORS.get(rc, rc)}")
+    if select is None and not multi:
+        out = out[:, 0]
     return (out, used.value) if return_threads else out

@@ -417,17 +417,13 @@ void or_cb4_dequant(const uint8_t* packed, const float* scales, int64_t nvec, in
 /* Partition bounds                                                          */
 /* ------------------------------------------------------------------------- */
 
-/* The attended positions of a sequence of length L are [start, L) with
- * start = max(0, L - window) when a window is set (only the last `window` tokens),
- * else 0. The sequence is split iff partition_size > 0 and the attended length
- * n = L - start is at least split_threshold; then partition p covers
- * [start + p * partition_size, min(start + (p + 1) * partition_size, L)) and
- * there are ceil(n / partition_size) of them; otherwise one range [start, L).
- * Reading: partitions are counted from the window start. An empty sequence has
- * no range. Writes up to `cap` (start, end) pairs; returns the count. */
-int or_partition_bounds(int L, int window, int partition_size, int split_threshold, int32_t* starts, int32_t* ends,
-                        int cap) {
-  int start = (window > 0 && L > window) ? L - window : 0;
+/* Partitions of the attended span [start, L): the span is split iff partition_size > 0
+ * and its length n = L - start is at least split_threshold; then partition p covers
+ * [start + p * partition_size, min(start + (p + 1) * partition_size, L)) and there are
+ * ceil(n / partition_size) of them; otherwise one range [start, L). An empty span has no
+ * range. Writes up to `cap` (start, end) pairs; returns the count. */
+int or_partition_bounds_span(int start, int L, int partition_size, int split_threshold, int32_t* starts, int32_t* ends,
+                             int cap) {
   int n = L - start, count, p;
   if (n <= 0) return 0;
   if (partition_size > 0 && n >= split_threshold) {
@@ -445,13 +441,38 @@ int or_partition_bounds(int L, int window, int partition_size, int split_thresho
   return 1;
 }
 
+/* First position attended by a query token at position `pos`: with a window of W tokens
+ * only positions t with pos - W < t <= pos are attended (reading: "only the last W tokens"
+ * of the context seen by that query, W of them including itself); else all t <= pos. */
+static int or_window_start(int pos, int window) {
+  int a = window > 0 ? pos + 1 - window : 0;
+  return a > 0 ? a : 0;
+}
+
+/* Single query token (the last position, L - 1): attended positions [start, L) with
+ * start = max(0, L - window) when a window is set, else 0; partitions counted from the
+ * window start. */
+int or_partition_bounds(int L, int window, int partition_size, int split_threshold, int32_t* starts, int32_t* ends,
+                        int cap) {
+  return or_partition_bounds_span(or_window_start(L - 1, window), L, partition_size, split_threshold, starts, ends,
+                                  cap);
+}
+
+/* T query tokens (multi-token decode): the grid spans every position attended by any of
+ * them, from the first query token's window start to L. */
+int or_partition_bounds_multi(int L, int T, int window, int partition_size, int split_threshold, int32_t* starts,
+                              int32_t* ends, int cap) {
+  return or_partition_bounds_span(or_window_start(L - T, window), L, partition_size, split_threshold, starts, ends,
+                                  cap);
+}
+
 /* ------------------------------------------------------------------------- */
 /* Paged GQA decode attention                                                */
 /* ------------------------------------------------------------------------- */
 
 typedef struct {
-  int B, Hq, Hkv, D, bs, fmt, num_blocks, max_blocks;
-  const uint16_t* q;      /* bf16 bits [B][Hq][D] */
+  int B, T, Hq, Hkv, D, bs, fmt, num_blocks, max_blocks;
+  const uint16_t* q;      /* bf16 bits [B][T][Hq][D] */
   const void* k_cache;    /* [num_blocks][Hkv][bs][row bytes of the side] */
   const void* v_cache;
   const float* k_scales;  /* fp8 side: [1]; codebook side: [num_blocks][Hkv][bs] */
@@ -462,7 +483,7 @@ typedef struct {
   const int32_t* context_lens; /* [B] */
   double scale, softcap;
   int window, partition_size, split_threshold;
-  const int32_t* out_row; /* [B*Hq]: output row of (b, h), or -1 when not requested */
+  const int32_t* out_row; /* [B*T*Hq]: output row of (b, j, h), or -1 when not requested */
   double* out;            /* [rows][D] */
   const double* H;        /* D x D Sylvester matrix (cb4) */
   int32_t* unit_b;        /* work units: (b, kv head g) with at least one requested head */
@@ -516,12 +537,14 @@ static void or_softmax_pv(const double* s, const double* V, int n, int D, double
   *l_out = l;
 }
 
+/* One (sequence b, kv head g) unit: every requested query head of the group, for every
+ * query token j (position L - T + j; T = 1 is ordinary decode). */
 static void or_attn_task(void* ctx, int64_t u) {
   or_attn_job* j = (or_attn_job*)ctx;
-  int b = j->unit_b[u], g = j->unit_g[u], D = j->D, G = j->Hq / j->Hkv;
+  int b = j->unit_b[u], g = j->unit_g[u], D = j->D, G = j->Hq / j->Hkv, T = j->T;
   int L = j->context_lens[b];
-  int start = (j->window > 0 && L > j->window) ? L - j->window : 0;
-  int n = L - start, t, d, i, hh;
+  int s0 = or_window_start(L - T, j->window); /* first position any query token attends */
+  int n = L - s0, t, d, i, hh, jq;
   double *K = NULL, *V = NULL, *s = NULL, *o = NULL, qh[1024];
   int32_t pst[4096], pen[4096];
   if (n < 0) n = 0;
@@ -540,53 +563,66 @@ static void or_attn_task(void* ctx, int64_t u) {
     }
     /* (1) gather and dequantise every attended key and value of kv head g */
     for (t = 0; t < n; ++t)
-      if (or_token(j, b, g, start + t, 0, K + (int64_t)t * D) || or_token(j, b, g, start + t, 1, V + (int64_t)t * D)) {
+      if (or_token(j, b, g, s0 + t, 0, K + (int64_t)t * D) || or_token(j, b, g, s0 + t, 1, V + (int64_t)t * D)) {
         j->status = OR_ERR_BLOCK;
         goto done;
       }
   }
-  for (hh = 0; hh < G; ++hh) {
-    int h = g * G + hh; /* GQA: query head h reads kv head h / G (consecutive grouping) */
-    int32_t row = j->out_row[(int64_t)b * j->Hq + h];
-    double* out;
-    if (row < 0) continue;
-    out = j->out + (int64_t)row * D;
-    for (d = 0; d < D; ++d) out[d] = 0.0; /* an empty sequence attends nothing: zero output */
-    if (n == 0) continue;
-    for (d = 0; d < D; ++d) qh[d] = or_bf16_decode(j->q[((int64_t)b * j->Hq + h) * D + d]);
-    /* (2) scores s_t = scale * q . k_t, then the optional softcap cap * tanh(s / cap) */
-    for (t = 0; t < n; ++t) {
-      double acc = 0.0;
-      for (d = 0; d < D; ++d) acc += qh[d] * K[(int64_t)t * D + d];
-      s[t] = j->scale * acc;
-      if (j->softcap > 0.0) s[t] = j->softcap * tanh(s[t] / j->softcap);
-    }
-    /* (3) out = softmax(s) V, either in one piece or through per-partition partials */
-    {
-      int np = or_partition_bounds(L, j->window, j->partition_size, j->split_threshold, pst, pen, 4096);
-      if (np > 4096) {
-        j->status = OR_ERR_ARG;
-        goto done;
+  for (jq = 0; jq < T; ++jq) {
+    int pos = L - T + jq;                       /* position of query token jq */
+    int a = or_window_start(pos, j->window), e = pos + 1; /* it attends [a, e) */
+    for (hh = 0; hh < G; ++hh) {
+      int h = g * G + hh; /* GQA: query head h reads kv head h / G (consecutive grouping) */
+      int64_t qi = ((int64_t)b * T + jq) * j->Hq + h;
+      int32_t row = j->out_row[qi];
+      double* out;
+      if (row < 0) continue;
+      out = j->out + (int64_t)row * D;
+      for (d = 0; d < D; ++d) out[d] = 0.0; /* nothing attended: zero output */
+      if (pos < 0 || n == 0) continue;
+      for (d = 0; d < D; ++d) qh[d] = or_bf16_decode(j->q[qi * D + d]);
+      /* (2) scores s_t = scale * q . k_t, then the optional softcap cap * tanh(s / cap) */
+      for (t = a; t < e; ++t) {
+        double acc = 0.0;
+        for (d = 0; d < D; ++d) acc += qh[d] * K[(int64_t)(t - s0) * D + d];
+        s[t - s0] = j->scale * acc;
+        if (j->softcap > 0.0) s[t - s0] = j->softcap * tanh(s[t - s0] / j->softcap);
       }
-      if (np == 1) {
-        double m, l;
-        or_softmax_pv(s, V, n, D, &m, &l, out);
-        for (d = 0; d < D; ++d) out[d] /= l;
-      } else {
-        /* per partition: running max m_p, sum l_p and the unnormalised o_p; then
-         * M = max m_p, Lsum = sum l_p e^(m_p - M), out = sum o_p e^(m_p - M) / Lsum */
-        double mp[4096], lp[4096], M = -INFINITY, Lsum = 0.0;
-        for (i = 0; i < np; ++i) {
-          or_softmax_pv(s + (pst[i] - start), V + (int64_t)(pst[i] - start) * D, pen[i] - pst[i], D, &mp[i], &lp[i],
-                        o + (int64_t)i * D);
-          if (mp[i] > M) M = mp[i];
+      /* (3) out = softmax(s) V over [a, e), in one piece or through per-partition partials */
+      {
+        int np = or_partition_bounds_span(s0, L, j->partition_size, j->split_threshold, pst, pen, 4096);
+        if (np > 4096) {
+          j->status = OR_ERR_ARG;
+          goto done;
         }
-        for (i = 0; i < np; ++i) {
-          double w = exp(mp[i] - M);
-          Lsum += lp[i] * w;
-          for (d = 0; d < D; ++d) out[d] += o[(int64_t)i * D + d] * w;
+        if (np == 1) {
+          double m, l;
+          or_softmax_pv(s + (a - s0), V + (int64_t)(a - s0) * D, e - a, D, &m, &l, out);
+          for (d = 0; d < D; ++d) out[d] /= l;
+        } else {
+          /* per partition: running max m_p, sum l_p and the unnormalised o_p over the part of
+           * it this query attends; then M = max m_p, Lsum = sum l_p e^(m_p - M),
+           * out = sum o_p e^(m_p - M) / Lsum */
+          double mp[4096], lp[4096], M = -INFINITY, Lsum = 0.0;
+          for (i = 0; i < np; ++i) {
+            int lo = pst[i] > a ? pst[i] : a, hi = pen[i] < e ? pen[i] : e;
+            if (lo >= hi) {
+              mp[i] = -INFINITY;
+              lp[i] = 0.0;
+              continue;
+            }
+            or_softmax_pv(s + (lo - s0), V + (int64_t)(lo - s0) * D, hi - lo, D, &mp[i], &lp[i], o + (int64_t)i * D);
+            if (mp[i] > M) M = mp[i];
+          }
+          for (i = 0; i < np; ++i) {
+            double w;
+            if (lp[i] == 0.0) continue;
+            w = exp(mp[i] - M);
+            Lsum += lp[i] * w;
+            for (d = 0; d < D; ++d) out[d] += o[(int64_t)i * D + d] * w;
+          }
+          for (d = 0; d < D; ++d) out[d] /= Lsum;
         }
-        for (d = 0; d < D; ++d) out[d] /= Lsum;
       }
     }
   }
@@ -597,27 +633,29 @@ done:
   free(o);
 }
 
-/* out_row[b * Hq + h] selects the (b, h) outputs to compute (row index into out,
- * or -1); pass NULL to compute all of them into out[B][Hq][D]. Returns OR_OK or an
- * error; *threads_used receives the thread count. */
-int or_decode_attention(int B, int Hq, int Hkv, int D, int block_size, int fmt, int num_blocks, int max_blocks,
-                        const uint16_t* q, const void* k_cache, const void* v_cache, const float* k_scales,
-                        const float* v_scales, const float* codebook, const float* sign, const int32_t* block_tables,
-                        const int32_t* context_lens, double scale, double softcap, int window, int partition_size,
-                        int split_threshold, const int32_t* out_row, double* out, int threads, int* threads_used) {
+/* out_row[(b * T + j) * Hq + h] selects the (b, j, h) outputs to compute (row index into
+ * out, or -1); pass NULL to compute all of them into out[B][T][Hq][D]. T is the number of
+ * query tokens per sequence (1 = ordinary decode). Returns OR_OK or an error;
+ * *threads_used receives the thread count. */
+int or_decode_attention(int B, int T, int Hq, int Hkv, int D, int block_size, int fmt, int num_blocks,
+                        int max_blocks, const uint16_t* q, const void* k_cache, const void* v_cache,
+                        const float* k_scales, const float* v_scales, const float* codebook, const float* sign,
+                        const int32_t* block_tables, const int32_t* context_lens, double scale, double softcap,
+                        int window, int partition_size, int split_threshold, const int32_t* out_row, double* out,
+                        int threads, int* threads_used) {
   or_attn_job j;
   int32_t* rows = NULL;
   double* H = NULL;
-  int64_t nu = 0, b, g, hh;
+  int64_t nu = 0, b, g, hh, jq;
   int used;
-  if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || D <= 0 || D > 1024 || block_size <= 0) return OR_ERR_ARG;
+  if (B < 0 || T < 1 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || D <= 0 || D > 1024 || block_size <= 0) return OR_ERR_ARG;
   if (fmt < OR_FMT_BF16 || fmt > OR_FMT_CB3K_CB4V) return OR_ERR_ARG;
   if (fmt >= OR_FMT_CB4 && (D & (D - 1))) return OR_ERR_ARG;
   memset(&j, 0, sizeof j);
   if (!out_row) {
-    rows = (int32_t*)malloc(sizeof(int32_t) * (size_t)(B * Hq + 1));
+    rows = (int32_t*)malloc(sizeof(int32_t) * (size_t)((int64_t)B * T * Hq + 1));
     if (!rows) return OR_ERR_NOMEM;
-    for (b = 0; b < (int64_t)B * Hq; ++b) rows[b] = (int32_t)b;
+    for (b = 0; b < (int64_t)B * T * Hq; ++b) rows[b] = (int32_t)b;
     out_row = rows;
   }
   j.unit_b = (int32_t*)malloc(sizeof(int32_t) * (size_t)(B * Hkv + 1));
@@ -636,7 +674,8 @@ int or_decode_attention(int B, int Hq, int Hkv, int D, int block_size, int fmt, 
   for (b = 0; b < B; ++b)
     for (g = 0; g < Hkv; ++g) {
       int want = 0;
-      for (hh = 0; hh < Hq / Hkv; ++hh) want |= out_row[b * Hq + g * (Hq / Hkv) + hh] >= 0;
+      for (jq = 0; jq < T; ++jq)
+        for (hh = 0; hh < Hq / Hkv; ++hh) want |= out_row[(b * T + jq) * Hq + g * (Hq / Hkv) + hh] >= 0;
       if (want) {
         j.unit_b[nu] = (int32_t)b;
         j.unit_g[nu] = (int32_t)g;
@@ -644,6 +683,7 @@ int or_decode_attention(int B, int Hq, int Hkv, int D, int block_size, int fmt, 
       }
     }
   j.B = B;
+  j.T = T;
   j.Hq = Hq;
   j.Hkv = Hkv;
   j.D = D;

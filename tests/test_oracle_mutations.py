@@ -8,16 +8,19 @@ import pytest
 import oracle
 import test_oracle_attention as A
 import test_oracle_encoders as E
+import test_oracle_multitoken as M
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
 
 # (name, text that occurs exactly once in oracle.c, replacement)
 MUTATIONS = [
     ("gqa mapping interleaved", "int h = g * G + hh;", "int h = hh * j->Hkv + g;"),
-    ("softmax scale dropped", "s[t] = j->scale * acc;", "s[t] = acc;"),
-    ("softcap without the cap", "s[t] = j->softcap * tanh(s[t] / j->softcap);", "s[t] = tanh(s[t]);"),
-    ("window off by one", "int start = (j->window > 0 && L > j->window) ? L - j->window : 0;",
-     "int start = (j->window > 0 && L > j->window) ? L - j->window + 1 : 0;"),
+    ("softmax scale dropped", "s[t - s0] = j->scale * acc;", "s[t - s0] = acc;"),
+    ("softcap without the cap", "s[t - s0] = j->softcap * tanh(s[t - s0] / j->softcap);",
+     "s[t - s0] = tanh(s[t - s0]);"),
+    ("window off by one", "int a = window > 0 ? pos + 1 - window : 0;", "int a = window > 0 ? pos - window : 0;"),
+    ("causal limit off by one", "int a = or_window_start(pos, j->window), e = pos + 1;",
+     "int a = or_window_start(pos, j->window), e = pos + 2 < L ? pos + 2 : L;"),
     ("page slot off by one", "row = ((int64_t)phys * j->Hkv + g) * bs + t % bs;",
      "row = ((int64_t)phys * j->Hkv + g) * bs + (t + 1) % bs;"),
     ("K and V swapped", "const uint8_t* base = (const uint8_t*)(which ? j->v_cache : j->k_cache);",
@@ -54,6 +57,8 @@ PINS = [
     (A.test_softcap_two_keys_closed_form, {}),
     (A.test_softcap_window_d256_matches_torch, {}),
     (A.test_partition_bounds_follow_pages, None),
+    (M.test_multitoken_matches_sdpa_with_mask, dict(T=4, window=0)),
+    (M.test_multitoken_matches_sdpa_with_mask, dict(T=3, window=20)),
     (E.test_e4m3_decode_fixed_points, {}),
     (E.test_e4m3_decode_matches_torch, {}),
     (E.test_e4m3_encode_matches_torch_cast, {}),

@@ -27,6 +27,7 @@ from ._binding import (  # noqa: F401
     decode_attn_get_device_error,
     decode_attn_max_partitions,
     decode_attn_paged,
+    decode_attn_paged_static_workspace,
     decode_attn_partition,
     decode_attn_reduce,
     decode_attn_rotate_q,

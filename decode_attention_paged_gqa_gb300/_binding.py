@@ -19,6 +19,7 @@ DA_KV_BF16, DA_KV_FP8_E4M3, DA_KV_CB4, DA_KV_FP8K_CB4V, DA_KV_CB3K_CB4V = 0, 1, 
 KV_FORMATS = {"bf16": DA_KV_BF16, "fp8": DA_KV_FP8_E4M3, "cb4": DA_KV_CB4, "fp8k_cb4v": DA_KV_FP8K_CB4V,
               "cb3k_cb4v": DA_KV_CB3K_CB4V}
 DA_OK, DA_ERR_INVALID_ARG, DA_ERR_UNSUPPORTED, DA_ERR_WORKSPACE, DA_ERR_LAUNCH, DA_ERR_CUDA = 0, -1, -2, -3, -4, -5
+DA_ERR_STATIC_WORKSPACE = -6
 DA_DEVERR_BLOCK_ID, DA_DEVERR_CONTEXT_LEN, DA_DEVERR_TIMEOUT = 0x1, 0x2, 0x4
 
 
@@ -89,6 +90,7 @@ def _load():
                 "decode_attn_workspace_bytes": (ctypes.c_size_t, [PP]),
                 "decode_attn_workspace_init": (I, [PP, P]),
                 "decode_attn_paged": (I, call),
+                "decode_attn_paged_static_workspace": (I, call),
                 "decode_attn_rotate_q": (I, call),
                 "decode_attn_partition": (I, call),
                 "decode_attn_reduce": (I, call),
@@ -169,6 +171,15 @@ def decode_attn_paged(q, k_cache, v_cache, k_scales, v_scales, codebook, sign_pa
                       out, params, stream=None) -> None:
     _call("decode_attn_paged", q, k_cache, v_cache, k_scales, v_scales, codebook, sign_pattern, block_tables,
           context_lens, out, params, stream)
+
+
+def decode_attn_paged_static_workspace(q, k_cache, v_cache, k_scales, v_scales, codebook, sign_pattern,
+                                      block_tables, context_lens, out, params, stream=None) -> None:
+    """decode_attn_paged for callers that cannot allocate device memory: the workspace is the
+    library's own fixed 64 MiB device array (params.workspace is ignored). Calls that overlap
+    on the GPU share that array and race; serialise them."""
+    _call("decode_attn_paged_static_workspace", q, k_cache, v_cache, k_scales, v_scales, codebook, sign_pattern,
+          block_tables, context_lens, out, params, stream)
 
 
 def decode_attn_rotate_q(q, k_cache, v_cache, k_scales, v_scales, codebook, sign_pattern, block_tables,

@@ -151,6 +151,12 @@ cudaError_t ensure_dynamic_smem(Kernel kern, size_t bytes, DeviceFlags& done) {
   return e;
 }
 
+// The checked launch sequence behind decode_attn_paged and its phases (decode_attn.cu).
+enum Phase { kRotate = 1, kPartition = 2, kReduce = 4, kAll = 7 };
+int run_phases(int phases, const void* q, const void* k, const void* v, const float* ks, const float* vs,
+               const float* cb, const float* sign, const int32_t* bt, const int32_t* lens, float* out,
+               const da_params* p, void* stream);
+
 // Launchers (one translation unit each). They return cudaGetLastError() of their launch.
 cudaError_t launch_rotate_q(const Args& a, cudaStream_t s);
 cudaError_t launch_partition(const Args& a, cudaStream_t s);     // dispatches on the format:

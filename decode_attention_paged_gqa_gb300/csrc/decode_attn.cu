@@ -96,10 +96,13 @@ Args make_args(const void* q, const void* k, const void* v, const float* ks, con
   return a;
 }
 
-enum Phase { kRotate = 1, kPartition = 2, kReduce = 4, kAll = 7 };
+}  // namespace
 
-int run(int phases, const void* q, const void* k, const void* v, const float* ks, const float* vs, const float* cb,
-        const float* sign, const int32_t* bt, const int32_t* lens, float* out, const da_params* p, void* stream) {
+namespace da {
+
+int run_phases(int phases, const void* q, const void* k, const void* v, const float* ks, const float* vs,
+               const float* cb, const float* sign, const int32_t* bt, const int32_t* lens, float* out,
+               const da_params* p, void* stream) {
   int rc = check_params(p);
   if (rc) return rc;
   if ((rc = check_workspace(p))) return rc;
@@ -114,7 +117,7 @@ int run(int phases, const void* q, const void* k, const void* v, const float* ks
   return DA_OK;
 }
 
-}  // namespace
+}  // namespace da
 
 extern "C" {
 
@@ -137,32 +140,32 @@ int decode_attn_paged(const void* q, const void* k_cache, const void* v_cache, c
                       const float* v_scales, const float* codebook, const float* sign_pattern,
                       const int32_t* block_tables, const int32_t* context_lens, float* out, const da_params* p,
                       void* stream) {
-  return run(kAll, q, k_cache, v_cache, k_scales, v_scales, codebook, sign_pattern, block_tables, context_lens, out,
-             p, stream);
+  return run_phases(kAll, q, k_cache, v_cache, k_scales, v_scales, codebook, sign_pattern, block_tables,
+                    context_lens, out, p, stream);
 }
 
 int decode_attn_rotate_q(const void* q, const void* k_cache, const void* v_cache, const float* k_scales,
                          const float* v_scales, const float* codebook, const float* sign_pattern,
                          const int32_t* block_tables, const int32_t* context_lens, float* out, const da_params* p,
                          void* stream) {
-  return run(kRotate, q, k_cache, v_cache, k_scales, v_scales, codebook, sign_pattern, block_tables, context_lens,
-             out, p, stream);
+  return run_phases(kRotate, q, k_cache, v_cache, k_scales, v_scales, codebook, sign_pattern, block_tables,
+                    context_lens, out, p, stream);
 }
 
 int decode_attn_partition(const void* q, const void* k_cache, const void* v_cache, const float* k_scales,
                           const float* v_scales, const float* codebook, const float* sign_pattern,
                           const int32_t* block_tables, const int32_t* context_lens, float* out, const da_params* p,
                           void* stream) {
-  return run(kPartition, q, k_cache, v_cache, k_scales, v_scales, codebook, sign_pattern, block_tables, context_lens,
-             out, p, stream);
+  return run_phases(kPartition, q, k_cache, v_cache, k_scales, v_scales, codebook, sign_pattern, block_tables,
+                    context_lens, out, p, stream);
 }
 
 int decode_attn_reduce(const void* q, const void* k_cache, const void* v_cache, const float* k_scales,
                        const float* v_scales, const float* codebook, const float* sign_pattern,
                        const int32_t* block_tables, const int32_t* context_lens, float* out, const da_params* p,
                        void* stream) {
-  return run(kReduce, q, k_cache, v_cache, k_scales, v_scales, codebook, sign_pattern, block_tables, context_lens,
-             out, p, stream);
+  return run_phases(kReduce, q, k_cache, v_cache, k_scales, v_scales, codebook, sign_pattern, block_tables,
+                    context_lens, out, p, stream);
 }
 
 int decode_attn_get_device_error(const da_params* p, void* stream, uint32_t* err_out) {
@@ -188,6 +191,7 @@ const char* decode_attn_strerror(int status) {
     case DA_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
     case DA_ERR_LAUNCH: return "kernel launch failed";
     case DA_ERR_CUDA: return "CUDA runtime call failed";
+    case DA_ERR_STATIC_WORKSPACE: return "the call needs more workspace than the library's static 64 MiB array holds";
   }
   return "unknown status";
 }

@@ -75,7 +75,9 @@ enum da_status {
   DA_ERR_UNSUPPORTED = -2,  /* valid arguments outside the built set (see da_params) */
   DA_ERR_WORKSPACE = -3,    /* workspace NULL, misaligned, or smaller than decode_attn_workspace_bytes */
   DA_ERR_LAUNCH = -4,       /* a kernel launch failed; see cudaGetLastError */
-  DA_ERR_CUDA = -5          /* another CUDA runtime call failed */
+  DA_ERR_CUDA = -5,         /* another CUDA runtime call failed */
+  DA_ERR_STATIC_WORKSPACE = -6 /* decode_attn_paged_static_workspace: the call needs more workspace
+                                  than the library's fixed 64 MiB array holds */
 };
 
 /* Bits of the device error word (decode_attn_get_device_error). */
@@ -157,6 +159,28 @@ int decode_attn_reduce(const void* q, const void* k_cache, const void* v_cache, 
                        const float* v_scales, const float* codebook, const float* sign_pattern,
                        const int32_t* block_tables, const int32_t* context_lens, float* out, const da_params* p,
                        void* stream);
+
+/* decode_attn_paged for callers that cannot allocate device memory: code where device
+ * allocation is forbidden or unavailable, such as a plugin inside a host framework that owns
+ * every allocation and exposes none to its extensions, a real-time loop that must not call
+ * the allocator (cudaMalloc can synchronise the device and take unbounded time), or a caller
+ * with no CUDA allocator of its own. (This entry point has no counterpart in the pages; it is
+ * an addition of this library.)
+ * Same arguments and results as decode_attn_paged, except that p->workspace and
+ * p->workspace_bytes are ignored: the workspace is a fixed 64 MiB array in device global
+ * memory defined by the library (every GPU that loads the library holds it until the process
+ * exits). Calls whose decode_attn_workspace_bytes(p) exceeds 64 MiB return
+ * DA_ERR_STATIC_WORKSPACE and enqueue nothing. Nothing is allocated and no allocating
+ * routine is called; each call clears the array's error word on `stream` first.
+ * All calls share the one array: calls that overlap on the GPU (on different streams, or
+ * from different host threads) race on it and must be serialised by the caller. The
+ * device-side bad-input bits of these calls are not reported.
+ * The first call on each device looks up the array's device address (cudaGetSymbolAddress,
+ * with that device current); make that first call before any stream capture. */
+int decode_attn_paged_static_workspace(const void* q, const void* k_cache, const void* v_cache,
+                                       const float* k_scales, const float* v_scales, const float* codebook,
+                                       const float* sign_pattern, const int32_t* block_tables,
+                                       const int32_t* context_lens, float* out, const da_params* p, void* stream);
 
 /* Synchronises `stream`, then reads the workspace's error word into *err_out (host
  * pointer; DA_DEVERR_* bits, 0 = no bad input seen since the last read) and clears it. */

@@ -118,7 +118,7 @@ def test_empty_batch_enqueues_nothing():
 
 
 def test_strerror():
-    for s in range(-5, 1):
+    for s in range(-6, 1):
         assert da.decode_attn_strerror(s) != "unknown status"
     assert da.decode_attn_strerror(-99) == "unknown status"
 

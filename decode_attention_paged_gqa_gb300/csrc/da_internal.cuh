@@ -40,6 +40,8 @@ struct Args {
   float* part_o;              // [B][Hq][P][D], unnormalised partial outputs
   float* part_m;              // [B][Hq][P], running max in log2 units
   float* part_l;              // [B][Hq][P], running sum of 2^(s - m)
+  unsigned long long* tickets;  // [B][Hkv]: (call generation << 32) | partitions finished
+  unsigned gen;               // this call's generation (never 0)
 };
 
 // Start of the attended positions of a sequence of length L.
@@ -101,7 +103,7 @@ __device__ __forceinline__ float bf16_to_f32(uint16_t h) { return __uint_as_floa
 
 // Workspace layout; every piece starts on a 256-byte boundary.
 struct Layout {
-  size_t err, q_rot, part_o, part_m, part_l, total;
+  size_t err, q_rot, part_o, part_m, part_l, tickets, total;
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -129,6 +131,8 @@ inline Layout workspace_layout(const da_params& p) {
   off = align256(off + BH * P * sizeof(float));
   l.part_l = off;
   off = align256(off + BH * P * sizeof(float));
+  l.tickets = off;
+  off = align256(off + (size_t)p.batch * p.num_kv_heads * sizeof(unsigned long long));
   l.total = off;
   return l;
 }

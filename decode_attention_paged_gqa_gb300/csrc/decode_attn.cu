@@ -8,6 +8,7 @@
 // partial buffers (workspace) instead of the wrapper allocating them per call.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 
@@ -17,6 +18,16 @@
 using namespace da;
 
 namespace {
+
+// A fresh nonzero number per call: the split-K completion tickets in the workspace carry
+// it, so counts left behind by an earlier call never mix with this call's.
+unsigned next_generation() {
+  static std::atomic<unsigned> g{0};
+  unsigned v;
+  do v = g.fetch_add(1, std::memory_order_relaxed) + 1;
+  while (v == 0);
+  return v;
+}
 
 int check_params(const da_params* p) {
   if (!p) return DA_ERR_INVALID_ARG;
@@ -93,6 +104,8 @@ Args make_args(const void* q, const void* k, const void* v, const float* ks, con
   a.part_o = reinterpret_cast<float*>(ws + l.part_o);
   a.part_m = reinterpret_cast<float*>(ws + l.part_m);
   a.part_l = reinterpret_cast<float*>(ws + l.part_l);
+  a.tickets = reinterpret_cast<unsigned long long*>(ws + l.tickets);
+  a.gen = next_generation();
   return a;
 }
 

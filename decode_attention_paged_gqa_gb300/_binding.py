@@ -32,6 +32,7 @@ class DecodeAttnError(RuntimeError):
 class da_params(ctypes.Structure):
     _fields_ = [
         ("batch", ctypes.c_int32),
+        ("query_len", ctypes.c_int32),
         ("num_q_heads", ctypes.c_int32),
         ("num_kv_heads", ctypes.c_int32),
         ("head_dim", ctypes.c_int32),
@@ -52,9 +53,10 @@ class da_params(ctypes.Structure):
 
 def make_params(*, batch, num_q_heads, num_kv_heads, head_dim, num_blocks, max_blocks_per_seq, max_context_len,
                 kv_format, softmax_scale, softcap=0.0, window=0, partition_size=512, split_threshold=1024,
-                block_size=16, workspace=None) -> da_params:
+                block_size=16, query_len=1, workspace=None) -> da_params:
     p = da_params()
     p.batch, p.num_q_heads, p.num_kv_heads, p.head_dim = batch, num_q_heads, num_kv_heads, head_dim
+    p.query_len = int(query_len)
     p.block_size, p.num_blocks, p.max_blocks_per_seq, p.max_context_len = (block_size, num_blocks,
                                                                            max_blocks_per_seq, max_context_len)
     p.kv_format = KV_FORMATS[kv_format] if isinstance(kv_format, str) else int(kv_format)

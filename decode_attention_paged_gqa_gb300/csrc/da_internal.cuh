@@ -20,7 +20,7 @@ constexpr int kMaxPartitions = 8192;
 
 // Everything a kernel needs, passed by value (no pointers into host memory).
 struct Args {
-  const uint16_t* q;          // [B][Hq][D] bf16 bits
+  const uint16_t* q;          // [B][T][Hq][D] bf16 bits
   const void* k_cache;        // layout by format, see decode_attn.h
   const void* v_cache;
   const float* k_scales;      // fp8: [1]; cb4: [num_blocks][Hkv][bs]
@@ -29,41 +29,51 @@ struct Args {
   const float* sign;          // cb4: [D]
   const int32_t* block_tables;  // [B][max_blocks]
   const int32_t* context_lens;  // [B]
-  float* out;                 // [B][Hq][D]
-  int B, Hq, Hkv, D, bs, num_blocks, max_blocks, max_ctx, fmt;
+  float* out;                 // [B][T][Hq][D]
+  int B, T, Hq, Hkv, D, bs, num_blocks, max_blocks, max_ctx, fmt;  // T: query tokens per sequence
   float scale, softcap;
   int window, psize, thresh;
   int P;                      // partitions the grid and the workspace are sized for
   // workspace pieces
   uint32_t* err;              // device error word (DA_DEVERR_* bits)
-  float* q_rot;               // [B][Hq][D] (formats whose keys are on the rotated basis)
-  float* part_o;              // [B][Hq][P][D], unnormalised partial outputs
-  float* part_m;              // [B][Hq][P], running max in log2 units
-  float* part_l;              // [B][Hq][P], running sum of 2^(s - m)
+  float* q_rot;               // [B][T][Hq][D] (formats whose keys are on the rotated basis)
+  float* part_o;              // [B][T][Hq][P][D], unnormalised partial outputs
+  float* part_m;              // [B][T][Hq][P], running max in log2 units
+  float* part_l;              // [B][T][Hq][P], running sum of 2^(s - m)
   unsigned long long* tickets;  // [B][Hkv]: (call generation << 32) | partitions finished
   unsigned gen;               // this call's generation (never 0)
 };
 
-// Start of the attended positions of a sequence of length L.
-__host__ __device__ __forceinline__ int attended_start(int L, int window) {
-  return (window > 0 && L > window) ? L - window : 0;
+// First position attended by a query token at position `pos`: with a window of W tokens,
+// the last W positions up to and including its own; else every position from 0.
+__host__ __device__ __forceinline__ int window_start(int pos, int window) {
+  const int s = window > 0 ? pos + 1 - window : 0;
+  return s > 0 ? s : 0;
 }
 
-// Partitions of an attended length n: 0 when empty, ceil(n / psize) when split, else 1.
+// First position attended by any of the T query tokens (positions L-T .. L-1) of a
+// sequence of length L. With T = 1 this is max(0, L - window), or 0 without a window.
+__host__ __device__ __forceinline__ int span_start(int L, int T, int window) { return window_start(L - T, window); }
+
+// Partitions of an attended span of n tokens: 0 when empty, ceil(n / psize) when split, else 1.
 __host__ __device__ __forceinline__ int num_partitions(int n, int psize, int thresh) {
   if (n <= 0) return 0;
   return (psize > 0 && n >= thresh) ? (n + psize - 1) / psize : 1;
+}
+
+__host__ __device__ __forceinline__ int seq_partitions(int L, int T, int window, int psize, int thresh) {
+  return num_partitions(L - span_start(L, T, window), psize, thresh);
 }
 
 struct Range {
   int start, end;  // [start, end) token positions; start >= end means "no such partition"
 };
 
-// Token range of partition p of a sequence of (already clamped) length L.
-__host__ __device__ __forceinline__ Range partition_range(int L, int p, int window, int psize, int thresh) {
-  const int s = attended_start(L, window);
-  const int n = L - s;
-  const int np = num_partitions(n, psize, thresh);
+// Token range of partition p of a sequence of (already clamped) length L with T query
+// tokens; partitions are counted from the span start.
+__host__ __device__ __forceinline__ Range partition_range(int L, int T, int p, int window, int psize, int thresh) {
+  const int s = span_start(L, T, window);
+  const int np = num_partitions(L - s, psize, thresh);
   Range r{0, 0};
   if (p >= np) return r;
   if (np == 1) return Range{s, L};
@@ -108,16 +118,19 @@ struct Layout {
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+inline int query_len(const da_params& p) { return p.query_len > 1 ? p.query_len : 1; }
+
+// Partition count of the longest possible span: that of a sequence of max_context_len tokens.
 inline int host_max_partitions(const da_params& p) {
-  int n = p.max_context_len;
-  if (p.window > 0 && n > p.window) n = p.window;
-  const int np = num_partitions(n, p.partition_size, p.split_threshold);
+  long long n = p.max_context_len;
+  if (p.window > 0 && n > (long long)p.window + query_len(p) - 1) n = (long long)p.window + query_len(p) - 1;
+  const int np = num_partitions((int)n, p.partition_size, p.split_threshold);
   return np < 1 ? 1 : np;
 }
 
 inline Layout workspace_layout(const da_params& p) {
   Layout l{};
-  const size_t BH = (size_t)p.batch * p.num_q_heads;
+  const size_t BH = (size_t)p.batch * query_len(p) * p.num_q_heads;
   const size_t P = (size_t)host_max_partitions(p);
   size_t off = 0;
   l.err = off;

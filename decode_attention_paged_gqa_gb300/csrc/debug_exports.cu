@@ -13,7 +13,7 @@ __global__ void debug_bounds_kernel(const Args a, int32_t* bounds) {
   const int b = blockIdx.x;
   const int L = load_len(a, b, threadIdx.x == 0);
   for (int p = threadIdx.x; p < a.P; p += blockDim.x) {
-    const Range r = partition_range(L, p, a.window, a.psize, a.thresh);
+    const Range r = partition_range(L, a.T, p, a.window, a.psize, a.thresh);
     const bool valid = r.start < r.end;
     bounds[((size_t)b * a.P + p) * 2 + 0] = valid ? r.start : -1;
     bounds[((size_t)b * a.P + p) * 2 + 1] = valid ? r.end : -1;

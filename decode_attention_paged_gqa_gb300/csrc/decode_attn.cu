@@ -31,7 +31,8 @@ unsigned next_generation() {
 
 int check_params(const da_params* p) {
   if (!p) return DA_ERR_INVALID_ARG;
-  if (p->batch < 0 || p->num_q_heads <= 0 || p->num_kv_heads <= 0 || p->head_dim <= 0 || p->block_size <= 0 ||
+  if (p->batch < 0 || p->query_len < 0 || p->num_q_heads <= 0 || p->num_kv_heads <= 0 || p->head_dim <= 0 ||
+      p->block_size <= 0 ||
       p->num_blocks <= 0 || p->max_blocks_per_seq <= 0 || p->max_context_len < 0 || p->window < 0 ||
       p->partition_size < 0 || p->split_threshold < 0)
     return DA_ERR_INVALID_ARG;
@@ -40,9 +41,11 @@ int check_params(const da_params* p) {
   if (p->kv_format < DA_KV_BF16 || p->kv_format > DA_KV_CB3K_CB4V) return DA_ERR_INVALID_ARG;
   const int G = p->num_q_heads / p->num_kv_heads;
   if (G != 1 && G != 2 && G != 4 && G != 8) return DA_ERR_UNSUPPORTED;
+  if ((long long)query_len(*p) * G > 8) return DA_ERR_UNSUPPORTED;  // query tokens x group heads per tile
   if (p->head_dim != 128 && p->head_dim != 256) return DA_ERR_UNSUPPORTED;
   if (p->block_size != kBlockSize) return DA_ERR_UNSUPPORTED;
-  if (p->batch > 65535 || p->num_kv_heads > 65535 || p->num_q_heads > 65535) return DA_ERR_UNSUPPORTED;
+  if ((long long)p->batch * query_len(*p) > 65535 || p->num_kv_heads > 65535 || p->num_q_heads > 65535)
+    return DA_ERR_UNSUPPORTED;
   if (host_max_partitions(*p) > kMaxPartitions) return DA_ERR_UNSUPPORTED;
   if ((long long)p->num_blocks * p->num_kv_heads * p->block_size >= (1ll << 31)) return DA_ERR_UNSUPPORTED;
   return DA_OK;
@@ -83,6 +86,7 @@ Args make_args(const void* q, const void* k, const void* v, const float* ks, con
   a.context_lens = lens;
   a.out = out;
   a.B = p->batch;
+  a.T = query_len(*p);
   a.Hq = p->num_q_heads;
   a.Hkv = p->num_kv_heads;
   a.D = p->head_dim;

@@ -3,7 +3,7 @@
 //
 // One CTA per (partition p, kv head g, sequence b). It walks the partition's tokens in
 // tiles of 32: the tile's K and V rows are gathered through the block table, dequantised
-// to fp32 in shared memory, scored against the G query heads of the group, folded into an
+// to fp32 in shared memory, scored against the query heads of the group, folded into an
 // online softmax (running max m, running sum l, unnormalised output o), and finally the
 // partition's (o, m, l) are written to the workspace for the reduce kernel.
 // (attention.rs README: split-K decode per KV format with a float-precision reduce;
@@ -34,47 +34,60 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-template <int FMT, int D, int G>
+// NV: the (query token, head) pairs of the group, padded to a power of two: "virtual
+// heads" v = jq * G + h, each with its own causal limit (query token jq sits at position
+// L - T + jq).
+template <int FMT, int D, int NV>
 __global__ void __launch_bounds__(kThreads) partition_simt_kernel(const Args a) {
   const int p = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int G = a.Hq / a.Hkv, V = a.T * G;
   const int L = load_len(a, b, p == 0 && g == 0 && tid == 0);
-  const Range r = partition_range(L, p, a.window, a.psize, a.thresh);
+  const Range r = partition_range(L, a.T, p, a.window, a.psize, a.thresh);
   if (r.start >= r.end) return;
 
   extern __shared__ float smem[];
-  float* q_s = smem;                        // [G][D]
-  float* k_s = q_s + G * D;                 // [kTile][D + 1]
+  float* q_s = smem;                        // [NV][D]
+  float* k_s = q_s + NV * D;                // [kTile][D + 1]
   float* v_s = k_s + kTile * (D + 1);       // [kTile][D]
-  float* p_s = v_s + kTile * D;             // [G][kTile]
-  float* alpha_s = p_s + G * kTile;         // [G]
-  float* cbk_s = alpha_s + G;               // [16] key codebook
+  float* p_s = v_s + kTile * D;             // [NV][kTile]
+  float* alpha_s = p_s + NV * kTile;        // [NV]
+  float* cbk_s = alpha_s + NV;              // [16] key codebook
   float* cbv_s = cbk_s + 16;                // [16] value codebook
   int* ok_s = reinterpret_cast<int*>(cbv_s + 16);  // [kTile]
   constexpr int KS = k_side(FMT), VS = v_side(FMT);
 
-  // queries of the group (rotated ones when the keys are stored on the rotated basis)
-  for (int i = tid; i < G * D; i += kThreads) {
-    const int h = g * G + i / D, d = i % D;
-    const size_t qi = ((size_t)b * a.Hq + h) * D + d;
-    q_s[i] = is_codebook(KS) ? a.q_rot[qi] : bf16_to_f32(a.q[qi]);
+  // queries of the group's virtual heads (rotated ones when the keys are on the rotated basis)
+  for (int i = tid; i < NV * D; i += kThreads) {
+    const int v = i / D, d = i % D;
+    float x = 0.0f;
+    if (v < V) {
+      const size_t qi = (((size_t)b * a.T + v / G) * a.Hq + g * G + v % G) * D + d;
+      x = is_codebook(KS) ? a.q_rot[qi] : bf16_to_f32(a.q[qi]);
+    }
+    q_s[i] = x;
   }
   if (tid < 16) {
     if (is_codebook(KS)) cbk_s[tid] = tid < (KS == kSideCB3 ? 8 : 16) ? __ldg(a.codebook + tid) : 0.0f;
     if (is_codebook(VS)) cbv_s[tid] = __ldg(a.codebook + (KS == kSideCB3 ? 8 : 0) + tid);
   }
 
-  constexpr int kHeadsPerWarp = (G + 3) / 4;
+  constexpr int kHeadsPerWarp = (NV + 3) / 4;
   float m_run[kHeadsPerWarp], l_run[kHeadsPerWarp];
+  int lo_v[kHeadsPerWarp], hi_v[kHeadsPerWarp];  // tokens virtual head w + 4i attends in this partition
 #pragma unroll
   for (int i = 0; i < kHeadsPerWarp; ++i) {
     m_run[i] = -INFINITY;
     l_run[i] = 0.0f;
+    const int v = warp + 4 * i, pos = L - a.T + (v < V ? v / G : 0);
+    const int lo = window_start(pos, a.window), hi = pos + 1;
+    lo_v[i] = lo > r.start ? lo : r.start;
+    hi_v[i] = hi < r.end ? hi : r.end;
   }
   constexpr int kDimsPerThread = D / kThreads;  // 1 or 2
-  float o[G][kDimsPerThread];
+  float o[NV][kDimsPerThread];
 #pragma unroll
-  for (int h = 0; h < G; ++h)
+  for (int h = 0; h < NV; ++h)
 #pragma unroll
     for (int j = 0; j < kDimsPerThread; ++j) o[h][j] = 0.0f;
 
@@ -109,14 +122,14 @@ __global__ void __launch_bounds__(kThreads) partition_simt_kernel(const Args a) 
     }
     __syncthreads();
 
-    // scores and online softmax: warp w owns heads w, w + 4; lane = token of the tile
+    // scores and online softmax: warp w owns virtual heads w, w + 4; lane = token of the tile
 #pragma unroll
     for (int i = 0; i < kHeadsPerWarp; ++i) {
       const int hh = warp + 4 * i;
-      if (hh < G) {
+      if (hh < NV) {
         const int t = t0 + lane;
         float s = -INFINITY;
-        if (t < r.end && ok_s[lane]) {
+        if (hh < V && t >= lo_v[i] && t < hi_v[i] && ok_s[lane]) {
           float acc = 0.0f;
           const float* qh = q_s + hh * D;
           const float* kr = k_s + lane * (D + 1);
@@ -139,7 +152,7 @@ __global__ void __launch_bounds__(kThreads) partition_simt_kernel(const Args a) 
 
     // o[h][d] = alpha_h * o[h][d] + sum_t p[h][t] * v[t][d]; thread owns d = tid (+128)
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
+    for (int h = 0; h < NV; ++h) {
       const float al = alpha_s[h];
 #pragma unroll
       for (int j = 0; j < kDimsPerThread; ++j) {
@@ -154,27 +167,28 @@ __global__ void __launch_bounds__(kThreads) partition_simt_kernel(const Args a) 
 
   // partials of this partition
 #pragma unroll
-  for (int h = 0; h < G; ++h) {
-    const size_t base = ((size_t)b * a.Hq + g * G + h) * a.P + p;
+  for (int h = 0; h < NV; ++h) {
+    if (h >= V) break;
+    const size_t base = (((size_t)b * a.T + h / G) * a.Hq + g * G + h % G) * a.P + p;
 #pragma unroll
     for (int j = 0; j < kDimsPerThread; ++j) a.part_o[base * D + tid + j * kThreads] = o[h][j];
   }
 #pragma unroll
   for (int i = 0; i < kHeadsPerWarp; ++i) {
     const int hh = warp + 4 * i;
-    if (hh < G && lane == 0) {
-      const size_t base = ((size_t)b * a.Hq + g * G + hh) * a.P + p;
+    if (hh < V && lane == 0) {
+      const size_t base = (((size_t)b * a.T + hh / G) * a.Hq + g * G + hh % G) * a.P + p;
       a.part_m[base] = m_run[i];
       a.part_l[base] = l_run[i];
     }
   }
 }
 
-template <int FMT, int D, int G>
+template <int FMT, int D, int NV>
 cudaError_t launch_fixed(const Args& a, cudaStream_t s) {
   const size_t smem =
-      sizeof(float) * (G * D + kTile * (D + 1) + kTile * D + G * kTile + G + 32) + sizeof(int) * kTile;
-  auto kern = partition_simt_kernel<FMT, D, G>;
+      sizeof(float) * (NV * D + kTile * (D + 1) + kTile * D + NV * kTile + NV + 32) + sizeof(int) * kTile;
+  auto kern = partition_simt_kernel<FMT, D, NV>;
   static DeviceFlags attr_set;
   cudaError_t e = ensure_dynamic_smem(kern, smem, attr_set);
   if (e != cudaSuccess) return e;
@@ -185,12 +199,11 @@ cudaError_t launch_fixed(const Args& a, cudaStream_t s) {
 
 template <int FMT, int D>
 cudaError_t launch_g(const Args& a, cudaStream_t s) {
-  switch (a.Hq / a.Hkv) {
-    case 1: return launch_fixed<FMT, D, 1>(a, s);
-    case 2: return launch_fixed<FMT, D, 2>(a, s);
-    case 4: return launch_fixed<FMT, D, 4>(a, s);
-    case 8: return launch_fixed<FMT, D, 8>(a, s);
-  }
+  const int v = a.T * (a.Hq / a.Hkv);  // virtual heads, padded to a power of two
+  if (v <= 1) return launch_fixed<FMT, D, 1>(a, s);
+  if (v <= 2) return launch_fixed<FMT, D, 2>(a, s);
+  if (v <= 4) return launch_fixed<FMT, D, 4>(a, s);
+  if (v <= 8) return launch_fixed<FMT, D, 8>(a, s);
   return cudaErrorInvalidValue;
 }
 

@@ -45,7 +45,9 @@ constexpr int kPage = 16;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr unsigned kFull = 0xffffffffu;
 
-template <int FMT, int D, int G>
+// NV: the group's (query token, head) pairs ("virtual heads" v = jq * G + h), padded to a
+// power of two <= 8; with one query token NV = G.
+template <int FMT, int D, int NV>
 struct Tc {
   static constexpr int kElemBytes = FMT == DA_KV_BF16 ? 2 : 1;
   static constexpr int kSubs = D * kElemBytes / 128;       // 128-byte swizzled column slabs per row
@@ -53,12 +55,11 @@ struct Tc {
   static constexpr int kPageBytes = kSubs * kSubBytes;      // one page of K (or V), one kv head
   static constexpr int kStageBytes = 2 * kPageBytes;        // K + V
   static constexpr int kStages = 16384 / kStageBytes > 0 ? 16384 / kStageBytes : 1;  // 64 KB of stages per CTA
-  static constexpr int kNT = G <= 4 ? 1 : 2;                // P.V column tiles (8 columns each)
-  static constexpr int kCols = 8 * kNT;
+  static constexpr int kNT = NV <= 4 ? 1 : 2;               // P.V column tiles (8 columns each)
   static constexpr int kMT = D / 16;                        // O^T row tiles
   static constexpr int kKS = D / 16;                        // k-steps of S^T
   static constexpr int kStageSmem = kWarps * kStages * kStageBytes;
-  static constexpr int kEpiSmem = (kWarps * G * (D + 4) + 2 * kWarps * 8) * 4;  // its own region
+  static constexpr int kEpiSmem = (kWarps * NV * (D + 4) + 2 * kWarps * 8) * 4;  // its own region
   static constexpr int kSmem = kStageSmem + kEpiSmem + 1024;
 };
 
@@ -111,8 +112,8 @@ __device__ __forceinline__ bool make_unit(const Args& a, long long u, Unit& x, b
   x.b = rem / a.Hkv;
   x.g = rem % a.Hkv;
   x.L = load_len(a, x.b, report && x.p == 0 && x.g == 0);
-  x.r = partition_range(x.L, x.p, a.window, a.psize, a.thresh);
-  x.np = num_partitions(x.L - attended_start(x.L, a.window), a.psize, a.thresh);
+  x.r = partition_range(x.L, a.T, x.p, a.window, a.psize, a.thresh);
+  x.np = seq_partitions(x.L, a.T, a.window, a.psize, a.thresh);
   if (x.r.start >= x.r.end) return false;
   x.first_page = x.r.start / kPage;
   x.npages = (x.r.end - 1) / kPage - x.first_page + 1;
@@ -137,11 +138,12 @@ __device__ __forceinline__ bool take_ticket(unsigned long long* t, unsigned gen,
 }
 
 // Persistent: gridDim.x CTAs walk the units u = blockIdx.x, blockIdx.x + gridDim.x, ...
-template <int FMT, int D, int G>
-__global__ void __launch_bounds__(kThreads, 2)
+template <int FMT, int D, int NV>
+__global__ void __launch_bounds__(kThreads, (D == 128 ? 3 : 2))
     partition_tc_kernel(const Args a, const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap) {
-  using T = Tc<FMT, D, G>;
+  using T = Tc<FMT, D, NV>;
+  const int G = a.Hq / a.Hkv, V = a.T * G;  // group size, virtual heads in use (<= NV)
   constexpr int DP = D + 4;  // padded row of the epilogue buffer (spreads the banks)
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int gid = lane >> 2, tig = lane & 3;
@@ -154,8 +156,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   unsigned char* smem_gen = smem_raw + (smem - ptx::smem_u32(smem_raw));
   const uint32_t bar0 = ptx::smem_u32(bars) + w * T::kStages * 8;
   const uint32_t stage0 = smem + w * T::kStages * T::kStageBytes;
-  float* ep_o = reinterpret_cast<float*>(smem_gen + T::kStageSmem);  // [kWarps][G][DP]
-  float* ep_m = ep_o + kWarps * G * DP;                               // [kWarps][8]
+  float* ep_o = reinterpret_cast<float*>(smem_gen + T::kStageSmem);  // [kWarps][NV][DP]
+  float* ep_m = ep_o + kWarps * NV * DP;                              // [kWarps][8]
   float* ep_l = ep_m + kWarps * 8;                                    // [kWarps][8]
 
   if (lane == 0) {
@@ -216,10 +218,14 @@ __global__ void __launch_bounds__(kThreads, 2)
   };
   for (int k = 0; k < T::kStages; ++k) issue_one();
 
-  // hi/lo role of this thread's two columns (G <= 4: column c carries part c / G)
-  int part[2];
+  // hi/lo role of this thread's two columns (NV <= 4: column c carries part c / NV) and the
+  // virtual head each column scores (columns past V repeat earlier ones and are not stored)
+  int part[2], vcol[2];
 #pragma unroll
-  for (int j = 0; j < 2; ++j) part[j] = G <= 4 ? (2 * tig + j) / G : 0;
+  for (int j = 0; j < 2; ++j) {
+    part[j] = NV <= 4 ? (2 * tig + j) / NV : 0;
+    vcol[j] = ((2 * tig + j) % NV) % V;
+  }
   const int mi = lane >> 3, ri = lane & 7;  // ldmatrix: matrix index and row of this lane's address
   const float cap = a.softcap;
   const float out_scale = FMT == DA_KV_FP8_E4M3 ? __ldg(a.v_scales) : 1.0f;
@@ -231,14 +237,26 @@ __global__ void __launch_bounds__(kThreads, 2)
     Unit un;
     if (!make_unit(a, cu, un, tid == 0)) {
       if (un.p == 0 && un.np == 0)  // an empty sequence: zero output rows
-        for (int idx = tid; idx < G * D; idx += kThreads)
-          a.out[((size_t)un.b * a.Hq + un.g * G + idx / D) * D + idx % D] = 0.0f;
+        for (int idx = tid; idx < V * D; idx += kThreads) {
+          const int v = idx / D;
+          a.out[(((size_t)un.b * a.T + v / G) * a.Hq + un.g * G + v % G) * D + idx % D] = 0.0f;
+        }
       continue;
     }
     const int cn = warp_pages(un.npages, w);
 
-    // -- query fragments (B operand of S^T): column n holds head n % G of the group
-    const uint16_t* qrow = a.q + ((size_t)un.b * a.Hq + un.g * G + (gid % G)) * D;
+    // -- query fragments (B operand of S^T): column n holds virtual head (n % NV) % V
+    const int qv = (gid % NV) % V;
+    const uint16_t* qrow = a.q + (((size_t)un.b * a.T + qv / G) * a.Hq + un.g * G + qv % G) * D;
+    // tokens each of this thread's two columns attends in this unit: its query token's causal
+    // (and window) limits, within the partition
+    int lo_c[2], hi_c[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int pos = un.L - a.T + vcol[j] / G, lo = window_start(pos, a.window);
+      lo_c[j] = lo > un.r.start ? lo : un.r.start;
+      hi_c[j] = pos + 1 < un.r.end ? pos + 1 : un.r.end;
+    }
     uint32_t qf[T::kKS][2];
     float score_scale = a.scale * kLog2e;  // applied to the MMA result (log2 domain)
     if constexpr (FMT == DA_KV_BF16) {
@@ -318,12 +336,11 @@ __global__ void __launch_bounds__(kThreads, 2)
           }
         }
         // -- scale, softcap, mask; sc[0], sc[1]: token gid; sc[2], sc[3]: token gid + 8
-        const bool ok0 = tok0 + gid >= un.r.start && tok0 + gid < un.r.end;
-        const bool ok1 = tok0 + gid + 8 >= un.r.start && tok0 + gid + 8 < un.r.end;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
+          const int t = tok0 + gid + (e >> 1) * 8, j = e & 1;
           const float x = cap > 0.0f ? cap_post * tanhf(sc[e] * cap_pre) : sc[e] * score_scale;
-          sc[e] = (e < 2 ? ok0 : ok1) ? x : -INFINITY;
+          sc[e] = (t >= lo_c[j] && t < hi_c[j]) ? x : -INFINITY;
         }
         // -- online softmax per column
         float alpha[2], pr[4];
@@ -354,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         // -- P^T as the B operand: hi/lo parts in C layout, transposed with movmatrix
         uint32_t pb[T::kNT][2];
-        if constexpr (G <= 4) {
+        if constexpr (NV <= 4) {
           float x[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
@@ -423,13 +440,13 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         float v = o[0][mt][e];
-        if constexpr (G == 8) v += o[T::kNT - 1][mt][e];
-        if constexpr (G == 4) v += __shfl_xor_sync(kFull, v, 2);
-        if constexpr (G == 2) v += __shfl_xor_sync(kFull, v, 1);
-        if constexpr (G == 1) v += (e & 1) ? 0.0f : o[0][mt][e + 1];
+        if constexpr (NV == 8) v += o[T::kNT - 1][mt][e];
+        if constexpr (NV == 4) v += __shfl_xor_sync(kFull, v, 2);
+        if constexpr (NV == 2) v += __shfl_xor_sync(kFull, v, 1);
+        if constexpr (NV == 1) v += (e & 1) ? 0.0f : o[0][mt][e + 1];
         const int col = 2 * tig + (e & 1);
         const int rowd = FMT == DA_KV_BF16 ? 16 * mt + gid + ((e >> 1) ? 8 : 0) : 16 * mt + 2 * gid + (e >> 1);
-        if (col < G) ep_o[(w * G + col) * DP + rowd] = v;
+        if (col < V) ep_o[(w * NV + col) * DP + rowd] = v;
       }
     if (gid == 0) {
 #pragma unroll
@@ -441,20 +458,20 @@ __global__ void __launch_bounds__(kThreads, 2)
     __syncthreads();
     // -- merge the four warps: the unit's partial (split sequence) or its output (unsplit)
     const bool direct = un.np == 1;
-    for (int idx = tid; idx < G * D; idx += kThreads) {
-      const int h = idx / D, d = idx % D;
+    for (int idx = tid; idx < V * D; idx += kThreads) {
+      const int v = idx / D, d = idx % D;
       float M = -INFINITY;
 #pragma unroll
-      for (int ww = 0; ww < kWarps; ++ww) M = fmaxf(M, ep_m[ww * 8 + h]);
+      for (int ww = 0; ww < kWarps; ++ww) M = fmaxf(M, ep_m[ww * 8 + v]);
       float acc = 0.0f, l = 0.0f;
 #pragma unroll
       for (int ww = 0; ww < kWarps; ++ww) {
-        const float mw = ep_m[ww * 8 + h];
+        const float mw = ep_m[ww * 8 + v];
         const float wt = mw == -INFINITY ? 0.0f : exp2f(mw - M);
-        acc += wt * ep_o[(ww * G + h) * DP + d];
-        l += wt * ep_l[ww * 8 + h];
+        acc += wt * ep_o[(ww * NV + v) * DP + d];
+        l += wt * ep_l[ww * 8 + v];
       }
-      const size_t bh = (size_t)un.b * a.Hq + un.g * G + h;
+      const size_t bh = ((size_t)un.b * a.T + v / G) * a.Hq + un.g * G + v % G;
       if (direct) {
         a.out[bh * D + d] = l > 0.0f ? acc * out_scale / l : 0.0f;
       } else {
@@ -478,19 +495,75 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       __syncthreads();
       if (ep_flag) {
-        for (int idx = tid; idx < G * D; idx += kThreads) {
-          const int h = idx / D, d = idx % D;
-          const size_t base = ((size_t)un.b * a.Hq + un.g * G + h) * a.P;
+        // (1) per virtual head, warps over partitions: M = max_p m_p and the sum of l_p 2^(m_p - M)
+        float* red_m = ep_m;  // [8] (the warps' per-column values are no longer needed)
+        float* red_l = ep_l;  // [8]
+        for (int v = w; v < V; v += kWarps) {
+          const size_t base = (((size_t)un.b * a.T + v / G) * a.Hq + un.g * G + v % G) * a.P;
           float M = -INFINITY;
-          for (int pp = 0; pp < un.np; ++pp) M = fmaxf(M, __ldcg(a.part_m + base + pp));
-          float acc = 0.0f, l = 0.0f;
-          for (int pp = 0; pp < un.np; ++pp) {
+          for (int pp = lane; pp < un.np; pp += 32) M = fmaxf(M, __ldcg(a.part_m + base + pp));
+#pragma unroll
+          for (int o2 = 16; o2 > 0; o2 >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o2));
+          float l = 0.0f;
+          for (int pp = lane; pp < un.np; pp += 32) {
             const float mp = __ldcg(a.part_m + base + pp);
-            const float wt = mp == -INFINITY ? 0.0f : exp2f(mp - M);
-            l += wt * __ldcg(a.part_l + base + pp);
-            acc += wt * __ldcg(a.part_o + (base + pp) * D + d);
+            l += mp == -INFINITY ? 0.0f : exp2f(mp - M) * __ldcg(a.part_l + base + pp);
           }
-          a.out[((size_t)un.b * a.Hq + un.g * G + h) * D + d] = l > 0.0f ? acc * out_scale / l : 0.0f;
+#pragma unroll
+          for (int o2 = 16; o2 > 0; o2 >>= 1) l += __shfl_xor_sync(kFull, l, o2);
+          if (lane == 0) {
+            red_m[v] = M;
+            red_l[v] = l;
+          }
+        }
+        __syncthreads();
+        // (2) out = sum_p 2^(m_p - M) o_p / that sum, partitions in chunks of 32 whose weights
+        //     sit in shared memory, the loads of a chunk independent of each other
+        constexpr int kChunk = 32;
+        float* wgt = ep_o;  // [V][kChunk], reusing the merge buffer
+        constexpr int kOut = (NV * D + kThreads - 1) / kThreads;
+        float acc[kOut];
+#pragma unroll
+        for (int k = 0; k < kOut; ++k) acc[k] = 0.0f;
+        for (int p0 = 0; p0 < un.np; p0 += kChunk) {
+          for (int i = tid; i < V * kChunk; i += kThreads) {
+            const int v = i / kChunk, pp = p0 + i % kChunk;
+            const size_t base = (((size_t)un.b * a.T + v / G) * a.Hq + un.g * G + v % G) * a.P;
+            const float mp = pp < un.np ? __ldcg(a.part_m + base + pp) : -INFINITY;
+            wgt[i] = mp == -INFINITY ? 0.0f : exp2f(mp - red_m[v]);
+          }
+          __syncthreads();
+          const int n = un.np - p0 < kChunk ? un.np - p0 : kChunk;
+#pragma unroll
+          for (int k = 0; k < kOut; ++k) {
+            const int idx = tid + k * kThreads;
+            if (idx < V * D) {
+              const int v = idx / D, d = idx % D;
+              const float* src =
+                  a.part_o + ((((size_t)un.b * a.T + v / G) * a.Hq + un.g * G + v % G) * a.P + p0) * D + d;
+              float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f, s3 = 0.0f;
+              int pp = 0;
+              for (; pp + 4 <= n; pp += 4) {
+                s0 += wgt[v * kChunk + pp] * __ldcg(src + (size_t)pp * D);
+                s1 += wgt[v * kChunk + pp + 1] * __ldcg(src + (size_t)(pp + 1) * D);
+                s2 += wgt[v * kChunk + pp + 2] * __ldcg(src + (size_t)(pp + 2) * D);
+                s3 += wgt[v * kChunk + pp + 3] * __ldcg(src + (size_t)(pp + 3) * D);
+              }
+              for (; pp < n; ++pp) s0 += wgt[v * kChunk + pp] * __ldcg(src + (size_t)pp * D);
+              acc[k] += (s0 + s1) + (s2 + s3);
+            }
+          }
+          __syncthreads();
+        }
+#pragma unroll
+        for (int k = 0; k < kOut; ++k) {
+          const int idx = tid + k * kThreads;
+          if (idx < V * D) {
+            const int v = idx / D, d = idx % D;
+            const size_t bh = ((size_t)un.b * a.T + v / G) * a.Hq + un.g * G + v % G;
+            const float l = red_l[v];
+            a.out[bh * D + d] = l > 0.0f ? acc[k] * out_scale / l : 0.0f;
+          }
         }
       }
     }
@@ -529,44 +602,34 @@ bool encode_cache_map(CUtensorMap* map, const void* base, int elem_bytes, int D,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int FMT, int D, int G>
+template <int FMT, int D, int NV>
 cudaError_t launch_fixed(const Args& a, cudaStream_t s) {
-  using T = Tc<FMT, D, G>;
+  using T = Tc<FMT, D, NV>;
   CUtensorMap km, vm;
   const long long rows = (long long)a.num_blocks * a.Hkv * kPage;
   if (!encode_cache_map(&km, a.k_cache, T::kElemBytes, D, rows) ||
       !encode_cache_map(&vm, a.v_cache, T::kElemBytes, D, rows))
     return cudaErrorInvalidValue;
-  auto kern = partition_tc_kernel<FMT, D, G>;
+  auto kern = partition_tc_kernel<FMT, D, NV>;
   static DeviceFlags attr;
   cudaError_t e = ensure_dynamic_smem(kern, T::kSmem, attr);
   if (e != cudaSuccess) return e;
-  // persistent grid: as many CTAs as fit on the GPU at once (never more than the units)
-  static int resident[64] = {};
-  int dev = 0;
-  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-  int& ctas = resident[dev & 63];
-  if (ctas == 0) {
-    int per_sm = 0, sms = 0;
-    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, T::kSmem)) != cudaSuccess)
-      return e;
-    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-    ctas = (per_sm > 0 ? per_sm : 1) * sms;
-  }
+  // one CTA per work unit: the unit loop of the kernel then runs once per CTA, and a
+  // CTA's start-up loads overlap with other CTAs' streaming
   const long long units = (long long)a.P * a.B * a.Hkv;
-  const int grid = (int)(units < ctas ? units : ctas);
+  if (units > 0x7fffffffll) return cudaErrorInvalidValue;
+  const int grid = (int)units;
   kern<<<grid, kThreads, T::kSmem, s>>>(a, km, vm);
   return cudaGetLastError();
 }
 
 template <int FMT, int D>
 cudaError_t launch_g(const Args& a, cudaStream_t s) {
-  switch (a.Hq / a.Hkv) {
-    case 1: return launch_fixed<FMT, D, 1>(a, s);
-    case 2: return launch_fixed<FMT, D, 2>(a, s);
-    case 4: return launch_fixed<FMT, D, 4>(a, s);
-    case 8: return launch_fixed<FMT, D, 8>(a, s);
-  }
+  const int v = a.T * (a.Hq / a.Hkv);  // virtual heads, padded to a power of two
+  if (v <= 1) return launch_fixed<FMT, D, 1>(a, s);
+  if (v <= 2) return launch_fixed<FMT, D, 2>(a, s);
+  if (v <= 4) return launch_fixed<FMT, D, 4>(a, s);
+  if (v <= 8) return launch_fixed<FMT, D, 8>(a, s);
   return cudaErrorInvalidValue;
 }
 

@@ -22,20 +22,20 @@ namespace {
 
 template <int D, bool kUnrotate>
 __global__ void __launch_bounds__(128) reduce_kernel(const Args a) {
-  const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x, lane = tid & 31;
+  const int h = blockIdx.x, row = blockIdx.y, tid = threadIdx.x, lane = tid & 31;  // row = b * T + query token
+  const int b = row / a.T;
   extern __shared__ float w_s[];  // [P] weights
   __shared__ float x_s[D];
   __shared__ float inv_l_s;
   const int L = load_len(a, b, false);
-  const int start = attended_start(L, a.window);
-  const int np = num_partitions(L - start, a.psize, a.thresh);
-  float* out = a.out + ((size_t)b * a.Hq + h) * D;
+  const int np = seq_partitions(L, a.T, a.window, a.psize, a.thresh);
+  float* out = a.out + ((size_t)row * a.Hq + h) * D;
   if (np == 0) {
     for (int d = tid; d < D; d += blockDim.x) out[d] = 0.0f;
     return;
   }
   if (np == 1 && !kUnrotate) return;
-  const size_t base = ((size_t)b * a.Hq + h) * a.P;
+  const size_t base = ((size_t)row * a.Hq + h) * a.P;
   if (tid < 32) {
     float M = -INFINITY;
     for (int p = lane; p < np; p += 32) M = fmaxf(M, a.part_m[base + p]);
@@ -70,7 +70,7 @@ __global__ void __launch_bounds__(128) reduce_kernel(const Args a) {
 
 template <int D>
 cudaError_t launch_d(const Args& a, cudaStream_t s) {
-  dim3 grid(a.Hq, a.B);
+  dim3 grid(a.Hq, a.B * a.T);
   const size_t smem = sizeof(float) * (size_t)a.P;  // P <= kMaxPartitions: within the default 48 KB
   if (is_codebook(v_side(a.fmt)))
     reduce_kernel<D, true><<<grid, 128, smem, s>>>(a);

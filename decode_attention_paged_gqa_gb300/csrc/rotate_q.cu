@@ -16,9 +16,9 @@ namespace {
 
 template <int D>
 __global__ void __launch_bounds__(128) rotate_q_kernel(const Args a) {
-  const int h = blockIdx.x, b = blockIdx.y;
+  const int h = blockIdx.x, row = blockIdx.y;  // row = b * T + query token
   __shared__ float x[D];
-  const size_t base = ((size_t)b * a.Hq + h) * D;
+  const size_t base = ((size_t)row * a.Hq + h) * D;
   for (int d = threadIdx.x; d < D; d += blockDim.x) x[d] = bf16_to_f32(a.q[base + d]) * __ldg(a.sign + d);
   fwht_shared<D>(x);
   const float inv_sqrt_d = 1.0f / sqrtf((float)D);
@@ -28,7 +28,7 @@ __global__ void __launch_bounds__(128) rotate_q_kernel(const Args a) {
 }  // namespace
 
 cudaError_t launch_rotate_q(const Args& a, cudaStream_t s) {
-  dim3 grid(a.Hq, a.B);
+  dim3 grid(a.Hq, a.B * a.T);
   if (a.D == 128)
     rotate_q_kernel<128><<<grid, 128, 0, s>>>(a);
   else

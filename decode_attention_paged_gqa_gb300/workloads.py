@@ -44,6 +44,7 @@ class WorkloadSpec:
     partition_size: int = 512
     split_threshold: int = 1024
     pool_blocks: Optional[int] = None      # fixed physical pool size (else the sum of pages needed)
+    query_len: int = 1         # query tokens per sequence (the last ones of the context)
 
     @property
     def scale(self) -> float:
@@ -117,9 +118,10 @@ def make_layout(spec: WorkloadSpec, lens=None) -> PagedLayout:
 
 
 def make_query(spec: WorkloadSpec) -> torch.Tensor:
-    """q [B, Hq, D], iid N(0, 1) rounded to bf16."""
+    """q [B, Hq, D] (or [B, T, Hq, D] with T = query_len > 1), iid N(0, 1) rounded to bf16."""
     g = _gen(_sub_seed(spec.seed, 3))
-    return torch.randn((spec.batch, spec.num_q_heads, spec.head_dim), generator=g).to(torch.bfloat16)
+    shape = (spec.batch,) + ((spec.query_len,) if spec.query_len > 1 else ()) + (spec.num_q_heads, spec.head_dim)
+    return torch.randn(shape, generator=g).to(torch.bfloat16)
 
 
 def kv_source(spec: WorkloadSpec, which: str, num_blocks: int, first: int = 0, count: Optional[int] = None):

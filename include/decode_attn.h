@@ -87,6 +87,10 @@ enum da_status {
 
 typedef struct da_params {
   int32_t batch;              /* B >= 0 sequences (B == 0: nothing to do) */
+  int32_t query_len;          /* T >= 1 query tokens per sequence (0 counts as 1). T = 1 is ordinary
+                                 decode; T > 1 is multi-token decode with a causal mask: query token j
+                                 sits at position L_b - T + j and attends positions up to its own (the
+                                 last `window` of them when a window is set). T * G <= 8. */
   int32_t num_q_heads;        /* Hq >= 1 */
   int32_t num_kv_heads;       /* Hkv >= 1, Hq % Hkv == 0; group size G = Hq / Hkv in {1, 2, 4, 8} */
   int32_t head_dim;           /* D in {128, 256} */
@@ -106,10 +110,11 @@ typedef struct da_params {
 } da_params;
 
 /* Bytes of workspace a call with these parameters needs (0 if the parameters are invalid).
- * The workspace holds the error word, the rotated queries of the codebook format
- * ([B][Hq][D] f32) and the split-K partials: output [B][Hq][P][D] f32 (unnormalised),
- * running max and running sum [B][Hq][P] f32, where P is the partition count of a
- * sequence of length max_context_len (the page's partial buffers, sized for a batch). */
+ * The workspace holds the error word, the rotated queries of the codebook formats
+ * ([B][T][Hq][D] f32), the split-K partials -- output [B][T][Hq][P][D] f32 (unnormalised),
+ * running max and running sum [B][T][Hq][P] f32, where P is the partition count of a
+ * sequence of length max_context_len (the page's partial buffers, sized for a batch) -- and
+ * one completion counter per (sequence, kv head). */
 size_t decode_attn_workspace_bytes(const da_params* p);
 
 /* Zero the workspace (in particular its error word) on `stream`. Call once after
@@ -117,7 +122,7 @@ size_t decode_attn_workspace_bytes(const da_params* p);
 int decode_attn_workspace_init(const da_params* p, void* stream);
 
 /* Full decode attention: [codebook format: query rotation] -> partition kernel -> reduce.
- *   q            [B][Hq][D] bf16, the single query token of each sequence (16-byte aligned).
+ *   q            [B][T][Hq][D] bf16, the query tokens of each sequence (16-byte aligned).
  *   k_cache,
  *   v_cache      the paged caches, layout by format (enum da_kv_format), 16-byte aligned;
  *                num_blocks * Hkv * block_size must stay below 2^31.
@@ -130,10 +135,12 @@ int decode_attn_workspace_init(const da_params* p, void* stream);
  *                block_tables[b][i]; token t of sequence b is slot t % block_size of page
  *                t / block_size. Only the pages holding attended tokens are read.
  *   context_lens [B] int32: L_b, tokens in sequence b. L_b == 0 gives an all-zero output row.
- *   out          [B][Hq][D] f32, fully written.
- * Partitioning: with n_b = attended length (min(L_b, window) when window > 0, else L_b), the
- * sequence is split iff partition_size > 0 and n_b >= split_threshold, into ceil(n_b /
- * partition_size) partitions counted from the first attended token. */
+ *   out          [B][T][Hq][D] f32, fully written (rows of query tokens that attend nothing,
+ *                i.e. L_b == 0 or position < 0, are zero).
+ * Partitioning: the span attended by the sequence's query tokens runs from the first query
+ * token's first attended position to L_b; with n_b its length (min(L_b, window + T - 1) with
+ * a window), the sequence is split iff partition_size > 0 and n_b >= split_threshold, into
+ * ceil(n_b / partition_size) partitions counted from the span start. */
 int decode_attn_paged(const void* q, const void* k_cache, const void* v_cache, const float* k_scales,
                       const float* v_scales, const float* codebook, const float* sign_pattern,
                       const int32_t* block_tables, const int32_t* context_lens, float* out, const da_params* p,

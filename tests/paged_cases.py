@@ -57,7 +57,8 @@ def params_for(c: dict, **override):
     kw = dict(batch=s.batch, num_q_heads=s.num_q_heads, num_kv_heads=s.num_kv_heads, head_dim=s.head_dim,
               num_blocks=c["num_blocks"], max_blocks_per_seq=c["bt"].shape[1], max_context_len=s.ctx_max,
               kv_format=s.kv_format, softmax_scale=s.scale, softcap=s.softcap, window=s.window,
-              partition_size=s.partition_size, split_threshold=s.split_threshold, block_size=s.block_size)
+              partition_size=s.partition_size, split_threshold=s.split_threshold, block_size=s.block_size,
+              query_len=s.query_len)
     kw.update(override)
     return da.make_params(**kw)
 
@@ -81,7 +82,7 @@ def run_gpu(c: dict, dev: dict | None = None, params=None, check_device_error=Tr
     da.attach_workspace(p, ws)
     da.decode_attn_workspace_init(p)
     s = c["spec"]
-    out = torch.full((s.batch, s.num_q_heads, s.head_dim), float("nan"), dtype=torch.float32, device="cuda")
+    out = torch.full(tuple(c["q"].shape), float("nan"), dtype=torch.float32, device="cuda")
     da.decode_attn_paged(dev["q"], dev["k"], dev["v"], dev["k_scales"], dev["v_scales"], dev["codebook"],
                          dev["sign"], dev["bt"], dev["lens"], out, p)
     err = da.decode_attn_get_device_error(p)

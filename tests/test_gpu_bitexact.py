@@ -30,9 +30,10 @@ def _ws(p):
     return ws
 
 
-@pytest.mark.parametrize("window,psize,thresh", [(0, 512, 1024), (4096, 512, 1024), (1000, 100, 1), (0, 0, 1024),
-                                                 (333, 16, 17)])
-def test_partition_bounds_match_oracle(window, psize, thresh):
+@pytest.mark.parametrize("window,psize,thresh,T", [(0, 512, 1024, 1), (4096, 512, 1024, 1), (1000, 100, 1, 1),
+                                                   (0, 0, 1024, 1), (333, 16, 17, 1), (4096, 512, 1024, 4),
+                                                   (1000, 100, 1, 8), (0, 512, 1024, 2)])
+def test_partition_bounds_match_oracle(window, psize, thresh, T):
     lens = np.array(sorted(set(list(range(0, 2100, 7)) + [4095, 4096, 4097, 8191, 8192, 9000, 16384, 32768])),
                     np.int32)
     B = len(lens)
@@ -40,7 +41,7 @@ def test_partition_bounds_match_oracle(window, psize, thresh):
                            split_threshold=thresh)
     p = da.make_params(batch=B, num_q_heads=8, num_kv_heads=8, head_dim=128, num_blocks=1,
                        max_blocks_per_seq=spec.max_blocks_per_seq, max_context_len=32768, kv_format="bf16",
-                       softmax_scale=0.1, window=window, partition_size=psize, split_threshold=thresh)
+                       softmax_scale=0.1, window=window, partition_size=psize, split_threshold=thresh, query_len=T)
     ws = _ws(p)
     P = da.decode_attn_max_partitions(p)
     bounds = torch.full((B, P, 2), -7, dtype=torch.int32, device="cuda")
@@ -48,7 +49,7 @@ def test_partition_bounds_match_oracle(window, psize, thresh):
     got = bounds.cpu().numpy()
     assert da.decode_attn_get_device_error(p) == 0
     for b, L in enumerate(lens):
-        ref = oracle.partition_bounds(int(L), window, psize, thresh)
+        ref = oracle.partition_bounds(int(L), window, psize, thresh, query_len=T)
         assert len(ref) <= P
         for i in range(P):
             exp = ref[i] if i < len(ref) else (-1, -1)

@@ -91,3 +91,27 @@ def test_query_magnitudes(fmt, qscale):
     c["q"] = (c["q"].float() * qscale).to(torch.bfloat16)
     assert_close(run_gpu(c, softmax_scale=1.0 / (qscale * math.sqrt(128))), run_oracle(
         c, softmax_scale=1.0 / (qscale * math.sqrt(128))), f"{fmt} q x{qscale}")
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "fp8", "cb4", "fp8k_cb4v"])
+@pytest.mark.parametrize("T,G,window", [(2, 4, 0), (4, 2, 0), (3, 2, 700), (8, 1, 0), (2, 1, 1000), (5, 1, 64)])
+def test_multi_token_causal(fmt, T, G, window):
+    """T query tokens per sequence at positions L-T .. L-1, each attending positions up to its
+    own (multi-token / speculative decode)."""
+    lens = [3, 17, 600, 1024, 1030, 2500]  # includes fewer tokens than queries
+    spec = wl.WorkloadSpec(f"mt_{fmt}", len(lens), 2 * G, 2, 128, fmt, 0, max(lens), seed=T * 10 + G, window=window,
+                           query_len=T)
+    c = make_case(spec, wl.make_layout(spec, lens=lens))
+    out = run_gpu(c)
+    assert out.shape == (len(lens), T, 2 * G, 128)
+    assert_close(out, run_oracle(c), f"{fmt} T{T} G{G} W{window}")
+
+
+def test_multi_token_group_too_wide_is_rejected():
+    import decode_attention_paged_gqa_gb300 as da
+
+    spec = wl.WorkloadSpec("wide", 2, 8, 2, 128, "bf16", 10, 40, seed=1, query_len=3)  # 3 x 4 > 8
+    c = make_case(spec)
+    with pytest.raises(da.DecodeAttnError) as e:
+        run_gpu(c)
+    assert e.value.status == da._binding.DA_ERR_UNSUPPORTED

@@ -368,9 +368,9 @@ def main():
     stream = torch.cuda.current_stream()
     call = (dev["q"], dev["k"], dev["v"], dev["k_scales"], dev["v_scales"], dev["codebook"], dev["sign"], dev["bt"],
             dev["lens"], out, p)
-    # kernels per step: BF16 / FP8 run one persistent partition kernel that also reduces;
-    # formats with codebook keys add the query rotation, codebook values the reduce kernel
-    kernels_per_step = {"bf16": 1, "fp8": 1, "cb4": 3, "fp8k_cb4v": 2, "cb3k_cb4v": 3}[spec.kv_format]
+    # kernels per step: the partition kernel and the reduce, plus the query rotation for
+    # formats whose keys are stored on the rotated basis
+    kernels_per_step = {"bf16": 2, "fp8": 2, "cb4": 3, "fp8k_cb4v": 2, "cb3k_cb4v": 3}[spec.kv_format]
 
     def step(ev=None):
         da.decode_attn_rotate_q(*call, stream=stream)

@@ -40,8 +40,6 @@ struct Args {
   float* part_o;              // [B][T][Hq][P][D], unnormalised partial outputs
   float* part_m;              // [B][T][Hq][P], running max in log2 units
   float* part_l;              // [B][T][Hq][P], running sum of 2^(s - m)
-  unsigned long long* tickets;  // [B][Hkv]: (call generation << 32) | partitions finished
-  unsigned gen;               // this call's generation (never 0)
 };
 
 // First position attended by a query token at position `pos`: with a window of W tokens,
@@ -113,7 +111,7 @@ __device__ __forceinline__ float bf16_to_f32(uint16_t h) { return __uint_as_floa
 
 // Workspace layout; every piece starts on a 256-byte boundary.
 struct Layout {
-  size_t err, q_rot, part_o, part_m, part_l, tickets, total;
+  size_t err, q_rot, part_o, part_m, part_l, total;
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -144,8 +142,6 @@ inline Layout workspace_layout(const da_params& p) {
   off = align256(off + BH * P * sizeof(float));
   l.part_l = off;
   off = align256(off + BH * P * sizeof(float));
-  l.tickets = off;
-  off = align256(off + (size_t)p.batch * p.num_kv_heads * sizeof(unsigned long long));
   l.total = off;
   return l;
 }

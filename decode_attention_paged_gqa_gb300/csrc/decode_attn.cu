@@ -19,16 +19,6 @@ using namespace da;
 
 namespace {
 
-// A fresh nonzero number per call: the split-K completion tickets in the workspace carry
-// it, so counts left behind by an earlier call never mix with this call's.
-unsigned next_generation() {
-  static std::atomic<unsigned> g{0};
-  unsigned v;
-  do v = g.fetch_add(1, std::memory_order_relaxed) + 1;
-  while (v == 0);
-  return v;
-}
-
 int check_params(const da_params* p) {
   if (!p) return DA_ERR_INVALID_ARG;
   if (p->batch < 0 || p->query_len < 0 || p->num_q_heads <= 0 || p->num_kv_heads <= 0 || p->head_dim <= 0 ||
@@ -108,8 +98,6 @@ Args make_args(const void* q, const void* k, const void* v, const float* ks, con
   a.part_o = reinterpret_cast<float*>(ws + l.part_o);
   a.part_m = reinterpret_cast<float*>(ws + l.part_m);
   a.part_l = reinterpret_cast<float*>(ws + l.part_l);
-  a.tickets = reinterpret_cast<unsigned long long*>(ws + l.tickets);
-  a.gen = next_generation();
   return a;
 }
 

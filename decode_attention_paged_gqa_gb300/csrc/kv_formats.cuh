@@ -3,7 +3,7 @@
 // Walsh-Hadamard codebook formats, alone or mixed as FP8 K + 4-bit V and 3-bit K +
 // 4-bit V). Codebook sides are dequantised in their rotated basis only: coordinate d is
 // scale_t * codebook[idx_d] (turboquant-rs 0.4.1, src/cache/cuda/attention.rs: the fused
-// kernel "reads directly from the compressed KV-cache (no full dequantization needed)").
+// kernel works on the compressed cache as stored and never dequantises it in full).
 #pragma once
 
 #include <cuda_fp16.h>

@@ -1,14 +1,15 @@
 // reduce.cu -- the float-precision reduce across split-K partitions (attention.rs README:
-// the Split-K decode kernels of every format share "a common float-precision reduce
-// kernel"; turboquant-rs 0.4.1, src/cache/cuda/attention.rs: partial_out / partial_max /
-// partial_sum buffers of [heads * partitions]).
+// one reduce kernel, in fp32, is shared by the split-K decode kernels of all formats;
+// turboquant-rs 0.4.1, src/cache/cuda/attention.rs: partial output, max and sum buffers of
+// [heads * partitions]).
 //
 // For sequence b, head h with partials (o_p, m_p, l_p), p < P_b (m in log2 units):
 //   M = max_p m_p,  w_p = 2^(m_p - M),  out = sum_p w_p o_p / sum_p w_p l_p.
-// An empty sequence gets an all-zero row. Used for the formats with a codebook side; the
-// BF16 and FP8 paths reduce inside their partition kernel. For the codebook format the result is still in the
-// rotated basis and is un-rotated here when the values are stored on it: out <- diag(sign)
-// H out / sqrt(D). For an FP8 value side the per-tensor V scale is applied once, here.
+// An empty sequence (or a query token that attends nothing) gets an all-zero row. An
+// unsplit sequence of a format without a codebook value side was written by the partition
+// kernel and is skipped here. When the values are stored on the rotated basis the result
+// is un-rotated here: out <- diag(sign) H out / sqrt(D). For an FP8 value side the
+// per-tensor V scale is applied once, here.
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -82,9 +83,6 @@ cudaError_t launch_d(const Args& a, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_reduce(const Args& a, cudaStream_t s) {
-  // BF16 / FP8: the tensor-core partition kernel finishes each split sequence itself (the
-  // last partition of a sequence and kv head to complete combines the partials)
-  if (a.fmt == DA_KV_BF16 || a.fmt == DA_KV_FP8_E4M3) return cudaSuccess;
   return a.D == 128 ? launch_d<128>(a, s) : launch_d<256>(a, s);
 }
 

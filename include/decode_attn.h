@@ -9,9 +9,9 @@
  * into partitions, each producing a partial output with its running max and sum, and a
  * float reduce combines them.
  *   - Operation, formats, split-K + float reduce, features: attention.rs README,
- *     "KV Cache Formats" table and the sentence under it ("dedicated Split-K decode
- *     kernels (triggered at 1024+ context length) ... sharing a common float-precision
- *     reduce kernel"); "Features: Softcapping, sliding window, GQA/MQA, paged block tables".
+ *     "KV Cache Formats" table and the paragraph under it (split-K decode kernels per
+ *     format, used from 1024 tokens of context, with one fp32 reduce shared by all), and
+ *     its feature list (softcap, sliding window, GQA/MQA, paged block tables).
  *   - Two-phase structure, partition size 512, ceil(kv_len / 512) partitions, partial
  *     output/max/sum buffers, f32 output [heads, head_dim], zero output for an empty
  *     context, codebook + sign_pattern inputs of the codebook format: turboquant-rs 0.4.1,

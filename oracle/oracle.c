@@ -442,8 +442,8 @@ int or_partition_bounds_span(int start, int L, int partition_size, int split_thr
 }
 
 /* First position attended by a query token at position `pos`: with a window of W tokens
- * only positions t with pos - W < t <= pos are attended (reading: "only the last W tokens"
- * of the context seen by that query, W of them including itself); else all t <= pos. */
+ * only positions t with pos - W < t <= pos are attended (reading: the window is the W most
+ * recent positions that query sees, its own included); else all t <= pos. */
 static int or_window_start(int pos, int window) {
   int a = window > 0 ? pos + 1 - window : 0;
   return a > 0 ? a : 0;

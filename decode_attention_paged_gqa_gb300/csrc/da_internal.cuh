@@ -174,7 +174,7 @@ int run_phases(int phases, const void* q, const void* k, const void* v, const fl
 cudaError_t launch_rotate_q(const Args& a, cudaStream_t s);
 cudaError_t launch_partition(const Args& a, cudaStream_t s);     // dispatches on the format:
 cudaError_t launch_partition_tc(const Args& a, cudaStream_t s);  //   BF16, FP8: TMA + tensor cores
-cudaError_t launch_partition_simt(const Args& a, cudaStream_t s);  // CB4: CUDA cores
+cudaError_t launch_partition_cb(const Args& a, cudaStream_t s);  //   4-bit codebook values: lookup tables + tensor cores
 cudaError_t launch_reduce(const Args& a, cudaStream_t s);
 cudaError_t launch_encode_fp8(const float* x, long long n, uint8_t* codes, float* scale, cudaStream_t s);
 cudaError_t launch_encode_codebook(const float* x, long long nvec, int D, int bits, const float* sign,

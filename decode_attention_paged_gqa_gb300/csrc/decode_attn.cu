@@ -59,6 +59,9 @@ int check_tensors(const void* q, const void* k, const void* v, const float* ks, 
   if (!aligned(k, 16) || !aligned(v, 16) || !aligned(q, 16) || !aligned(out, 4) || !aligned(bt, 4) ||
       !aligned(lens, 4))
     return DA_ERR_INVALID_ARG;
+  // per-token norms of a codebook side are copied 16 tokens (64 bytes) at a time
+  if ((is_codebook(k_side(p->kv_format)) && !aligned(ks, 16)) || (is_codebook(v_side(p->kv_format)) && !aligned(vs, 16)))
+    return DA_ERR_INVALID_ARG;
   return DA_OK;
 }
 

@@ -1,0 +1,649 @@
+// partition_cb.cu -- split-K partition kernel for the formats whose values are stored as
+// 4-bit codebook indices on the random-sign Walsh-Hadamard basis: 4-bit K and V, FP8 K +
+// 4-bit V, 3-bit K + 4-bit V. Tensor-core MMAs on operands dequantised through a shared-
+// memory lookup table.
+//
+// One CTA per (partition p, kv head g, sequence b), four warps; the partition's pages are
+// dealt round-robin to the warps, each with its own pipeline of shared-memory stages filled
+// by TMA / bulk copies (a page's K codes, V codes and their per-token norms) and signalled on
+// an mbarrier, as in the BF16 / FP8 kernel. Per page a warp computes, in the rotated basis
+// (the keys' and values' own basis, no dequantisation to the original one):
+//   S^T[16 tokens x 8 cols] = K_rot[16 x D] . Q_rot^T     then  s_t *= ||k_t||
+//   O^T[D x 8 cols]        += V_rot^T[D x 16] . (P ||v||)^T
+// with mma.m16n8k16 on f16 operands and fp32 accumulators. A codebook operand is built
+// from its codes with one shared-memory load per byte: a 256-entry table maps a byte (two
+// 4-bit codes) to the f16 pair (cb[lo], cb[hi]) -- for 3-bit keys a 64-entry table maps a
+// 6-bit pair of codes. Each table is replicated 32 times, copy l in bank l, so the lanes of
+// a warp never conflict whatever codes they look up.
+//
+// The dot product's coordinate order is free, so each thread takes the coordinates that
+// sit in a contiguous run of its key rows: thread (gid, tig) reads D/8 bytes of K rows gid
+// and gid + 8, which hold the k-columns its A fragments need; Q^T's B fragments use the
+// same coordinate order. For V^T (coordinates as the MMA's M) an m-tile's rows gid and
+// gid + 8 are the two coordinates of one byte, and prmt pairs the bytes of two tokens.
+//
+// Precision: the rotated query is split q = q_hi + q_lo (both f16, after scaling by a power
+// of two), the lo half riding in the spare columns of S^T (G <= 4) or in a second MMA, so
+// the scores carry only the rounding of the codebook values to f16 (2^-12 relative); P is
+// split hi + lo as in the BF16 kernel. Partials are always written: the reduce kernel
+// un-rotates the combined output.
+//
+// (attention.rs README, KV Cache Formats table: the 4-bit Walsh-Hadamard codebook format and
+// split-K decode for it; turboquant-rs 0.4.1, src/cache/cuda/attention.rs: the fused kernel
+// reads the compressed cache as stored, with codebook and sign_pattern inputs, and writes
+// partial output, max and sum per partition.)
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <cudaTypedefs.h>
+
+#include <cfloat>
+#include <cmath>
+#include <mutex>
+
+#include "da_internal.cuh"
+#include "kv_formats.cuh"
+#include "ptx.cuh"
+
+namespace da {
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kThreads = 32 * kWarps;
+constexpr int kPage = 16;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr unsigned kFull = 0xffffffffu;
+
+constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
+
+// KS: the key side (kSideCB4, kSideFP8, kSideCB3); values are 4-bit codes. NV: the group's
+// (query token, head) pairs ("virtual heads" v = jq * G + h) padded to a power of two <= 8.
+template <int KS, int D, int NV>
+struct Cb {
+  static constexpr int kKRow = row_bytes(KS, D);  // bytes of one key row
+  static constexpr int kVRow = D / 2;             // bytes of one value row
+  static constexpr int kKBytes = kPage * kKRow;
+  static constexpr int kVBytes = kPage * kVRow;
+  static constexpr bool kKNorms = KS != kSideFP8;  // per-token key norms
+  // keys by TMA: FP8 in 128-byte swizzled slabs (read with ldmatrix), 4-bit D = 256 with the
+  // 128-byte swizzle; 4-bit D = 128 and 3-bit keys by a plain bulk copy (rows read unswizzled)
+  static constexpr bool kKTma = KS == kSideFP8 || (KS == kSideCB4 && D == 256);
+  static constexpr int kKAlign = kKTma ? 1024 : 128;
+  // values by TMA: 64-byte rows with the 64-byte swizzle (D = 128), 128-byte rows with the
+  // 128-byte swizzle (D = 256)
+  static constexpr int kVAlign = D == 256 ? 1024 : 512;
+  static constexpr int kOffV = align_up(kKBytes, kVAlign);
+  static constexpr int kOffKN = kOffV + kVBytes;
+  static constexpr int kOffVN = kOffKN + (kKNorms ? 64 : 0);
+  static constexpr int kAlign = kKAlign > kVAlign ? kKAlign : kVAlign;
+  static constexpr int kStageBytes = align_up(kOffVN + 64, kAlign);
+  static constexpr int kTxBytes = kKBytes + kVBytes + (kKNorms ? 64 : 0) + 64;
+  static constexpr int kStages = 16384 / kStageBytes;  // 16 KB of stages per warp
+  static constexpr int kNT = NV <= 4 ? 1 : 2;           // P.V column tiles
+  static constexpr int kCols = 8 * kNT;
+  static constexpr int kMT = D / 16;                    // O^T row tiles
+  static constexpr int kKS = D / 16;                    // k-steps of S^T
+  static constexpr int kLutV = 256 * 32 * 4;            // 4-bit pair table, 32 copies
+  static constexpr int kLutK = KS == kSideCB3 ? 64 * 32 * 4 : 0;
+  static constexpr int kOffStages = kLutV + kLutK;
+  static constexpr int kStageSmem = kWarps * kStages * kStageBytes;
+  static constexpr int kEpiSmem = (kWarps * kCols * D + 2 * kWarps * 8) * 4;
+  static constexpr int kBody = kOffStages + kStageSmem;
+  static constexpr int kSmem = (kBody > kEpiSmem ? kBody : kEpiSmem) + 1024;
+  static_assert(kStages >= 2, "too few stages");
+};
+
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+__device__ __forceinline__ float hi_f16(float p) { return __half2float(__float2half_rn(p)); }
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
+  __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two & 0xffffu), __NV_E4M3);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ float ldsf(uint32_t addr) { return __uint_as_float(lds32(addr)); }
+
+// Table lookup: entry e of a table whose copy for this lane starts at `lane_base`.
+__device__ __forceinline__ uint32_t lut(uint32_t lane_base, uint32_t e) { return lds32(lane_base + e * 128u); }
+// byte j of a little-endian word array
+template <int J>
+__device__ __forceinline__ uint32_t byte_of(const uint32_t* w) {
+  return __byte_perm(w[J >> 2], 0, 0x4440 | (J & 3));
+}
+// 6-bit field j (bits 6j .. 6j + 5) of a little-endian word array
+template <int J>
+__device__ __forceinline__ uint32_t field6(const uint32_t* w) {
+  constexpr int bit = 6 * J, wi = bit >> 5, sh = bit & 31;
+  if constexpr (sh <= 26)
+    return (w[wi] >> sh) & 63u;
+  else
+    return __funnelshift_r(w[wi], w[wi + 1], sh) & 63u;
+}
+
+// A fragments of S^T for k-step KS_ from the thread's key bytes (rows gid: k0, gid + 8: k1).
+template <int KS, int D, int S>
+__device__ __forceinline__ void key_frag(uint32_t (&af)[4], const uint32_t* k0, const uint32_t* k1, uint32_t lutk) {
+  if constexpr (KS == kSideCB4) {
+    af[0] = lut(lutk, byte_of<2 * S>(k0));
+    af[1] = lut(lutk, byte_of<2 * S>(k1));
+    af[2] = lut(lutk, byte_of<2 * S + 1>(k0));
+    af[3] = lut(lutk, byte_of<2 * S + 1>(k1));
+  } else {
+    af[0] = lut(lutk, field6<2 * S>(k0));
+    af[1] = lut(lutk, field6<2 * S>(k1));
+    af[2] = lut(lutk, field6<2 * S + 1>(k0));
+    af[3] = lut(lutk, field6<2 * S + 1>(k1));
+  }
+}
+
+template <int S, int N, int KS, int D, int NV>
+struct KeySteps {
+  // S^T += A(k-step S) . Q^T for S = S .. N-1 (compile-time unrolled so byte offsets are constants)
+  __device__ static __forceinline__ void run(float (&sc)[4], const uint32_t* k0, const uint32_t* k1, uint32_t lutk,
+                                             const uint32_t (*qf)[2], const uint32_t (*ql)[2]) {
+    if constexpr (S < N) {
+      uint32_t af[4];
+      key_frag<KS, D, S>(af, k0, k1, lutk);
+      ptx::mma_f16(sc, af, qf[S][0], qf[S][1]);
+      if constexpr (NV == 8) ptx::mma_f16(sc, af, ql[S][0], ql[S][1]);
+      KeySteps<S + 1, N, KS, D, NV>::run(sc, k0, k1, lutk, qf, ql);
+    }
+  }
+};
+
+template <int M, int N, int D, int NT>
+struct ValueTiles {
+  // O^T[m-tile M] += V^T(m-tile M) . P^T for M = M .. N-1
+  __device__ static __forceinline__ void run(float (&o)[NT][D / 16][4], const uint32_t (*vw)[D / 64], uint32_t lutv,
+                                             const uint32_t (&pb)[NT][2]) {
+    if constexpr (M < N) {
+      const uint32_t l0 = lut(lutv, byte_of<M>(vw[0])), l1 = lut(lutv, byte_of<M>(vw[1]));
+      const uint32_t l2 = lut(lutv, byte_of<M>(vw[2])), l3 = lut(lutv, byte_of<M>(vw[3]));
+      const uint32_t af[4] = {__byte_perm(l0, l1, 0x5410), __byte_perm(l0, l1, 0x7632), __byte_perm(l2, l3, 0x5410),
+                              __byte_perm(l2, l3, 0x7632)};
+#pragma unroll
+      for (int t = 0; t < NT; ++t) ptx::mma_f16(o[t][M], af, pb[t][0], pb[t][1]);
+      ValueTiles<M + 1, N, D, NT>::run(o, vw, lutv, pb);
+    }
+  }
+};
+
+template <int KS, int D, int NV>
+__global__ void __launch_bounds__(kThreads, 2)
+    partition_cb_kernel(const Args a, const __grid_constant__ CUtensorMap kmap,
+                        const __grid_constant__ CUtensorMap vmap) {
+  using C = Cb<KS, D, NV>;
+  const int p = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int gid = lane >> 2, tig = lane & 3;
+  const int G = a.Hq / a.Hkv, V = a.T * G;
+  const int L = load_len(a, b, p == 0 && g == 0 && tid == 0);
+  const Range r = partition_range(L, a.T, p, a.window, a.psize, a.thresh);
+  if (r.start >= r.end) return;
+
+  extern __shared__ unsigned char smem_raw[];
+  __shared__ __align__(8) uint64_t bars[kWarps * C::kStages];
+  const uint32_t smem = (ptx::smem_u32(smem_raw) + 1023u) & ~1023u;
+  unsigned char* smem_gen = smem_raw + (smem - ptx::smem_u32(smem_raw));
+  const uint32_t bar0 = ptx::smem_u32(bars) + w * C::kStages * 8;
+  const uint32_t stage0 = smem + C::kOffStages + w * C::kStages * C::kStageBytes;
+
+  if (lane == 0) {
+    if constexpr (C::kKTma) ptx::prefetch_tensor_map(&kmap);
+    ptx::prefetch_tensor_map(&vmap);
+    for (int s = 0; s < C::kStages; ++s) ptx::mbar_init(bar0 + 8 * s, 1);
+    ptx::fence_mbar_init();
+  }
+  __syncwarp();
+
+  // ---- pages of this partition and this warp's share of them
+  const int first_page = r.start / kPage, npages = (r.end - 1) / kPage - first_page + 1;
+  const int nw = npages > w ? (npages - w + kWarps - 1) / kWarps : 0;
+  int bid = -1;  // lane l: physical block of local page 32*chunk + l
+  auto load_bids = [&](int chunk) {
+    const int i = 32 * chunk + lane;
+    bid = i < nw ? load_block(a, b, first_page + w + kWarps * i) : -1;
+  };
+  load_bids(0);
+  uint32_t valid_mask = 0;  // bit s: the page in stage s has a valid block (warp-uniform)
+  auto issue = [&](int k) {  // all lanes; lane 0 issues the copies of local page k
+    if (k > 0 && (k & 31) == 0) load_bids(k >> 5);
+    const int phys = __shfl_sync(kFull, bid, k & 31);
+    const int s = k % C::kStages;
+    valid_mask = phys >= 0 ? (valid_mask | (1u << s)) : (valid_mask & ~(1u << s));
+    if (lane == 0) {
+      const uint32_t bar = bar0 + 8 * s, dst = stage0 + s * C::kStageBytes;
+      if (phys < 0) {
+        ptx::mbar_arrive(bar);  // completes the phase with nothing loaded
+      } else {
+        ptx::fence_proxy_async();
+        ptx::mbar_arrive_expect_tx(bar, C::kTxBytes);
+        const size_t unit = (size_t)phys * a.Hkv + g;  // (block, kv head): 16 consecutive rows
+        const int y = (int)unit * kPage;
+        if constexpr (KS == kSideFP8) {
+#pragma unroll
+          for (int u = 0; u < D / 128; ++u) ptx::tma_load_2d(dst + u * 2048, &kmap, u * 128, y, bar);
+        } else if constexpr (C::kKTma) {
+          ptx::tma_load_2d(dst, &kmap, 0, y, bar);
+        } else {
+          ptx::bulk_load(dst, static_cast<const uint8_t*>(a.k_cache) + unit * C::kKBytes, C::kKBytes, bar);
+        }
+        ptx::tma_load_2d(dst + C::kOffV, &vmap, 0, y, bar);
+        if constexpr (C::kKNorms) ptx::bulk_load(dst + C::kOffKN, a.k_scales + unit * kPage, 64, bar);
+        ptx::bulk_load(dst + C::kOffVN, a.v_scales + unit * kPage, 64, bar);
+      }
+    }
+  };
+  for (int k = 0; k < C::kStages && k < nw; ++k) issue(k);
+
+  // ---- lookup tables: byte -> (cb[lo], cb[hi]) for values (and 4-bit keys), 6-bit pair ->
+  //      (cbk[lo], cbk[hi]) for 3-bit keys; 32 copies, entry e of copy l at word 32 e + l
+  {
+    const float* cbv = a.codebook + (KS == kSideCB3 ? 8 : 0);
+    uint32_t* lv = reinterpret_cast<uint32_t*>(smem_gen);
+    for (int i = tid; i < 256 * 8; i += kThreads) {
+      const int e = i >> 3;
+      const uint32_t x = pack_f16(__ldg(cbv + (e & 15)), __ldg(cbv + (e >> 4)));
+      *reinterpret_cast<uint4*>(lv + e * 32 + (i & 7) * 4) = make_uint4(x, x, x, x);
+    }
+    if constexpr (KS == kSideCB3) {
+      uint32_t* lk = lv + 256 * 32;
+      for (int i = tid; i < 64 * 8; i += kThreads) {
+        const int e = i >> 3;
+        const uint32_t x = pack_f16(__ldg(a.codebook + (e & 7)), __ldg(a.codebook + (e >> 3)));
+        *reinterpret_cast<uint4*>(lk + e * 32 + (i & 7) * 4) = make_uint4(x, x, x, x);
+      }
+    }
+  }
+  const uint32_t lutv = smem + lane * 4u;
+  const uint32_t lutk = KS == kSideCB3 ? lutv + C::kLutV : lutv;
+
+  // ---- query fragments (B operand of S^T). Column n scores virtual head (n % NV) % V.
+  const int qv = (gid % NV) % V;
+  const size_t qrow = (((size_t)b * a.T + qv / G) * a.Hq + g * G + qv % G) * D;
+  uint32_t qf[C::kKS][2], ql[NV == 8 ? C::kKS : 1][2];
+  float score_scale;
+  if constexpr (KS == kSideFP8) {
+    // unrotated bf16 query, scaled by a power of two into the f16 range (exact)
+    const uint16_t* qp = a.q + qrow;
+    float x[C::kKS][4];
+    float mx = 0.0f;
+#pragma unroll
+    for (int ks = 0; ks < C::kKS; ++ks)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        x[ks][e] = bf16_to_f32(qp[16 * ks + 4 * tig + e]);
+        mx = fmaxf(mx, fabsf(x[ks][e]));
+      }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+    int ex = 0;
+    frexpf(mx, &ex);
+    const int e2 = ex > 14 ? 14 - ex : 0;
+    const float qs = ldexpf(1.0f, e2);
+#pragma unroll
+    for (int ks = 0; ks < C::kKS; ++ks) {
+      qf[ks][0] = pack_f16(x[ks][0] * qs, x[ks][1] * qs);
+      qf[ks][1] = pack_f16(x[ks][2] * qs, x[ks][3] * qs);
+    }
+    score_scale = a.scale * __ldg(a.k_scales) * ldexpf(1.0f, -e2) * kLog2e;
+  } else {
+    // rotated fp32 query: coordinates (D/4) tig + 4 ks + {0, 1} (b0) and + {2, 3} (b1),
+    // scaled by 2^e2 (max below 2^15) and split into f16 hi + lo; for NV <= 4 the columns
+    // n >= 4 carry the lo half (same heads as n - 4)
+    const float4* qp = reinterpret_cast<const float4*>(a.q_rot + qrow + (D / 4) * tig);
+    float4 x[C::kKS];
+    float mx = 0.0f;
+#pragma unroll
+    for (int ks = 0; ks < C::kKS; ++ks) {
+      x[ks] = qp[ks];
+      mx = fmaxf(fmaxf(mx, fmaxf(fabsf(x[ks].x), fabsf(x[ks].y))), fmaxf(fabsf(x[ks].z), fabsf(x[ks].w)));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+    int ex = 0;
+    frexpf(mx, &ex);
+    const int e2 = 15 - ex;
+    const float qs = ldexpf(1.0f, e2);
+    const bool lo_col = NV <= 4 && gid >= 4;
+#pragma unroll
+    for (int ks = 0; ks < C::kKS; ++ks) {
+      const float y0 = x[ks].x * qs, y1 = x[ks].y * qs, y2 = x[ks].z * qs, y3 = x[ks].w * qs;
+      const float h0 = hi_f16(y0), h1 = hi_f16(y1), h2 = hi_f16(y2), h3 = hi_f16(y3);
+      if constexpr (NV == 8) {
+        qf[ks][0] = pack_f16(h0, h1);
+        qf[ks][1] = pack_f16(h2, h3);
+        ql[ks][0] = pack_f16(y0 - h0, y1 - h1);
+        ql[ks][1] = pack_f16(y2 - h2, y3 - h3);
+      } else {
+        qf[ks][0] = lo_col ? pack_f16(y0 - h0, y1 - h1) : pack_f16(h0, h1);
+        qf[ks][1] = lo_col ? pack_f16(y2 - h2, y3 - h3) : pack_f16(h2, h3);
+      }
+    }
+    score_scale = a.scale * ldexpf(1.0f, -e2) * kLog2e;
+  }
+  const float cap = a.softcap;
+  const float cap_pre = cap > 0.0f ? 1.0f / (cap * kLog2e) : 0.0f;  // log2-domain score -> s_nat / cap
+  const float cap_post = cap * kLog2e;
+
+  // ---- running state: column c = 2*tig + j of S^T and of every O^T column tile
+  float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.0f, 0.0f};
+  float o[C::kNT][C::kMT][4];
+#pragma unroll
+  for (int t = 0; t < C::kNT; ++t)
+#pragma unroll
+    for (int mt = 0; mt < C::kMT; ++mt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) o[t][mt][e] = 0.0f;
+  // hi/lo role of this thread's two P columns (NV <= 4: column c carries part c / NV), and
+  // the tokens each column attends in this partition (its query token's causal and window
+  // limits, within [r.start, r.end))
+  int part[2], lo_c[2], hi_c[2];
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    part[j] = NV <= 4 ? (2 * tig + j) / NV : 0;
+    const int pos = L - a.T + (((2 * tig + j) % NV) % V) / G, lo = window_start(pos, a.window);
+    lo_c[j] = lo > r.start ? lo : r.start;
+    hi_c[j] = pos + 1 < r.end ? pos + 1 : r.end;
+  }
+
+  __syncthreads();  // lookup tables written
+
+  const int mi = lane >> 3, ri = lane & 7;  // ldmatrix (FP8 keys): matrix index and row of this lane's address
+  int stalled_at = -1;
+  for (int i = 0; i < nw; ++i) {
+    const int s = i % C::kStages;
+    if (!ptx::mbar_wait(bar0 + 8 * s, (i / C::kStages) & 1)) {
+      stalled_at = i;
+      break;
+    }
+    if (valid_mask & (1u << s)) {
+      const uint32_t kb = stage0 + s * C::kStageBytes, vb = kb + C::kOffV;
+      const int tok0 = (first_page + w + kWarps * i) * kPage;
+      // -- S^T = K . Q^T
+      float sc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      if constexpr (KS == kSideFP8) {
+#pragma unroll
+        for (int j2 = 0; j2 < C::kKS / 2; ++j2) {
+          const int row = ri + 8 * (mi & 1), chunk = 2 * j2 + (mi >> 1);
+          uint32_t rr[4];
+          ptx::ldmatrix_x4(rr, kb + (chunk >> 3) * 2048 + row * 128 + (((chunk & 7) ^ (row & 7)) << 4));
+          const uint32_t a0[4] = {e4m3x2_to_f16x2(rr[0]), e4m3x2_to_f16x2(rr[1]), e4m3x2_to_f16x2(rr[0] >> 16),
+                                  e4m3x2_to_f16x2(rr[1] >> 16)};
+          ptx::mma_f16(sc, a0, qf[2 * j2][0], qf[2 * j2][1]);
+          const uint32_t a1[4] = {e4m3x2_to_f16x2(rr[2]), e4m3x2_to_f16x2(rr[3]), e4m3x2_to_f16x2(rr[2] >> 16),
+                                  e4m3x2_to_f16x2(rr[3] >> 16)};
+          ptx::mma_f16(sc, a1, qf[2 * j2 + 1][0], qf[2 * j2 + 1][1]);
+        }
+      } else {
+        // the thread's key bytes: D/8 per row (4-bit) or 3D/32 (3-bit), rows gid and gid + 8
+        constexpr int kWords = KS == kSideCB4 ? D / 32 : 3 * D / 128;
+        uint32_t k0[kWords + 1], k1[kWords + 1];
+        k0[kWords] = k1[kWords] = 0u;
+        if constexpr (KS == kSideCB4 && D == 128) {
+          const uint4 x0 = lds128(kb + gid * 64 + 16 * tig), x1 = lds128(kb + (gid + 8) * 64 + 16 * tig);
+          k0[0] = x0.x, k0[1] = x0.y, k0[2] = x0.z, k0[3] = x0.w;
+          k1[0] = x1.x, k1[1] = x1.y, k1[2] = x1.z, k1[3] = x1.w;
+        } else if constexpr (KS == kSideCB4) {  // D = 256, 128-byte swizzle: chunks 2 tig, 2 tig + 1
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            const int ch = 2 * tig + c;
+            const uint4 x0 = lds128(kb + gid * 128 + ((ch ^ gid) << 4));
+            const uint4 x1 = lds128(kb + (gid + 8) * 128 + ((ch ^ gid) << 4));  // (gid + 8) & 7 == gid
+            k0[4 * c] = x0.x, k0[4 * c + 1] = x0.y, k0[4 * c + 2] = x0.z, k0[4 * c + 3] = x0.w;
+            k1[4 * c] = x1.x, k1[4 * c + 1] = x1.y, k1[4 * c + 2] = x1.z, k1[4 * c + 3] = x1.w;
+          }
+        } else {  // 3-bit: 12 (D = 128) or 24 (D = 256) bytes per row at (3D/32) tig
+#pragma unroll
+          for (int c = 0; c < kWords; ++c) {
+            k0[c] = lds32(kb + gid * C::kKRow + (3 * D / 32) * tig + 4 * c);
+            k1[c] = lds32(kb + (gid + 8) * C::kKRow + (3 * D / 32) * tig + 4 * c);
+          }
+        }
+        KeySteps<0, C::kKS, KS, D, NV>::run(sc, k0, k1, lutk, qf, ql);
+        if constexpr (NV <= 4) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) sc[e] += __shfl_xor_sync(kFull, sc[e], 2);  // hi + lo columns
+        }
+      }
+      // -- scale (and key norms), softcap, mask; sc[0], sc[1]: token gid; sc[2], sc[3]: gid + 8
+      float kn0 = 1.0f, kn1 = 1.0f;
+      if constexpr (C::kKNorms) {
+        kn0 = ldsf(kb + C::kOffKN + 4 * gid);
+        kn1 = ldsf(kb + C::kOffKN + 4 * (gid + 8));
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int t = tok0 + gid + (e >> 1) * 8, j = e & 1;
+        const float y = sc[e] * score_scale * ((e >> 1) ? kn1 : kn0);
+        const float x = cap > 0.0f ? cap_post * tanhf(y * cap_pre) : y;
+        sc[e] = (t >= lo_c[j] && t < hi_c[j]) ? x : -INFINITY;
+      }
+      // -- online softmax per column
+      float alpha[2], pr[4];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        float mx = fmaxf(sc[j], sc[j + 2]);
+        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 4));
+        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
+        const float mn = fmaxf(m_run[j], mx);
+        const bool none = mn == -INFINITY;
+        alpha[j] = none ? 1.0f : exp2f(m_run[j] - mn);
+        pr[j] = none ? 0.0f : exp2f(sc[j] - mn);
+        pr[j + 2] = none ? 0.0f : exp2f(sc[j + 2] - mn);
+        l_run[j] = l_run[j] * alpha[j] + pr[j] + pr[j + 2];
+        m_run[j] = mn;
+      }
+      if (__any_sync(kFull, alpha[0] != 1.0f || alpha[1] != 1.0f)) {
+#pragma unroll
+        for (int t = 0; t < C::kNT; ++t)
+#pragma unroll
+          for (int mt = 0; mt < C::kMT; ++mt) {
+            o[t][mt][0] *= alpha[0];
+            o[t][mt][1] *= alpha[1];
+            o[t][mt][2] *= alpha[0];
+            o[t][mt][3] *= alpha[1];
+          }
+      }
+      // -- (P * value norms)^T as the B operand: hi/lo parts in C layout, transposed with movmatrix
+      const float vn0 = ldsf(kb + C::kOffVN + 4 * gid), vn1 = ldsf(kb + C::kOffVN + 4 * (gid + 8));
+      float pv[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) pv[e] = pr[e] * ((e >> 1) ? vn1 : vn0);
+      uint32_t pb[C::kNT][2];
+      if constexpr (NV <= 4) {
+        float x[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int pt = part[e & 1];
+          const float h = hi_f16(pv[e]);
+          x[e] = pt == 0 ? h : (pt == 1 ? pv[e] - h : 0.0f);
+        }
+        pb[0][0] = ptx::movmatrix_trans(pack_f16(x[0], x[1]));
+        pb[0][1] = ptx::movmatrix_trans(pack_f16(x[2], x[3]));
+      } else {
+        float hi[4], lo[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          hi[e] = hi_f16(pv[e]);
+          lo[e] = pv[e] - hi[e];
+        }
+        pb[0][0] = ptx::movmatrix_trans(pack_f16(hi[0], hi[1]));
+        pb[0][1] = ptx::movmatrix_trans(pack_f16(hi[2], hi[3]));
+        pb[C::kNT - 1][0] = ptx::movmatrix_trans(pack_f16(lo[0], lo[1]));
+        pb[C::kNT - 1][1] = ptx::movmatrix_trans(pack_f16(lo[2], lo[3]));
+      }
+      // -- O^T += V^T . P^T: the thread's value bytes of tokens 2 tig, 2 tig + 1, 2 tig + 8,
+      //    2 tig + 9, D/16 bytes each at byte (D/16) gid
+      uint32_t vw[4][D / 64];
+#pragma unroll
+      for (int i4 = 0; i4 < 4; ++i4) {
+        const int row = 2 * tig + (i4 & 1) + 8 * (i4 >> 1);
+        if constexpr (D == 128) {  // 64-byte rows, 64-byte swizzle
+          const uint2 x = lds64(vb + row * 64 + ((((gid >> 1) ^ ((row >> 1) & 3))) << 4) + 8 * (gid & 1));
+          vw[i4][0] = x.x, vw[i4][1] = x.y;
+        } else {  // 128-byte rows, 128-byte swizzle
+          const uint4 x = lds128(vb + row * 128 + ((gid ^ (row & 7)) << 4));
+          vw[i4][0] = x.x, vw[i4][1] = x.y, vw[i4][2] = x.z, vw[i4][3] = x.w;
+        }
+      }
+      ValueTiles<0, C::kMT, D, C::kNT>::run(o, vw, lutv, pb);
+    }
+    __syncwarp();
+    if (i + C::kStages < nw) issue(i + C::kStages);
+  }
+  if (stalled_at >= 0) {
+    if (lane == 0) atomicOr(a.err, DA_DEVERR_TIMEOUT);
+    // give the copies still in flight into this warp's stages a bounded chance to land
+    for (int k = stalled_at; k < nw && k < stalled_at + C::kStages; ++k)
+      ptx::mbar_wait(bar0 + 8 * (k % C::kStages), (k / C::kStages) & 1);
+  }
+
+  // ---- merge the four warps through shared memory (tables and stages are free now)
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    l_run[j] += __shfl_xor_sync(kFull, l_run[j], 4);
+    l_run[j] += __shfl_xor_sync(kFull, l_run[j], 8);
+    l_run[j] += __shfl_xor_sync(kFull, l_run[j], 16);
+  }
+  __syncthreads();
+  float* ep_o = reinterpret_cast<float*>(smem_gen);  // [kWarps][kCols][D]
+  float* ep_m = ep_o + kWarps * C::kCols * D;          // [kWarps][8]
+  float* ep_l = ep_m + kWarps * 8;                     // [kWarps][8]
+#pragma unroll
+  for (int t = 0; t < C::kNT; ++t)
+#pragma unroll
+    for (int mt = 0; mt < C::kMT; ++mt) {
+      const int d0 = 2 * ((D / 16) * gid + mt);  // rows gid and gid + 8: the two coordinates of one byte
+      float* base = ep_o + (w * C::kCols + 8 * t + 2 * tig) * D;
+      base[d0] = o[t][mt][0];
+      base[D + d0] = o[t][mt][1];
+      base[d0 + 1] = o[t][mt][2];
+      base[D + d0 + 1] = o[t][mt][3];
+    }
+  if (gid == 0) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      ep_m[w * 8 + 2 * tig + j] = m_run[j];
+      ep_l[w * 8 + 2 * tig + j] = l_run[j];
+    }
+  }
+  __syncthreads();
+  for (int idx = tid; idx < V * D; idx += kThreads) {
+    const int v = idx / D, d = idx % D;  // column v: the hi part of virtual head v, column v + NV its lo part
+    float M = -INFINITY;
+#pragma unroll
+    for (int ww = 0; ww < kWarps; ++ww) M = fmaxf(M, ep_m[ww * 8 + v]);
+    float acc = 0.0f, l = 0.0f;
+#pragma unroll
+    for (int ww = 0; ww < kWarps; ++ww) {
+      const float mw = ep_m[ww * 8 + v];
+      const float wt = mw == -INFINITY ? 0.0f : exp2f(mw - M);
+      const float* ow = ep_o + ww * C::kCols * D;
+      acc += wt * (ow[v * D + d] + ow[(v + NV) * D + d]);
+      l += wt * ep_l[ww * 8 + v];
+    }
+    const size_t pi = (((size_t)b * a.T + v / G) * a.Hq + g * G + v % G) * a.P + p;
+    a.part_o[pi * D + d] = acc;
+    if (d == 0) {
+      a.part_m[pi] = M;
+      a.part_l[pi] = l;
+    }
+  }
+}
+
+// ---------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// 2-D byte view of a paged cache side: rows = (block, kv head, slot) of `row` bytes; boxes of
+// 16 rows x `box` bytes with the given swizzle.
+bool encode_map(CUtensorMap* map, const void* base, int row, int box, CUtensorMapSwizzle swz, long long rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)row, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)row};
+  const cuuint32_t boxd[2] = {(cuuint32_t)box, (cuuint32_t)kPage};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, boxd, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int KS, int D, int NV>
+cudaError_t launch_fixed(const Args& a, cudaStream_t s) {
+  using C = Cb<KS, D, NV>;
+  CUtensorMap km{}, vm{};
+  const long long rows = (long long)a.num_blocks * a.Hkv * kPage;
+  if (C::kKTma && !encode_map(&km, a.k_cache, C::kKRow, 128, CU_TENSOR_MAP_SWIZZLE_128B, rows))
+    return cudaErrorInvalidValue;
+  if (!encode_map(&vm, a.v_cache, C::kVRow, C::kVRow,
+                  D == 128 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B, rows))
+    return cudaErrorInvalidValue;
+  auto kern = partition_cb_kernel<KS, D, NV>;
+  static DeviceFlags attr;
+  cudaError_t e = ensure_dynamic_smem(kern, C::kSmem, attr);
+  if (e != cudaSuccess) return e;
+  kern<<<dim3(a.P, a.Hkv, a.B), kThreads, C::kSmem, s>>>(a, km, vm);
+  return cudaGetLastError();
+}
+
+template <int KS, int D>
+cudaError_t launch_nv(const Args& a, cudaStream_t s) {
+  const int v = a.T * (a.Hq / a.Hkv);  // virtual heads, padded to a power of two
+  if (v <= 1) return launch_fixed<KS, D, 1>(a, s);
+  if (v <= 2) return launch_fixed<KS, D, 2>(a, s);
+  if (v <= 4) return launch_fixed<KS, D, 4>(a, s);
+  if (v <= 8) return launch_fixed<KS, D, 8>(a, s);
+  return cudaErrorInvalidValue;
+}
+
+template <int KS>
+cudaError_t launch_d(const Args& a, cudaStream_t s) {
+  return a.D == 128 ? launch_nv<KS, 128>(a, s) : launch_nv<KS, 256>(a, s);
+}
+
+}  // namespace
+
+cudaError_t launch_partition_cb(const Args& a, cudaStream_t s) {
+  switch (a.fmt) {
+    case DA_KV_CB4: return launch_d<kSideCB4>(a, s);
+    case DA_KV_FP8K_CB4V: return launch_d<kSideFP8>(a, s);
+    case DA_KV_CB3K_CB4V: return launch_d<kSideCB3>(a, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_partition(const Args& a, cudaStream_t s) {
+  return a.fmt == DA_KV_BF16 || a.fmt == DA_KV_FP8_E4M3 ? launch_partition_tc(a, s) : launch_partition_cb(a, s);
+}
+
+}  // namespace da

@@ -1,0 +1,58 @@
+// page_softmax.cuh -- the online-softmax step of the tensor-core partition kernels, per
+// 16-token page, on the C-fragment layout of S^T[16 tokens x 8 columns] (mma.m16n8k16):
+// thread (gid, tig) holds sc[0], sc[1] = token gid, columns 2 tig and 2 tig + 1, and sc[2],
+// sc[3] = token gid + 8, same columns. Scores are in the log2 domain (x log2 e).
+//
+// The running state per column is (m, l): the reference max and the sum of 2^(s - m); the
+// caller's unnormalised output O^T is scaled by alpha whenever m moves. The reference moves
+// lazily: only when a page's max exceeds it by more than kLazyLog2, so most pages rescale
+// nothing and the probabilities stay below 2^kLazyLog2 (well inside f16 / bf16 range). The
+// final (m, l, o) is exact up to rounding whatever reference was used.
+#pragma once
+
+#include <cmath>
+
+namespace da {
+
+constexpr float kLazyLog2 = 8.0f;
+
+// Tokens outside [lo_c[j], hi_c[j]) of column j get -inf (no weight). tok0: first token of
+// the page.
+__device__ __forceinline__ void mask_page(float (&sc)[4], int tok0, int gid, const int (&lo_c)[2],
+                                          const int (&hi_c)[2]) {
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const int t = tok0 + gid + (e >> 1) * 8, j = e & 1;
+    if (t < lo_c[j] || t >= hi_c[j]) sc[e] = -INFINITY;
+  }
+}
+
+// One page: updates (m, l) of the thread's two columns and returns the page's
+// probabilities pr (relative to the new reference) and the factor alpha[j] the column's
+// running output must be multiplied by. Returns true if any column of the warp moved its
+// reference (alpha != 1 somewhere).
+__device__ __forceinline__ bool page_softmax(const float (&sc)[4], float (&m)[2], float (&l)[2], float (&alpha)[2],
+                                             float (&pr)[4]) {
+  bool moved = false;
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    float mx = fmaxf(sc[j], sc[j + 2]);
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+    // m = -inf (nothing seen yet) moves to the first finite max; 2^(-inf) = 0 then clears
+    // the (zero) state
+    const bool move = mx > m[j] + kLazyLog2;
+    const float mn = move ? mx : m[j];
+    alpha[j] = move ? exp2f(m[j] - mn) : 1.0f;
+    moved |= move;
+    const bool none = mn == -INFINITY;
+    pr[j] = none ? 0.0f : exp2f(sc[j] - mn);
+    pr[j + 2] = none ? 0.0f : exp2f(sc[j + 2] - mn);
+    l[j] = l[j] * alpha[j] + pr[j] + pr[j + 2];
+    m[j] = mn;
+  }
+  return __any_sync(0xffffffffu, moved);
+}
+
+}  // namespace da

@@ -43,13 +43,12 @@
 
 #include "da_internal.cuh"
 #include "kv_formats.cuh"
+#include "page_softmax.cuh"
 #include "ptx.cuh"
 
 namespace da {
 namespace {
 
-constexpr int kWarps = 4;
-constexpr int kThreads = 32 * kWarps;
 constexpr int kPage = 16;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr unsigned kFull = 0xffffffffu;
@@ -60,6 +59,10 @@ constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
 // (query token, head) pairs ("virtual heads" v = jq * G + h) padded to a power of two <= 8.
 template <int KS, int D, int NV>
 struct Cb {
+  // eight warps share one CTA's lookup tables where their registers allow two such CTAs
+  // per SM (D = 128, up to four columns of virtual heads), else four
+  static constexpr int kWarps = (D == 128 && NV <= 4) ? 8 : 4;
+  static constexpr int kThreads = 32 * kWarps;
   static constexpr int kKRow = row_bytes(KS, D);  // bytes of one key row
   static constexpr int kVRow = D / 2;             // bytes of one value row
   static constexpr int kKBytes = kPage * kKRow;
@@ -78,13 +81,16 @@ struct Cb {
   static constexpr int kAlign = kKAlign > kVAlign ? kKAlign : kVAlign;
   static constexpr int kStageBytes = align_up(kOffVN + 64, kAlign);
   static constexpr int kTxBytes = kKBytes + kVBytes + (kKNorms ? 64 : 0) + 64;
-  static constexpr int kStages = 16384 / kStageBytes;  // 16 KB of stages per warp
+  static constexpr int kLutV = 256 * 32 * 4;  // 4-bit pair table, 32 copies
+  static constexpr int kLutK = KS == kSideCB3 ? 64 * 32 * 4 : 0;
+  // stages: what two CTAs per SM leave after the tables (228 KB per SM, 1 KB reserved and
+  // ~1 KB of alignment slack and barriers per CTA), at most 6 per warp
+  static constexpr int kStageBudget = (233472 / 2 - 3072 - kLutV - kLutK) / kWarps;
+  static constexpr int kStages = kStageBudget / kStageBytes < 6 ? kStageBudget / kStageBytes : 6;
   static constexpr int kNT = NV <= 4 ? 1 : 2;           // P.V column tiles
   static constexpr int kCols = 8 * kNT;
   static constexpr int kMT = D / 16;                    // O^T row tiles
   static constexpr int kKS = D / 16;                    // k-steps of S^T
-  static constexpr int kLutV = 256 * 32 * 4;            // 4-bit pair table, 32 copies
-  static constexpr int kLutK = KS == kSideCB3 ? 64 * 32 * 4 : 0;
   static constexpr int kOffStages = kLutV + kLutK;
   static constexpr int kStageSmem = kWarps * kStages * kStageBytes;
   static constexpr int kEpiSmem = (kWarps * kCols * D + 2 * kWarps * 8) * 4;
@@ -184,11 +190,13 @@ struct ValueTiles {
   }
 };
 
-template <int KS, int D, int NV>
-__global__ void __launch_bounds__(kThreads, 2)
+// CAP: softcap on (a separate instantiation, so the plain kernel carries no tanh)
+template <int KS, int D, int NV, bool CAP>
+__global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 2)
     partition_cb_kernel(const Args a, const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap) {
   using C = Cb<KS, D, NV>;
+  constexpr int kWarps = C::kWarps, kThreads = C::kThreads;
   const int p = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int gid = lane >> 2, tig = lane & 3;
@@ -339,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     score_scale = a.scale * ldexpf(1.0f, -e2) * kLog2e;
   }
   const float cap = a.softcap;
-  const float cap_pre = cap > 0.0f ? 1.0f / (cap * kLog2e) : 0.0f;  // log2-domain score -> s_nat / cap
+  const float cap_pre = CAP ? 1.0f / (cap * kLog2e) : 0.0f;  // log2-domain score -> s_nat / cap
   const float cap_post = cap * kLog2e;
 
   // ---- running state: column c = 2*tig + j of S^T and of every O^T column tile
@@ -362,6 +370,16 @@ __global__ void __launch_bounds__(kThreads, 2)
     lo_c[j] = lo > r.start ? lo : r.start;
     hi_c[j] = pos + 1 < r.end ? pos + 1 : r.end;
   }
+  // pages inside [lo_all, hi_all) need no mask in any column (warp-uniform)
+  int lo_all = max(lo_c[0], lo_c[1]), hi_all = min(hi_c[0], hi_c[1]);
+  lo_all = max(lo_all, __shfl_xor_sync(kFull, lo_all, 1));
+  lo_all = max(lo_all, __shfl_xor_sync(kFull, lo_all, 2));
+  hi_all = min(hi_all, __shfl_xor_sync(kFull, hi_all, 1));
+  hi_all = min(hi_all, __shfl_xor_sync(kFull, hi_all, 2));
+  // O^T is kept in units of 2^(ev_run - 127): ev_run is the largest biased binary32 exponent
+  // of the value norms seen so far, so P * ||v|| * 2^(127 - ev_run) < 2^(kLazyLog2 + 1) fits f16
+  int ev_run = 0;
+  float v_unit = 1.0f;  // 2^(127 - ev_run)
 
   __syncthreads();  // lookup tables written
 
@@ -428,30 +446,31 @@ __global__ void __launch_bounds__(kThreads, 2)
         kn0 = ldsf(kb + C::kOffKN + 4 * gid);
         kn1 = ldsf(kb + C::kOffKN + 4 * (gid + 8));
       }
+      const float ss0 = score_scale * kn0, ss1 = score_scale * kn1;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int t = tok0 + gid + (e >> 1) * 8, j = e & 1;
-        const float y = sc[e] * score_scale * ((e >> 1) ? kn1 : kn0);
-        const float x = cap > 0.0f ? cap_post * tanhf(y * cap_pre) : y;
-        sc[e] = (t >= lo_c[j] && t < hi_c[j]) ? x : -INFINITY;
+        const float y = sc[e] * ((e >> 1) ? ss1 : ss0);
+        sc[e] = CAP ? cap_post * tanhf(y * cap_pre) : y;
       }
-      // -- online softmax per column
+      if (tok0 < lo_all || tok0 + kPage > hi_all) mask_page(sc, tok0, gid, lo_c, hi_c);
+      // -- online softmax per column (lazily moved reference max); a larger value-norm
+      //    exponent on this page rescales O^T by the same exact power of two
       float alpha[2], pr[4];
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        float mx = fmaxf(sc[j], sc[j + 2]);
-        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 4));
-        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 8));
-        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
-        const float mn = fmaxf(m_run[j], mx);
-        const bool none = mn == -INFINITY;
-        alpha[j] = none ? 1.0f : exp2f(m_run[j] - mn);
-        pr[j] = none ? 0.0f : exp2f(sc[j] - mn);
-        pr[j + 2] = none ? 0.0f : exp2f(sc[j + 2] - mn);
-        l_run[j] = l_run[j] * alpha[j] + pr[j] + pr[j + 2];
-        m_run[j] = mn;
+      bool rescale = page_softmax(sc, m_run, l_run, alpha, pr);
+      const float vn0 = ldsf(kb + C::kOffVN + 4 * gid), vn1 = ldsf(kb + C::kOffVN + 4 * (gid + 8));
+      int ev = (int)(__float_as_uint(fmaxf(fabsf(vn0), fabsf(vn1))) >> 23);
+      ev = max(ev, __shfl_xor_sync(kFull, ev, 4));
+      ev = max(ev, __shfl_xor_sync(kFull, ev, 8));
+      ev = max(ev, __shfl_xor_sync(kFull, ev, 16));
+      if (ev > ev_run) {  // warp-uniform
+        const float f = ldexpf(1.0f, ev_run - ev);
+        alpha[0] *= f;
+        alpha[1] *= f;
+        ev_run = ev;
+        v_unit = ldexpf(1.0f, 127 - ev);
+        rescale = true;
       }
-      if (__any_sync(kFull, alpha[0] != 1.0f || alpha[1] != 1.0f)) {
+      if (rescale) {
 #pragma unroll
         for (int t = 0; t < C::kNT; ++t)
 #pragma unroll
@@ -463,10 +482,10 @@ __global__ void __launch_bounds__(kThreads, 2)
           }
       }
       // -- (P * value norms)^T as the B operand: hi/lo parts in C layout, transposed with movmatrix
-      const float vn0 = ldsf(kb + C::kOffVN + 4 * gid), vn1 = ldsf(kb + C::kOffVN + 4 * (gid + 8));
+      const float vu0 = vn0 * v_unit, vu1 = vn1 * v_unit;
       float pv[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) pv[e] = pr[e] * ((e >> 1) ? vn1 : vn0);
+      for (int e = 0; e < 4; ++e) pv[e] = pr[e] * ((e >> 1) ? vu1 : vu0);
       uint32_t pb[C::kNT][2];
       if constexpr (NV <= 4) {
         float x[4];
@@ -516,7 +535,15 @@ __global__ void __launch_bounds__(kThreads, 2)
       ptx::mbar_wait(bar0 + 8 * (k % C::kStages), (k / C::kStages) & 1);
   }
 
-  // ---- merge the four warps through shared memory (tables and stages are free now)
+  // ---- merge the warps through shared memory (tables and stages are free now); O^T back
+  //      to absolute units
+  const float o_unit = ldexpf(1.0f, ev_run - 127);
+#pragma unroll
+  for (int t = 0; t < C::kNT; ++t)
+#pragma unroll
+    for (int mt = 0; mt < C::kMT; ++mt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) o[t][mt][e] *= o_unit;
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
     l_run[j] += __shfl_xor_sync(kFull, l_run[j], 4);
@@ -598,7 +625,7 @@ bool encode_map(CUtensorMap* map, const void* base, int row, int box, CUtensorMa
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int KS, int D, int NV>
+template <int KS, int D, int NV, bool CAP>
 cudaError_t launch_fixed(const Args& a, cudaStream_t s) {
   using C = Cb<KS, D, NV>;
   CUtensorMap km{}, vm{};
@@ -608,27 +635,32 @@ cudaError_t launch_fixed(const Args& a, cudaStream_t s) {
   if (!encode_map(&vm, a.v_cache, C::kVRow, C::kVRow,
                   D == 128 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B, rows))
     return cudaErrorInvalidValue;
-  auto kern = partition_cb_kernel<KS, D, NV>;
+  auto kern = partition_cb_kernel<KS, D, NV, CAP>;
   static DeviceFlags attr;
   cudaError_t e = ensure_dynamic_smem(kern, C::kSmem, attr);
   if (e != cudaSuccess) return e;
-  kern<<<dim3(a.P, a.Hkv, a.B), kThreads, C::kSmem, s>>>(a, km, vm);
+  kern<<<dim3(a.P, a.Hkv, a.B), C::kThreads, C::kSmem, s>>>(a, km, vm);
   return cudaGetLastError();
 }
 
-template <int KS, int D>
+template <int KS, int D, bool CAP>
 cudaError_t launch_nv(const Args& a, cudaStream_t s) {
   const int v = a.T * (a.Hq / a.Hkv);  // virtual heads, padded to a power of two
-  if (v <= 1) return launch_fixed<KS, D, 1>(a, s);
-  if (v <= 2) return launch_fixed<KS, D, 2>(a, s);
-  if (v <= 4) return launch_fixed<KS, D, 4>(a, s);
-  if (v <= 8) return launch_fixed<KS, D, 8>(a, s);
+  if (v <= 1) return launch_fixed<KS, D, 1, CAP>(a, s);
+  if (v <= 2) return launch_fixed<KS, D, 2, CAP>(a, s);
+  if (v <= 4) return launch_fixed<KS, D, 4, CAP>(a, s);
+  if (v <= 8) return launch_fixed<KS, D, 8, CAP>(a, s);
   return cudaErrorInvalidValue;
+}
+
+template <int KS, int D>
+cudaError_t launch_cap(const Args& a, cudaStream_t s) {
+  return a.softcap > 0.0f ? launch_nv<KS, D, true>(a, s) : launch_nv<KS, D, false>(a, s);
 }
 
 template <int KS>
 cudaError_t launch_d(const Args& a, cudaStream_t s) {
-  return a.D == 128 ? launch_nv<KS, 128>(a, s) : launch_nv<KS, 256>(a, s);
+  return a.D == 128 ? launch_cap<KS, 128>(a, s) : launch_cap<KS, 256>(a, s);
 }
 
 }  // namespace

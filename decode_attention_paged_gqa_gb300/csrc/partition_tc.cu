@@ -34,6 +34,7 @@
 #include <mutex>
 
 #include "da_internal.cuh"
+#include "page_softmax.cuh"
 #include "ptx.cuh"
 
 namespace da {
@@ -99,7 +100,8 @@ __device__ __forceinline__ void mma(float (&d)[4], const uint32_t (&a)[4], uint3
     ptx::mma_f16(d, a, b0, b1);
 }
 
-template <int FMT, int D, int NV>
+// CAP: softcap on (a separate instantiation, so the plain kernel carries no tanh)
+template <int FMT, int D, int NV, bool CAP>
 __global__ void __launch_bounds__(kThreads, 2)
     partition_tc_kernel(const Args a, const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap) {
@@ -197,7 +199,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     score_scale = a.scale * __ldg(a.k_scales) * ldexpf(1.0f, -e2) * kLog2e;
   }
   const float cap = a.softcap;
-  const float cap_pre = cap > 0.0f ? score_scale / (cap * kLog2e) : 0.0f;  // s_nat / cap
+  const float cap_pre = CAP ? score_scale / (cap * kLog2e) : 0.0f;  // s_nat / cap
   const float cap_post = cap * kLog2e;
 
   // ---- running state: column c = 2*tig + j of S^T and of every O^T column tile
@@ -220,6 +222,12 @@ __global__ void __launch_bounds__(kThreads, 2)
     lo_c[j] = lo > r.start ? lo : r.start;
     hi_c[j] = pos + 1 < r.end ? pos + 1 : r.end;
   }
+  // pages inside [lo_all, hi_all) need no mask in any column (warp-uniform)
+  int lo_all = max(lo_c[0], lo_c[1]), hi_all = min(hi_c[0], hi_c[1]);
+  lo_all = max(lo_all, __shfl_xor_sync(kFull, lo_all, 1));
+  lo_all = max(lo_all, __shfl_xor_sync(kFull, lo_all, 2));
+  hi_all = min(hi_all, __shfl_xor_sync(kFull, hi_all, 1));
+  hi_all = min(hi_all, __shfl_xor_sync(kFull, hi_all, 2));
 
   const int mi = lane >> 3, ri = lane & 7;  // ldmatrix: matrix index and row of this lane's address
   int stalled_at = -1;  // local page whose copy never arrived (never expected)
@@ -256,30 +264,13 @@ __global__ void __launch_bounds__(kThreads, 2)
           mma<FMT>(sc, a1, qf[2 * j2 + 1][0], qf[2 * j2 + 1][1]);
         }
       }
-      // -- scale, softcap, mask; sc[0], sc[1]: token gid; sc[2], sc[3]: token gid + 8
+      // -- scale (log2 domain), softcap, mask; sc[0], sc[1]: token gid; sc[2], sc[3]: token gid + 8
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int t = tok0 + gid + (e >> 1) * 8, j = e & 1;
-        const float x = cap > 0.0f ? cap_post * tanhf(sc[e] * cap_pre) : sc[e] * score_scale;
-        sc[e] = (t >= lo_c[j] && t < hi_c[j]) ? x : -INFINITY;
-      }
-      // -- online softmax per column
+      for (int e = 0; e < 4; ++e) sc[e] = CAP ? cap_post * tanhf(sc[e] * cap_pre) : sc[e] * score_scale;
+      if (tok0 < lo_all || tok0 + kPage > hi_all) mask_page(sc, tok0, gid, lo_c, hi_c);
+      // -- online softmax per column (lazily moved reference max)
       float alpha[2], pr[4];
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        float mx = fmaxf(sc[j], sc[j + 2]);
-        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 4));
-        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 8));
-        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
-        const float mn = fmaxf(m_run[j], mx);
-        const bool none = mn == -INFINITY;
-        alpha[j] = none ? 1.0f : exp2f(m_run[j] - mn);
-        pr[j] = none ? 0.0f : exp2f(sc[j] - mn);
-        pr[j + 2] = none ? 0.0f : exp2f(sc[j + 2] - mn);
-        l_run[j] = l_run[j] * alpha[j] + pr[j] + pr[j + 2];
-        m_run[j] = mn;
-      }
-      if (__any_sync(kFull, alpha[0] != 1.0f || alpha[1] != 1.0f)) {
+      if (page_softmax(sc, m_run, l_run, alpha, pr)) {
 #pragma unroll
         for (int t = 0; t < T::kNT; ++t)
 #pragma unroll
@@ -445,7 +436,7 @@ bool encode_cache_map(CUtensorMap* map, const void* base, int elem_bytes, int D,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int FMT, int D, int NV>
+template <int FMT, int D, int NV, bool CAP>
 cudaError_t launch_fixed(const Args& a, cudaStream_t s) {
   using T = Tc<FMT, D, NV>;
   CUtensorMap km, vm;
@@ -453,7 +444,7 @@ cudaError_t launch_fixed(const Args& a, cudaStream_t s) {
   if (!encode_cache_map(&km, a.k_cache, T::kElemBytes, D, rows) ||
       !encode_cache_map(&vm, a.v_cache, T::kElemBytes, D, rows))
     return cudaErrorInvalidValue;
-  auto kern = partition_tc_kernel<FMT, D, NV>;
+  auto kern = partition_tc_kernel<FMT, D, NV, CAP>;
   static DeviceFlags attr;
   cudaError_t e = ensure_dynamic_smem(kern, T::kSmem, attr);
   if (e != cudaSuccess) return e;
@@ -461,14 +452,19 @@ cudaError_t launch_fixed(const Args& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+template <int FMT, int D, bool CAP>
+cudaError_t launch_nv(const Args& a, cudaStream_t s) {
+  const int v = a.T * (a.Hq / a.Hkv);  // virtual heads, padded to a power of two
+  if (v <= 1) return launch_fixed<FMT, D, 1, CAP>(a, s);
+  if (v <= 2) return launch_fixed<FMT, D, 2, CAP>(a, s);
+  if (v <= 4) return launch_fixed<FMT, D, 4, CAP>(a, s);
+  if (v <= 8) return launch_fixed<FMT, D, 8, CAP>(a, s);
+  return cudaErrorInvalidValue;
+}
+
 template <int FMT, int D>
 cudaError_t launch_g(const Args& a, cudaStream_t s) {
-  const int v = a.T * (a.Hq / a.Hkv);  // virtual heads, padded to a power of two
-  if (v <= 1) return launch_fixed<FMT, D, 1>(a, s);
-  if (v <= 2) return launch_fixed<FMT, D, 2>(a, s);
-  if (v <= 4) return launch_fixed<FMT, D, 4>(a, s);
-  if (v <= 8) return launch_fixed<FMT, D, 8>(a, s);
-  return cudaErrorInvalidValue;
+  return a.softcap > 0.0f ? launch_nv<FMT, D, true>(a, s) : launch_nv<FMT, D, false>(a, s);
 }
 
 }  // namespace

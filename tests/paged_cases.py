@@ -20,8 +20,9 @@ def u16(t: torch.Tensor) -> np.ndarray:
     return t.contiguous().view(torch.int16).numpy().view(np.uint16)
 
 
-def make_case(spec: wl.WorkloadSpec, layout: wl.PagedLayout | None = None) -> dict:
-    """All inputs of one call, on the CPU, in the library's layouts."""
+def make_case(spec: wl.WorkloadSpec, layout: wl.PagedLayout | None = None, sources: dict | None = None) -> dict:
+    """All inputs of one call, on the CPU, in the library's layouts. `sources` may replace the
+    generated fp32 K or V source ({"k": [num_blocks, Hkv, 16, D] tensor}) before encoding."""
     lay = layout or wl.make_layout(spec)
     nb = lay.num_blocks
     c = dict(spec=spec, lens=lay.context_lens, bt=lay.block_tables, num_blocks=nb, q=wl.make_query(spec),
@@ -33,11 +34,12 @@ def make_case(spec: wl.WorkloadSpec, layout: wl.PagedLayout | None = None) -> di
         cb8 = oracle.lloyd_max(8, 1.0 / math.sqrt(D))[1]
         c["codebook"] = torch.from_numpy(np.concatenate([cb8, cb16]) if k_side == "cb3" else cb16)
         c["sign"] = wl.sign_pattern(spec)
+    sources = sources or {}
     for w, side in (("k", k_side), ("v", v_side)):
         if side == "bf16":
-            c[w] = wl.kv_bf16(spec, w, nb)
+            c[w] = sources[w].to(torch.bfloat16) if w in sources else wl.kv_bf16(spec, w, nb)
             continue
-        src = wl.kv_source(spec, w, nb).numpy()
+        src = sources[w].float().numpy() if w in sources else wl.kv_source(spec, w, nb).numpy()
         if side == "fp8":
             codes, s = oracle.fp8_quantize(src)
             c[w] = torch.from_numpy(codes)

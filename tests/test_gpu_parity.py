@@ -93,6 +93,43 @@ def test_query_magnitudes(fmt, qscale):
         c, softmax_scale=1.0 / (qscale * math.sqrt(128))), f"{fmt} q x{qscale}")
 
 
+@pytest.mark.parametrize("fmt", ["fp8", "cb4", "fp8k_cb4v", "cb3k_cb4v"])
+@pytest.mark.parametrize("vscale", [1e-30, 3e4])
+def test_value_magnitudes(fmt, vscale):
+    """Value scales far from 1: the 4-bit value side multiplies P by the token's norm before a
+    16-bit MMA, which must neither overflow (norms ~3e5 here, above the f16 range) nor lose
+    tiny norms."""
+    spec, lay = small_spec(fmt, 128, 4, lens=[1, 600, 1500], seed=13)
+    c = make_case(spec, lay)
+    c["v_scales"] = c["v_scales"] * vscale
+    ref = run_oracle(c)
+    scale = float(np.abs(ref).max())
+    assert_close(run_gpu(c) / scale, ref / scale, f"{fmt} v x{vscale}")
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "fp8", "cb4", "cb3k_cb4v"])
+def test_rising_scores(fmt):
+    """Scores that rise slowly along the context (about one log2 unit per page) keep the
+    lazily moved softmax reference stale for many pages before it moves."""
+    lens = [16 * 40 + 5, 2500]
+    spec, lay = small_spec(fmt, 128, 4, lens=lens, seed=17)
+    q_dir = torch.zeros(128)
+    q_dir[0] = 1.0
+    nb = lay.num_blocks
+    k = torch.randn(nb, 2, 16, 128) * 0.05
+    # key of (block, slot) at token position t gets a component along q's first axis that
+    # grows with t: block_tables map positions to blocks, so walk them
+    for b, L in enumerate(lens):
+        for t in range(L):
+            phys = int(lay.block_tables[b, t // 16])
+            k[phys, :, t % 16, 0] = t / 16.0
+    c = make_case(spec, lay, sources={"k": k})
+    q = torch.zeros_like(c["q"].float())
+    q[..., 0] = 8.0
+    c["q"] = q.to(torch.bfloat16)
+    assert_close(run_gpu(c), run_oracle(c), f"{fmt} rising scores")
+
+
 @pytest.mark.parametrize("fmt", ["bf16", "fp8", "cb4", "fp8k_cb4v"])
 @pytest.mark.parametrize("T,G,window", [(2, 4, 0), (4, 2, 0), (3, 2, 700), (8, 1, 0), (2, 1, 1000), (5, 1, 64)])
 def test_multi_token_causal(fmt, T, G, window):

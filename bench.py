@@ -207,29 +207,39 @@ def build_inputs(spec, encode_on_gpu=True):
     return lay, host, src
 
 
-# the sources the tensor-core partition kernel is compiled from
-PARTITION_SOURCES = ("partition_tc.cu", "ptx.cuh", "da_internal.cuh")
+# the sources each partition kernel is compiled from (a recorded DRAM traffic figure is only
+# reported while the kernel's sources still hash to the profiled build)
+PARTITION_SOURCES = {
+    "partition_tc_kernel": ("partition_tc.cu", "page_softmax.cuh", "page_walk.cuh", "ptx.cuh", "da_internal.cuh"),
+    "partition_cb_kernel": ("partition_cb.cu", "page_softmax.cuh", "page_walk.cuh", "ptx.cuh", "da_internal.cuh",
+                            "kv_formats.cuh"),
+}
 
 
-def source_hash(files=PARTITION_SOURCES):
+def partition_kernel(kv_format: str) -> str:
+    return "partition_tc_kernel" if kv_format in ("bf16", "fp8") else "partition_cb_kernel"
+
+
+def source_hash(kernel: str) -> str:
     h = hashlib.sha1()
-    for name in files:
+    for name in PARTITION_SOURCES[kernel]:
         with open(os.path.join(ROOT, "decode_attention_paged_gqa_gb300", "csrc", name), "rb") as fh:
             h.update(name.encode() + fh.read())
     return h.hexdigest()[:16]
 
 
 def recorded_traffic(kernel: str, workload: str):
-    """DRAM bytes per launch from the committed ncu summary, if taken on this kernel source."""
+    """DRAM bytes per launch from the committed ncu summaries, if taken on this kernel source."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
-            t = json.load(f)[kernel]
+            entries = json.load(f)["entries"]
     except (OSError, KeyError, ValueError):
         return None
-    if t.get("source_hash") != source_hash() or t.get("workload") != workload:
-        return None
-    return t.get("dram_bytes_per_launch")
+    for t in entries:
+        if t.get("kernel") == kernel and t.get("workload") == workload and t.get("source_hash") == source_hash(kernel):
+            return t.get("dram_bytes_per_launch")
+    return None
 
 
 # ----------------------------------------------------------------------------- CPU oracle
@@ -452,7 +462,8 @@ def main():
     peak, peak_src = hbm_peak()
     gbs = world * kv_bytes / (step_ms * 1e-3) / 1e9
     part_gbs = kv_bytes / (part_ms * 1e-3) / 1e9
-    traffic = recorded_traffic("partition", spec.name)
+    kernel = partition_kernel(spec.kv_format)
+    traffic = recorded_traffic(kernel, spec.name)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
@@ -474,7 +485,7 @@ def main():
                    "algorithmic_kv_bytes": kv_bytes, "cache_bytes": cache_bytes,
                    "l2": "inputs larger than L2 (KV cache %.2f GB vs 129 MB L2), no flush" % (cache_bytes / 1e9)
                    if cache_bytes > L2_BYTES else "inputs smaller than L2", "parallelism": f"replicas x{world}"},
-        "roofline": {"bound": "hbm", "kernel": "partition", "achieved": part_gbs, "peak": peak, "unit": "GB/s",
+        "roofline": {"bound": "hbm", "kernel": kernel, "achieved": part_gbs, "peak": peak, "unit": "GB/s",
                      "frac": part_gbs / peak, "peak_source": peak_src, "traffic": traffic,
                      "partition_us": part_ms * 1000, "bytes_per_launch": kv_bytes},
         "cpu_baseline": cpu,

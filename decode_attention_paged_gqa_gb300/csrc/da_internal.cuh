@@ -34,6 +34,7 @@ struct Args {
   float scale, softcap;
   int window, psize, thresh;
   int P;                      // partitions the grid and the workspace are sized for
+  int ppc;                    // partitions a partition-kernel CTA walks (set by its launcher)
   // workspace pieces
   uint32_t* err;              // device error word (DA_DEVERR_* bits)
   float* q_rot;               // [B][T][Hq][D] (formats whose keys are on the rotated basis)
@@ -169,6 +170,22 @@ enum Phase { kRotate = 1, kPartition = 2, kReduce = 4, kAll = 7 };
 int run_phases(int phases, const void* q, const void* k, const void* v, const float* ks, const float* vs,
                const float* cb, const float* sign, const int32_t* bt, const int32_t* lens, float* out,
                const da_params* p, void* stream);
+
+// Partitions per CTA for a partition kernel with `per_sm` resident CTAs per SM: the CTAs
+// walk consecutive partitions of one (sequence, kv head) so their pipelines stay full across
+// partition boundaries, while the grid keeps about eight waves of CTAs. Cached per device.
+inline int partitions_per_cta(const Args& a, int per_sm, int* cached_sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+  if (cached_sms[dev] == 0) {
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) return 1;
+    cached_sms[dev] = sms;
+  }
+  const long long units = (long long)a.P * a.Hkv * a.B;
+  const long long waves = units / (8ll * cached_sms[dev] * (per_sm > 0 ? per_sm : 1));
+  return waves < 1 ? 1 : (waves > 8 ? 8 : (int)waves);
+}
 
 // Launchers (one translation unit each). They return cudaGetLastError() of their launch.
 cudaError_t launch_rotate_q(const Args& a, cudaStream_t s);

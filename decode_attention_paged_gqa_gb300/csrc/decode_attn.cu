@@ -94,6 +94,7 @@ Args make_args(const void* q, const void* k, const void* v, const float* ks, con
   a.psize = p->partition_size;
   a.thresh = p->split_threshold;
   a.P = host_max_partitions(*p);
+  a.ppc = 1;
   const Layout l = workspace_layout(*p);
   char* ws = static_cast<char*>(p->workspace);
   a.err = reinterpret_cast<uint32_t*>(ws + l.err);

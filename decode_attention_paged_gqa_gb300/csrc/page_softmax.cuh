@@ -16,6 +16,14 @@ namespace da {
 
 constexpr float kLazyLog2 = 8.0f;
 
+// 2^x with the hardware approximation (ex2.approx: relative error ~2^-22; results below
+// 2^-126 flush to zero, 2^-inf = 0), one instruction.
+__device__ __forceinline__ float exp2_fast(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Tokens outside [lo_c[j], hi_c[j]) of column j get -inf (no weight). tok0: first token of
 // the page.
 __device__ __forceinline__ void mask_page(float (&sc)[4], int tok0, int gid, const int (&lo_c)[2],
@@ -44,11 +52,12 @@ __device__ __forceinline__ bool page_softmax(const float (&sc)[4], float (&m)[2]
     // the (zero) state
     const bool move = mx > m[j] + kLazyLog2;
     const float mn = move ? mx : m[j];
-    alpha[j] = move ? exp2f(m[j] - mn) : 1.0f;
+    alpha[j] = move ? exp2_fast(m[j] - mn) : 1.0f;
     moved |= move;
-    const bool none = mn == -INFINITY;
-    pr[j] = none ? 0.0f : exp2f(sc[j] - mn);
-    pr[j + 2] = none ? 0.0f : exp2f(sc[j + 2] - mn);
+    // with no finite score yet every score is -inf: any finite reference gives 2^-inf = 0
+    const float ref = mn == -INFINITY ? 0.0f : mn;
+    pr[j] = exp2_fast(sc[j] - ref);
+    pr[j + 2] = exp2_fast(sc[j + 2] - ref);
     l[j] = l[j] * alpha[j] + pr[j] + pr[j + 2];
     m[j] = mn;
   }

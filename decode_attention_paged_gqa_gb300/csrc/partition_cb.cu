@@ -44,6 +44,7 @@
 #include "da_internal.cuh"
 #include "kv_formats.cuh"
 #include "page_softmax.cuh"
+#include "page_walk.cuh"
 #include "ptx.cuh"
 
 namespace da {
@@ -59,9 +60,10 @@ constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
 // (query token, head) pairs ("virtual heads" v = jq * G + h) padded to a power of two <= 8.
 template <int KS, int D, int NV>
 struct Cb {
-  // eight warps share one CTA's lookup tables where their registers allow two such CTAs
-  // per SM (D = 128, up to four columns of virtual heads), else four
-  static constexpr int kWarps = (D == 128 && NV <= 4) ? 8 : 4;
+  // eight warps share one CTA's lookup tables where their registers and two stages of 4 KB
+  // or less per warp allow two such CTAs per SM (D = 128, up to four columns of virtual
+  // heads, codebook keys), else four
+  static constexpr int kWarps = (D == 128 && NV <= 4 && KS != kSideFP8) ? 8 : 4;
   static constexpr int kThreads = 32 * kWarps;
   static constexpr int kKRow = row_bytes(KS, D);  // bytes of one key row
   static constexpr int kVRow = D / 2;             // bytes of one value row
@@ -83,20 +85,22 @@ struct Cb {
   static constexpr int kTxBytes = kKBytes + kVBytes + (kKNorms ? 64 : 0) + 64;
   static constexpr int kLutV = 256 * 32 * 4;  // 4-bit pair table, 32 copies
   static constexpr int kLutK = KS == kSideCB3 ? 64 * 32 * 4 : 0;
-  // stages: what two CTAs per SM leave after the tables (228 KB per SM, 1 KB reserved and
-  // ~1 KB of alignment slack and barriers per CTA), at most 6 per warp
-  static constexpr int kStageBudget = (233472 / 2 - 3072 - kLutV - kLutK) / kWarps;
-  static constexpr int kStages = kStageBudget / kStageBytes < 6 ? kStageBudget / kStageBytes : 6;
+  static constexpr int kDP = D + 4;  // padded row of the merge buffer
+  static constexpr int kMergeSmem = (kWarps * NV * kDP + 2 * kWarps * 8) * 4;
+  // stages: what two CTAs per SM leave after the tables and the merge buffer (228 KB per SM,
+  // 1 KB reserved and ~2 KB of alignment slack and barriers per CTA), 2 to 6 per warp
+  static constexpr int kStageBudget = (233472 / 2 - 3072 - kLutV - kLutK - kMergeSmem) / kWarps;
+  static constexpr int kFit = kStageBudget / kStageBytes;
+  static constexpr int kStages = kFit < 2 ? 2 : (kFit > 6 ? 6 : kFit);
   static constexpr int kNT = NV <= 4 ? 1 : 2;           // P.V column tiles
-  static constexpr int kCols = 8 * kNT;
   static constexpr int kMT = D / 16;                    // O^T row tiles
   static constexpr int kKS = D / 16;                    // k-steps of S^T
   static constexpr int kOffStages = kLutV + kLutK;
   static constexpr int kStageSmem = kWarps * kStages * kStageBytes;
-  static constexpr int kEpiSmem = (kWarps * kCols * D + 2 * kWarps * 8) * 4;
-  static constexpr int kBody = kOffStages + kStageSmem;
-  static constexpr int kSmem = (kBody > kEpiSmem ? kBody : kEpiSmem) + 1024;
-  static_assert(kStages >= 2, "too few stages");
+  static constexpr int kOffMerge = kOffStages + kStageSmem;
+  static constexpr int kSmem = kOffMerge + kMergeSmem + 1024;
+  // two CTAs per SM (228 KB, 1 KB reserved per CTA, barriers) wherever the stage budget allowed
+  static_assert(kFit < 2 || 2 * (kSmem + 1024 + 8 * kWarps * kStages) <= 233472, "two CTAs per SM do not fit");
 };
 
 __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
@@ -175,17 +179,17 @@ struct KeySteps {
 
 template <int M, int N, int D, int NT>
 struct ValueTiles {
-  // O^T[m-tile M] += V^T(m-tile M) . P^T for M = M .. N-1
-  __device__ static __forceinline__ void run(float (&o)[NT][D / 16][4], const uint32_t (*vw)[D / 64], uint32_t lutv,
+  // O^T[m-tile M] += V^T(m-tile M) . P^T for M = M .. N-1. vx[r]: table indices, byte M of
+  // word array r: r = 0 / 1: the low / high nibbles of tokens (2 tig, 2 tig + 1) paired, r =
+  // 2 / 3 the same for tokens (2 tig + 8, 2 tig + 9); one lookup gives an A register.
+  __device__ static __forceinline__ void run(float (&o)[NT][D / 16][4], const uint32_t (*vx)[D / 64], uint32_t lutv,
                                              const uint32_t (&pb)[NT][2]) {
     if constexpr (M < N) {
-      const uint32_t l0 = lut(lutv, byte_of<M>(vw[0])), l1 = lut(lutv, byte_of<M>(vw[1]));
-      const uint32_t l2 = lut(lutv, byte_of<M>(vw[2])), l3 = lut(lutv, byte_of<M>(vw[3]));
-      const uint32_t af[4] = {__byte_perm(l0, l1, 0x5410), __byte_perm(l0, l1, 0x7632), __byte_perm(l2, l3, 0x5410),
-                              __byte_perm(l2, l3, 0x7632)};
+      const uint32_t af[4] = {lut(lutv, byte_of<M>(vx[0])), lut(lutv, byte_of<M>(vx[1])),
+                              lut(lutv, byte_of<M>(vx[2])), lut(lutv, byte_of<M>(vx[3]))};
 #pragma unroll
       for (int t = 0; t < NT; ++t) ptx::mma_f16(o[t][M], af, pb[t][0], pb[t][1]);
-      ValueTiles<M + 1, N, D, NT>::run(o, vw, lutv, pb);
+      ValueTiles<M + 1, N, D, NT>::run(o, vx, lutv, pb);
     }
   }
 };
@@ -196,14 +200,16 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 2)
     partition_cb_kernel(const Args a, const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap) {
   using C = Cb<KS, D, NV>;
-  constexpr int kWarps = C::kWarps, kThreads = C::kThreads;
-  const int p = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  constexpr int kWarps = C::kWarps, kThreads = C::kThreads, DP = C::kDP;
+  const int g = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int gid = lane >> 2, tig = lane & 3;
   const int G = a.Hq / a.Hkv, V = a.T * G;
-  const int L = load_len(a, b, p == 0 && g == 0 && tid == 0);
-  const Range r = partition_range(L, a.T, p, a.window, a.psize, a.thresh);
-  if (r.start >= r.end) return;
+  const int L = load_len(a, b, blockIdx.x == 0 && g == 0 && tid == 0);
+  const int np = seq_partitions(L, a.T, a.window, a.psize, a.thresh);
+  // this CTA's partitions of (b, g)
+  const int p_begin = blockIdx.x * a.ppc, p_end = min(p_begin + a.ppc, np);
+  if (p_begin >= p_end) return;
 
   extern __shared__ unsigned char smem_raw[];
   __shared__ __align__(8) uint64_t bars[kWarps * C::kStages];
@@ -220,20 +226,17 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 2)
   }
   __syncwarp();
 
-  // ---- pages of this partition and this warp's share of them
-  const int first_page = r.start / kPage, npages = (r.end - 1) / kPage - first_page + 1;
-  const int nw = npages > w ? (npages - w + kWarps - 1) / kWarps : 0;
-  int bid = -1;  // lane l: physical block of local page 32*chunk + l
-  auto load_bids = [&](int chunk) {
-    const int i = 32 * chunk + lane;
-    bid = i < nw ? load_block(a, b, first_page + w + kWarps * i) : -1;
-  };
-  load_bids(0);
+  // ---- the warp's pages over the CTA's partitions, copied kStages ahead of the compute
+  IssueCursor<kWarps> cur;
+  cur.init(a, b, L, p_begin, p_end, w, lane);
   uint32_t valid_mask = 0;  // bit s: the page in stage s has a valid block (warp-uniform)
-  auto issue = [&](int k) {  // all lanes; lane 0 issues the copies of local page k
-    if (k > 0 && (k & 31) == 0) load_bids(k >> 5);
-    const int phys = __shfl_sync(kFull, bid, k & 31);
-    const int s = k % C::kStages;
+  unsigned issued = 0;
+  int is = 0;  // stage of the next copy (issued % kStages)
+  auto issue_next = [&]() {  // all lanes; lane 0 issues the copies of the page at the cursor
+    const int phys = cur.take(a);
+    const int s = is;
+    is = is + 1 == C::kStages ? 0 : is + 1;
+    ++issued;
     valid_mask = phys >= 0 ? (valid_mask | (1u << s)) : (valid_mask & ~(1u << s));
     if (lane == 0) {
       const uint32_t bar = bar0 + 8 * s, dst = stage0 + s * C::kStageBytes;
@@ -258,7 +261,7 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 2)
       }
     }
   };
-  for (int k = 0; k < C::kStages && k < nw; ++k) issue(k);
+  for (int k = 0; k < C::kStages && cur.more; ++k) issue_next();
 
   // ---- lookup tables: byte -> (cb[lo], cb[hi]) for values (and 4-bit keys), 6-bit pair ->
   //      (cbk[lo], cbk[hi]) for 3-bit keys; 32 copies, entry e of copy l at word 32 e + l
@@ -350,7 +353,48 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 2)
   const float cap_pre = CAP ? 1.0f / (cap * kLog2e) : 0.0f;  // log2-domain score -> s_nat / cap
   const float cap_post = cap * kLog2e;
 
-  // ---- running state: column c = 2*tig + j of S^T and of every O^T column tile
+  // hi/lo role of this thread's two P columns (NV <= 4: column c carries part c / NV), and
+  // the positions its columns' query tokens attend: [lo_w, pos] (causal limit and window)
+  int part[2], lo_w[2], pos_c[2];
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    part[j] = NV <= 4 ? (2 * tig + j) / NV : 0;
+    pos_c[j] = L - a.T + (((2 * tig + j) % NV) % V) / G;
+    lo_w[j] = window_start(pos_c[j], a.window);
+  }
+  float* ep_o = reinterpret_cast<float*>(smem_gen + C::kOffMerge);  // [kWarps][NV][DP]
+  float* ep_m = ep_o + kWarps * NV * DP;                             // [kWarps][8]
+  float* ep_l = ep_m + kWarps * 8;                                   // [kWarps][8]
+
+  __syncthreads();  // lookup tables written
+
+  const int mi = lane >> 3, ri = lane & 7;  // ldmatrix (FP8 keys): matrix index and row of this lane's address
+  unsigned consumed = 0, stall_from = 0;
+  int cs = 0;            // stage of the next page to compute (consumed % kStages)
+  uint32_t cphase = 0;   // its mbarrier phase parity ((consumed / kStages) & 1)
+  bool stalled = false;  // a copy never arrived: no more waits, copies or compute
+
+  for (int p = p_begin; p < p_end; ++p) {
+  const Range r = partition_range(L, a.T, p, a.window, a.psize, a.thresh);
+  int first_page, npages;
+  range_pages(r, first_page, npages);
+  const int nw = warp_pages(npages, w, kWarps);
+  // tokens each column attends in this partition, and the pages that need no mask in any
+  // column: [lo_all, hi_all) (warp-uniform)
+  int lo_c[2], hi_c[2];
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    lo_c[j] = max(lo_w[j], r.start);
+    hi_c[j] = min(pos_c[j] + 1, r.end);
+  }
+  int lo_all = max(lo_c[0], lo_c[1]), hi_all = min(hi_c[0], hi_c[1]);
+  lo_all = max(lo_all, __shfl_xor_sync(kFull, lo_all, 1));
+  lo_all = max(lo_all, __shfl_xor_sync(kFull, lo_all, 2));
+  hi_all = min(hi_all, __shfl_xor_sync(kFull, hi_all, 1));
+  hi_all = min(hi_all, __shfl_xor_sync(kFull, hi_all, 2));
+  // ---- running state: column c = 2*tig + j of S^T and of every O^T column tile. O^T is kept
+  //      in units of 2^(ev_run - 127): ev_run is the largest biased binary32 exponent of the
+  //      value norms seen so far, so P * ||v|| * 2^(127 - ev_run) < 2^(kLazyLog2 + 1) fits f16
   float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.0f, 0.0f};
   float o[C::kNT][C::kMT][4];
 #pragma unroll
@@ -359,39 +403,20 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 2)
     for (int mt = 0; mt < C::kMT; ++mt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) o[t][mt][e] = 0.0f;
-  // hi/lo role of this thread's two P columns (NV <= 4: column c carries part c / NV), and
-  // the tokens each column attends in this partition (its query token's causal and window
-  // limits, within [r.start, r.end))
-  int part[2], lo_c[2], hi_c[2];
-#pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    part[j] = NV <= 4 ? (2 * tig + j) / NV : 0;
-    const int pos = L - a.T + (((2 * tig + j) % NV) % V) / G, lo = window_start(pos, a.window);
-    lo_c[j] = lo > r.start ? lo : r.start;
-    hi_c[j] = pos + 1 < r.end ? pos + 1 : r.end;
-  }
-  // pages inside [lo_all, hi_all) need no mask in any column (warp-uniform)
-  int lo_all = max(lo_c[0], lo_c[1]), hi_all = min(hi_c[0], hi_c[1]);
-  lo_all = max(lo_all, __shfl_xor_sync(kFull, lo_all, 1));
-  lo_all = max(lo_all, __shfl_xor_sync(kFull, lo_all, 2));
-  hi_all = min(hi_all, __shfl_xor_sync(kFull, hi_all, 1));
-  hi_all = min(hi_all, __shfl_xor_sync(kFull, hi_all, 2));
-  // O^T is kept in units of 2^(ev_run - 127): ev_run is the largest biased binary32 exponent
-  // of the value norms seen so far, so P * ||v|| * 2^(127 - ev_run) < 2^(kLazyLog2 + 1) fits f16
   int ev_run = 0;
   float v_unit = 1.0f;  // 2^(127 - ev_run)
 
-  __syncthreads();  // lookup tables written
-
-  const int mi = lane >> 3, ri = lane & 7;  // ldmatrix (FP8 keys): matrix index and row of this lane's address
-  int stalled_at = -1;
-  for (int i = 0; i < nw; ++i) {
-    const int s = i % C::kStages;
-    if (!ptx::mbar_wait(bar0 + 8 * s, (i / C::kStages) & 1)) {
-      stalled_at = i;
-      break;
+  for (int i = 0; i < nw; ++i, ++consumed) {
+    const int s = cs;
+    if (!stalled && !ptx::mbar_wait(bar0 + 8 * s, cphase)) {
+      stalled = true;
+      stall_from = consumed;
     }
-    if (valid_mask & (1u << s)) {
+    if (++cs == C::kStages) {
+      cs = 0;
+      cphase ^= 1u;
+    }
+    if (!stalled && (valid_mask & (1u << s))) {
       const uint32_t kb = stage0 + s * C::kStageBytes, vb = kb + C::kOffV;
       const int tok0 = (first_page + w + kWarps * i) * kPage;
       // -- S^T = K . Q^T
@@ -523,47 +548,46 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 2)
           vw[i4][0] = x.x, vw[i4][1] = x.y, vw[i4][2] = x.z, vw[i4][3] = x.w;
         }
       }
-      ValueTiles<0, C::kMT, D, C::kNT>::run(o, vw, lutv, pb);
+      // byte b of token t holds coordinates 2b (low nibble) and 2b + 1 (high nibble); pair
+      // tokens t, t + 1 into the index (code_t | code_t+1 << 4) of the table, whose entry is
+      // then the A register (v_t, v_t+1) of one coordinate
+      uint32_t vx[4][D / 64];
+#pragma unroll
+      for (int k = 0; k < D / 64; ++k) {
+        vx[0][k] = (vw[0][k] & 0x0f0f0f0fu) | ((vw[1][k] << 4) & 0xf0f0f0f0u);
+        vx[1][k] = ((vw[0][k] >> 4) & 0x0f0f0f0fu) | (vw[1][k] & 0xf0f0f0f0u);
+        vx[2][k] = (vw[2][k] & 0x0f0f0f0fu) | ((vw[3][k] << 4) & 0xf0f0f0f0u);
+        vx[3][k] = ((vw[2][k] >> 4) & 0x0f0f0f0fu) | (vw[3][k] & 0xf0f0f0f0u);
+      }
+      ValueTiles<0, C::kMT, D, C::kNT>::run(o, vx, lutv, pb);
     }
     __syncwarp();
-    if (i + C::kStages < nw) issue(i + C::kStages);
-  }
-  if (stalled_at >= 0) {
-    if (lane == 0) atomicOr(a.err, DA_DEVERR_TIMEOUT);
-    // give the copies still in flight into this warp's stages a bounded chance to land
-    for (int k = stalled_at; k < nw && k < stalled_at + C::kStages; ++k)
-      ptx::mbar_wait(bar0 + 8 * (k % C::kStages), (k / C::kStages) & 1);
+    if (!stalled && cur.more) issue_next();
   }
 
-  // ---- merge the warps through shared memory (tables and stages are free now); O^T back
-  //      to absolute units
+  // ---- partition epilogue: each warp's (o, m, l) per virtual head into shared memory (hi
+  //      and lo columns added, O^T back to absolute units), then the warps merged into the
+  //      partition's partial
   const float o_unit = ldexpf(1.0f, ev_run - 127);
-#pragma unroll
-  for (int t = 0; t < C::kNT; ++t)
-#pragma unroll
-    for (int mt = 0; mt < C::kMT; ++mt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) o[t][mt][e] *= o_unit;
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
     l_run[j] += __shfl_xor_sync(kFull, l_run[j], 4);
     l_run[j] += __shfl_xor_sync(kFull, l_run[j], 8);
     l_run[j] += __shfl_xor_sync(kFull, l_run[j], 16);
   }
-  __syncthreads();
-  float* ep_o = reinterpret_cast<float*>(smem_gen);  // [kWarps][kCols][D]
-  float* ep_m = ep_o + kWarps * C::kCols * D;          // [kWarps][8]
-  float* ep_l = ep_m + kWarps * 8;                     // [kWarps][8]
 #pragma unroll
-  for (int t = 0; t < C::kNT; ++t)
+  for (int mt = 0; mt < C::kMT; ++mt)
 #pragma unroll
-    for (int mt = 0; mt < C::kMT; ++mt) {
-      const int d0 = 2 * ((D / 16) * gid + mt);  // rows gid and gid + 8: the two coordinates of one byte
-      float* base = ep_o + (w * C::kCols + 8 * t + 2 * tig) * D;
-      base[d0] = o[t][mt][0];
-      base[D + d0] = o[t][mt][1];
-      base[d0 + 1] = o[t][mt][2];
-      base[D + d0 + 1] = o[t][mt][3];
+    for (int e = 0; e < 4; ++e) {
+      float v = o[0][mt][e];
+      if constexpr (NV == 8) v += o[C::kNT - 1][mt][e];
+      if constexpr (NV == 4) v += __shfl_xor_sync(kFull, v, 2);  // columns c, c + 4
+      if constexpr (NV == 2) v += __shfl_xor_sync(kFull, v, 1);  // columns c, c + 2
+      if constexpr (NV == 1) v += (e & 1) ? 0.0f : o[0][mt][e + 1];  // columns 0, 1
+      const int col = 2 * tig + (e & 1);
+      // O^T rows gid and gid + 8 of m-tile mt: the two coordinates of byte (D/16) gid + mt
+      const int rowd = 2 * ((D / 16) * gid + mt) + (e >> 1);
+      if (col < V) ep_o[(w * NV + col) * DP + rowd] = v * o_unit;
     }
   if (gid == 0) {
 #pragma unroll
@@ -574,7 +598,7 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 2)
   }
   __syncthreads();
   for (int idx = tid; idx < V * D; idx += kThreads) {
-    const int v = idx / D, d = idx % D;  // column v: the hi part of virtual head v, column v + NV its lo part
+    const int v = idx / D, d = idx % D;
     float M = -INFINITY;
 #pragma unroll
     for (int ww = 0; ww < kWarps; ++ww) M = fmaxf(M, ep_m[ww * 8 + v]);
@@ -583,8 +607,7 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 2)
     for (int ww = 0; ww < kWarps; ++ww) {
       const float mw = ep_m[ww * 8 + v];
       const float wt = mw == -INFINITY ? 0.0f : exp2f(mw - M);
-      const float* ow = ep_o + ww * C::kCols * D;
-      acc += wt * (ow[v * D + d] + ow[(v + NV) * D + d]);
+      acc += wt * ep_o[(ww * NV + v) * DP + d];
       l += wt * ep_l[ww * 8 + v];
     }
     const size_t pi = (((size_t)b * a.T + v / G) * a.Hq + g * G + v % G) * a.P + p;
@@ -593,6 +616,14 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 2)
       a.part_m[pi] = M;
       a.part_l[pi] = l;
     }
+  }
+  __syncthreads();  // the merge buffer is rewritten by the next partition
+  }  // partitions
+
+  if (stalled) {
+    if (lane == 0) atomicOr(a.err, DA_DEVERR_TIMEOUT);
+    // give the copies still in flight into this warp's stages a bounded chance to land
+    for (unsigned k = stall_from; k < issued; ++k) ptx::mbar_wait(bar0 + 8 * (k % C::kStages), (k / C::kStages) & 1);
   }
 }
 
@@ -639,7 +670,13 @@ cudaError_t launch_fixed(const Args& a, cudaStream_t s) {
   static DeviceFlags attr;
   cudaError_t e = ensure_dynamic_smem(kern, C::kSmem, attr);
   if (e != cudaSuccess) return e;
-  kern<<<dim3(a.P, a.Hkv, a.B), C::kThreads, C::kSmem, s>>>(a, km, vm);
+  static int per_sm = 0, sms[64] = {};
+  if (per_sm == 0 &&
+      (e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, C::kThreads, C::kSmem)) != cudaSuccess)
+    return e;
+  Args b = a;
+  b.ppc = partitions_per_cta(a, per_sm, sms);
+  kern<<<dim3((a.P + b.ppc - 1) / b.ppc, a.Hkv, a.B), C::kThreads, C::kSmem, s>>>(b, km, vm);
   return cudaGetLastError();
 }
 

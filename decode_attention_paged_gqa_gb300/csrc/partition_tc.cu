@@ -35,6 +35,7 @@
 
 #include "da_internal.cuh"
 #include "page_softmax.cuh"
+#include "page_walk.cuh"
 #include "ptx.cuh"
 
 namespace da {
@@ -57,12 +58,12 @@ struct Tc {
   static constexpr int kStageBytes = 2 * kPageBytes;        // K + V
   static constexpr int kStages = 16384 / kStageBytes > 0 ? 16384 / kStageBytes : 1;  // 64 KB of stages per CTA
   static constexpr int kNT = NV <= 4 ? 1 : 2;               // P.V column tiles (8 columns each)
-  static constexpr int kCols = 8 * kNT;
   static constexpr int kMT = D / 16;                        // O^T row tiles
   static constexpr int kKS = D / 16;                        // k-steps of S^T
   static constexpr int kStageSmem = kWarps * kStages * kStageBytes;
-  static constexpr int kEpiSmem = (kWarps * kCols * D + 2 * kWarps * 8) * 4;
-  static constexpr int kSmem = (kStageSmem > kEpiSmem ? kStageSmem : kEpiSmem) + 1024;
+  static constexpr int kDP = D + 4;  // padded row of the merge buffer
+  static constexpr int kMergeSmem = (kWarps * NV * kDP + 2 * kWarps * 8) * 4;
+  static constexpr int kSmem = kStageSmem + kMergeSmem + 1024;
 };
 
 __device__ __forceinline__ uint32_t swz(uint32_t slab, int row, int chunk) {
@@ -102,18 +103,20 @@ __device__ __forceinline__ void mma(float (&d)[4], const uint32_t (&a)[4], uint3
 
 // CAP: softcap on (a separate instantiation, so the plain kernel carries no tanh)
 template <int FMT, int D, int NV, bool CAP>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, D == 128 ? 3 : 2)
     partition_tc_kernel(const Args a, const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap) {
   using T = Tc<FMT, D, NV>;
-  const int p = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  constexpr int DP = T::kDP;
+  const int g = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int gid = lane >> 2, tig = lane & 3;
   const int G = a.Hq / a.Hkv, V = a.T * G;  // group size; virtual heads in use (<= NV)
-  const int L = load_len(a, b, p == 0 && g == 0 && tid == 0);
-  const Range r = partition_range(L, a.T, p, a.window, a.psize, a.thresh);
-  if (r.start >= r.end) return;
+  const int L = load_len(a, b, blockIdx.x == 0 && g == 0 && tid == 0);
   const int np = seq_partitions(L, a.T, a.window, a.psize, a.thresh);
+  // this CTA's partitions of (b, g)
+  const int p_begin = blockIdx.x * a.ppc, p_end = min(p_begin + a.ppc, np);
+  if (p_begin >= p_end) return;
 
   extern __shared__ unsigned char smem_raw[];
   __shared__ __align__(8) uint64_t bars[kWarps * T::kStages];
@@ -130,20 +133,17 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
   __syncwarp();
 
-  // ---- pages of this partition and this warp's share of them
-  const int first_page = r.start / kPage, npages = (r.end - 1) / kPage - first_page + 1;
-  const int nw = npages > w ? (npages - w + kWarps - 1) / kWarps : 0;
-  int bid = -1;  // lane l: physical block of local page 32*chunk + l
-  auto load_bids = [&](int chunk) {
-    const int i = 32 * chunk + lane;
-    bid = i < nw ? load_block(a, b, first_page + w + kWarps * i) : -1;
-  };
-  load_bids(0);
+  // ---- the warp's pages over the CTA's partitions, copied kStages ahead of the compute
+  IssueCursor<kWarps> cur;
+  cur.init(a, b, L, p_begin, p_end, w, lane);
   uint32_t valid_mask = 0;  // bit s: the page in stage s has a valid block (warp-uniform)
-  auto issue = [&](int k) {  // all lanes; lane 0 issues the copies of local page k
-    if (k > 0 && (k & 31) == 0) load_bids(k >> 5);
-    const int phys = __shfl_sync(kFull, bid, k & 31);
-    const int s = k % T::kStages;
+  unsigned issued = 0;
+  int is = 0;  // stage of the next copy (issued % kStages)
+  auto issue_next = [&]() {  // all lanes; lane 0 issues the copies of the page at the cursor
+    const int phys = cur.take(a);
+    const int s = is;
+    is = is + 1 == T::kStages ? 0 : is + 1;
+    ++issued;
     valid_mask = phys >= 0 ? (valid_mask | (1u << s)) : (valid_mask & ~(1u << s));
     if (lane == 0) {
       const uint32_t bar = bar0 + 8 * s, dst = stage0 + s * T::kStageBytes;
@@ -161,7 +161,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
     }
   };
-  for (int k = 0; k < T::kStages && k < nw; ++k) issue(k);
+  for (int k = 0; k < T::kStages && cur.more; ++k) issue_next();
 
   // ---- query fragments (B operand of S^T): column n holds virtual head (n % NV) % V
   const int qv = (gid % NV) % V;
@@ -202,6 +202,43 @@ __global__ void __launch_bounds__(kThreads, 2)
   const float cap_pre = CAP ? score_scale / (cap * kLog2e) : 0.0f;  // s_nat / cap
   const float cap_post = cap * kLog2e;
 
+  // hi/lo role of this thread's two columns (NV <= 4: column c carries part c / NV), and the
+  // positions its columns' query tokens attend: [lo_w, pos] (causal limit and window)
+  int part[2], lo_w[2], pos_c[2];
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    part[j] = NV <= 4 ? (2 * tig + j) / NV : 0;
+    pos_c[j] = L - a.T + (((2 * tig + j) % NV) % V) / G;
+    lo_w[j] = window_start(pos_c[j], a.window);
+  }
+  float* ep_o = reinterpret_cast<float*>(smem_gen + T::kStageSmem);  // [kWarps][NV][DP]
+  float* ep_m = ep_o + kWarps * NV * DP;                              // [kWarps][8]
+  float* ep_l = ep_m + kWarps * 8;                                    // [kWarps][8]
+  const float out_scale = FMT == DA_KV_FP8_E4M3 ? __ldg(a.v_scales) : 1.0f;
+  const int mi = lane >> 3, ri = lane & 7;  // ldmatrix: matrix index and row of this lane's address
+  unsigned consumed = 0, stall_from = 0;
+  int cs = 0;            // stage of the next page to compute (consumed % kStages)
+  uint32_t cphase = 0;   // its mbarrier phase parity ((consumed / kStages) & 1)
+  bool stalled = false;  // a copy never arrived: no more waits, copies or compute
+
+  for (int p = p_begin; p < p_end; ++p) {
+  const Range r = partition_range(L, a.T, p, a.window, a.psize, a.thresh);
+  int first_page, npages;
+  range_pages(r, first_page, npages);
+  const int nw = warp_pages(npages, w, kWarps);
+  // tokens each column attends in this partition, and the pages that need no mask in any
+  // column: [lo_all, hi_all) (warp-uniform)
+  int lo_c[2], hi_c[2];
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    lo_c[j] = max(lo_w[j], r.start);
+    hi_c[j] = min(pos_c[j] + 1, r.end);
+  }
+  int lo_all = max(lo_c[0], lo_c[1]), hi_all = min(hi_c[0], hi_c[1]);
+  lo_all = max(lo_all, __shfl_xor_sync(kFull, lo_all, 1));
+  lo_all = max(lo_all, __shfl_xor_sync(kFull, lo_all, 2));
+  hi_all = min(hi_all, __shfl_xor_sync(kFull, hi_all, 1));
+  hi_all = min(hi_all, __shfl_xor_sync(kFull, hi_all, 2));
   // ---- running state: column c = 2*tig + j of S^T and of every O^T column tile
   float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.0f, 0.0f};
   float o[T::kNT][T::kMT][4];
@@ -211,33 +248,18 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int mt = 0; mt < T::kMT; ++mt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) o[t][mt][e] = 0.0f;
-  // hi/lo role of this thread's two columns (NV <= 4: column c carries part c / NV), and the
-  // tokens each column attends in this partition: its query token's causal (and window)
-  // limits, within [r.start, r.end)
-  int part[2], lo_c[2], hi_c[2];
-#pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    part[j] = NV <= 4 ? (2 * tig + j) / NV : 0;
-    const int pos = L - a.T + (((2 * tig + j) % NV) % V) / G, lo = window_start(pos, a.window);
-    lo_c[j] = lo > r.start ? lo : r.start;
-    hi_c[j] = pos + 1 < r.end ? pos + 1 : r.end;
-  }
-  // pages inside [lo_all, hi_all) need no mask in any column (warp-uniform)
-  int lo_all = max(lo_c[0], lo_c[1]), hi_all = min(hi_c[0], hi_c[1]);
-  lo_all = max(lo_all, __shfl_xor_sync(kFull, lo_all, 1));
-  lo_all = max(lo_all, __shfl_xor_sync(kFull, lo_all, 2));
-  hi_all = min(hi_all, __shfl_xor_sync(kFull, hi_all, 1));
-  hi_all = min(hi_all, __shfl_xor_sync(kFull, hi_all, 2));
 
-  const int mi = lane >> 3, ri = lane & 7;  // ldmatrix: matrix index and row of this lane's address
-  int stalled_at = -1;  // local page whose copy never arrived (never expected)
-  for (int i = 0; i < nw; ++i) {
-    const int s = i % T::kStages;
-    if (!ptx::mbar_wait(bar0 + 8 * s, (i / T::kStages) & 1)) {
-      stalled_at = i;
-      break;
+  for (int i = 0; i < nw; ++i, ++consumed) {
+    const int s = cs;
+    if (!stalled && !ptx::mbar_wait(bar0 + 8 * s, cphase)) {
+      stalled = true;
+      stall_from = consumed;
     }
-    if (valid_mask & (1u << s)) {
+    if (++cs == T::kStages) {
+      cs = 0;
+      cphase ^= 1u;
+    }
+    if (!stalled && (valid_mask & (1u << s))) {
       const uint32_t kb = stage0 + s * T::kStageBytes, vb = kb + T::kPageBytes;
       const int tok0 = (first_page + w + kWarps * i) * kPage;
       // -- S^T = K . Q^T
@@ -336,37 +358,30 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
     }
     __syncwarp();
-    if (i + T::kStages < nw) issue(i + T::kStages);
-  }
-  if (stalled_at >= 0) {
-    if (lane == 0) atomicOr(a.err, DA_DEVERR_TIMEOUT);
-    // give the copies still in flight into this warp's stages a bounded chance to land
-    for (int k = stalled_at; k < nw && k < stalled_at + T::kStages; ++k)
-      ptx::mbar_wait(bar0 + 8 * (k % T::kStages), (k / T::kStages) & 1);
+    if (!stalled && cur.more) issue_next();
   }
 
-  // ---- merge the four warps through shared memory (the stage buffers are free now)
+  // ---- partition epilogue: each warp's (o, m, l) per virtual head into shared memory (hi
+  //      and lo columns added), then the warps merged into the partial (split sequence) or
+  //      the normalised output (unsplit)
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
     l_run[j] += __shfl_xor_sync(kFull, l_run[j], 4);
     l_run[j] += __shfl_xor_sync(kFull, l_run[j], 8);
     l_run[j] += __shfl_xor_sync(kFull, l_run[j], 16);
   }
-  __syncthreads();
-  float* ep_o = reinterpret_cast<float*>(smem_gen);  // [kWarps][kCols][D]
-  float* ep_m = ep_o + kWarps * T::kCols * D;          // [kWarps][8]
-  float* ep_l = ep_m + kWarps * 8;                     // [kWarps][8]
 #pragma unroll
-  for (int t = 0; t < T::kNT; ++t)
+  for (int mt = 0; mt < T::kMT; ++mt)
 #pragma unroll
-    for (int mt = 0; mt < T::kMT; ++mt) {
-      const int d0 = FMT == DA_KV_BF16 ? 16 * mt + gid : 16 * mt + 2 * gid;
-      const int d1 = FMT == DA_KV_BF16 ? d0 + 8 : d0 + 1;
-      float* base = ep_o + (w * T::kCols + 8 * t + 2 * tig) * D;
-      base[d0] = o[t][mt][0];
-      base[D + d0] = o[t][mt][1];
-      base[d1] = o[t][mt][2];
-      base[D + d1] = o[t][mt][3];
+    for (int e = 0; e < 4; ++e) {
+      float v = o[0][mt][e];
+      if constexpr (NV == 8) v += o[T::kNT - 1][mt][e];
+      if constexpr (NV == 4) v += __shfl_xor_sync(kFull, v, 2);  // columns c, c + 4
+      if constexpr (NV == 2) v += __shfl_xor_sync(kFull, v, 1);  // columns c, c + 2
+      if constexpr (NV == 1) v += (e & 1) ? 0.0f : o[0][mt][e + 1];  // columns 0, 1
+      const int col = 2 * tig + (e & 1);
+      const int rowd = FMT == DA_KV_BF16 ? 16 * mt + gid + ((e >> 1) ? 8 : 0) : 16 * mt + 2 * gid + (e >> 1);
+      if (col < V) ep_o[(w * NV + col) * DP + rowd] = v;
     }
   if (gid == 0) {
 #pragma unroll
@@ -377,9 +392,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
   __syncthreads();
   const bool direct = np == 1;
-  const float out_scale = FMT == DA_KV_FP8_E4M3 ? __ldg(a.v_scales) : 1.0f;
   for (int idx = tid; idx < V * D; idx += kThreads) {
-    const int v = idx / D, d = idx % D;  // column v: the hi part of virtual head v, column v + NV its lo part
+    const int v = idx / D, d = idx % D;
     float M = -INFINITY;
 #pragma unroll
     for (int ww = 0; ww < kWarps; ++ww) M = fmaxf(M, ep_m[ww * 8 + v]);
@@ -388,8 +402,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int ww = 0; ww < kWarps; ++ww) {
       const float mw = ep_m[ww * 8 + v];
       const float wt = mw == -INFINITY ? 0.0f : exp2f(mw - M);
-      const float* ow = ep_o + ww * T::kCols * D;
-      acc += wt * (ow[v * D + d] + ow[(v + NV) * D + d]);
+      acc += wt * ep_o[(ww * NV + v) * DP + d];
       l += wt * ep_l[ww * 8 + v];
     }
     const size_t bh = ((size_t)b * a.T + v / G) * a.Hq + g * G + v % G;
@@ -403,6 +416,14 @@ __global__ void __launch_bounds__(kThreads, 2)
         a.part_l[pi] = l;
       }
     }
+  }
+  __syncthreads();  // the merge buffer is rewritten by the next partition
+  }  // partitions
+
+  if (stalled) {
+    if (lane == 0) atomicOr(a.err, DA_DEVERR_TIMEOUT);
+    // give the copies still in flight into this warp's stages a bounded chance to land
+    for (unsigned k = stall_from; k < issued; ++k) ptx::mbar_wait(bar0 + 8 * (k % T::kStages), (k / T::kStages) & 1);
   }
 }
 
@@ -448,7 +469,12 @@ cudaError_t launch_fixed(const Args& a, cudaStream_t s) {
   static DeviceFlags attr;
   cudaError_t e = ensure_dynamic_smem(kern, T::kSmem, attr);
   if (e != cudaSuccess) return e;
-  kern<<<dim3(a.P, a.Hkv, a.B), kThreads, T::kSmem, s>>>(a, km, vm);
+  static int per_sm = 0, sms[64] = {};
+  if (per_sm == 0 && (e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, T::kSmem)) != cudaSuccess)
+    return e;
+  Args b = a;
+  b.ppc = partitions_per_cta(a, per_sm, sms);
+  kern<<<dim3((a.P + b.ppc - 1) / b.ppc, a.Hkv, a.B), kThreads, T::kSmem, s>>>(b, km, vm);
   return cudaGetLastError();
 }
 

@@ -1,11 +1,12 @@
 // page_walk.cuh -- which pages a warp of a partition kernel handles, and in what order.
 //
-// A CTA handles the partitions [p_begin, p_end) of one (sequence, kv head), one after the
-// other; inside a partition (first page f, n pages of 16 tokens) warp w of W takes pages
-// f + w, f + w + W, ... The copy side of a warp walks this list ahead of the compute side
-// with IssueCursor, across partition boundaries, so the next partition's pages are already
-// in flight while a partition is merged; the compute side walks the same list with the same
-// counts (warp_pages).
+// A CTA handles partitions [p_begin, p_end) of one (sequence, kv head). Either its warps
+// share each partition (warp w of W takes pages f + w, f + w + W, ... of a partition whose
+// first page is f) and walk the partitions one after the other, or each warp owns whole
+// partitions (p_begin + w, p_begin + w + W, ...). The copy side of a warp walks its page list
+// ahead of the compute side with IssueCursor, across partition boundaries, so the next
+// partition's pages are already in flight while a partition is finished; the compute side
+// walks the same list with the same counts (warp_pages).
 #pragma once
 
 #include "da_internal.cuh"
@@ -23,26 +24,30 @@ __device__ __forceinline__ void range_pages(const Range& r, int& first, int& npa
   npages = (r.end - 1) / kPageTokens - first + 1;
 }
 
-template <int W>
+// Walks the pages a warp copies: partitions p0, p0 + p_step, ... below p_end; in each, the
+// pages first + page_off, first + page_off + page_step, ... (page_step W, page_off w when the
+// warps of a CTA share a partition; 1 and 0 when a warp owns whole partitions).
 struct IssueCursor {
-  int b, L, w, lane;
-  int p, p_end;  // partition of the cursor, end of the CTA's partitions
-  int i, n;      // index of the warp's next page in partition p, and the warp's page count there
-  int first;     // first page of partition p
-  int bid;       // lane l: physical block of the warp's page (i & ~31) + l of partition p (-1 if none)
-  bool more;     // a page is left at the cursor
+  int b, L, lane;
+  int p, p_step, p_end;   // partition of the cursor, stride between the warp's partitions, end
+  int page_off, page_step;
+  int i, n;               // index of the warp's next page in partition p, and its page count there
+  int first;              // first page of partition p
+  int bid;                // lane l: physical block of the warp's page (i & ~31) + l of partition p (-1 if none)
+  bool more;              // a page is left at the cursor
 
   __device__ __forceinline__ void load_bids(const Args& a) {
     const int k = (i & ~31) + lane;
-    bid = k < n ? load_block(a, b, first + w + W * k) : -1;
+    bid = k < n ? load_block(a, b, first + page_off + page_step * k) : -1;
   }
-  // Moves to the next partition that has pages for this warp.
+  // Moves to the next of the warp's partitions that has pages for it (the first one when
+  // p < p0 on entry).
   __device__ __forceinline__ void next_partition(const Args& a) {
     more = false;
-    while (++p < p_end) {
+    for (p += p_step; p < p_end; p += p_step) {
       int npages;
       range_pages(partition_range(L, a.T, p, a.window, a.psize, a.thresh), first, npages);
-      n = warp_pages(npages, w, W);
+      n = warp_pages(npages, page_off, page_step);
       i = 0;
       if (n > 0) {
         more = true;
@@ -51,13 +56,16 @@ struct IssueCursor {
       }
     }
   }
-  __device__ __forceinline__ void init(const Args& a, int b_, int L_, int p_begin, int p_end_, int w_, int lane_) {
+  __device__ __forceinline__ void init(const Args& a, int b_, int L_, int p0, int p_step_, int p_end_, int page_off_,
+                                       int page_step_, int lane_) {
     b = b_;
     L = L_;
-    w = w_;
     lane = lane_;
-    p = p_begin - 1;
+    p_step = p_step_;
+    p = p0 - p_step;
     p_end = p_end_;
+    page_off = page_off_;
+    page_step = page_step_;
     next_partition(a);
   }
   // Physical block (-1: bad block id, nothing to load) of the page at the cursor, the same

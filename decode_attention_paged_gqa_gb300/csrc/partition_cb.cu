@@ -3,11 +3,13 @@
 // 4-bit V, 3-bit K + 4-bit V. Tensor-core MMAs on operands dequantised through a shared-
 // memory lookup table.
 //
-// One CTA per (partition p, kv head g, sequence b), four warps; the partition's pages are
-// dealt round-robin to the warps, each with its own pipeline of shared-memory stages filled
-// by TMA / bulk copies (a page's K codes, V codes and their per-token norms) and signalled on
-// an mbarrier, as in the BF16 / FP8 kernel. Per page a warp computes, in the rotated basis
-// (the keys' and values' own basis, no dequantisation to the original one):
+// A CTA of four or eight warps takes consecutive partitions of one (sequence, kv head); each
+// warp owns whole partitions (p_begin + w, p_begin + w + W, ...), so it writes its partition's
+// partial itself and no warp ever waits for another after the tables are built. Each warp
+// runs its own pipeline of shared-memory stages filled by TMA / bulk copies (a page's K
+// codes, V codes and their per-token norms) and signalled on an mbarrier, continuing across
+// its partitions. Per page a warp computes, in the rotated basis (the keys' and values' own
+// basis, no dequantisation to the original one):
 //   S^T[16 tokens x 8 cols] = K_rot[16 x D] . Q_rot^T     then  s_t *= ||k_t||
 //   O^T[D x 8 cols]        += V_rot^T[D x 16] . (P ||v||)^T
 // with mma.m16n8k16 on f16 operands and fp32 accumulators. A codebook operand is built
@@ -86,7 +88,7 @@ struct Cb {
   static constexpr int kLutV = 256 * 32 * 4;  // 4-bit pair table, 32 copies
   static constexpr int kLutK = KS == kSideCB3 ? 64 * 32 * 4 : 0;
   static constexpr int kDP = D + 4;  // padded row of the merge buffer
-  static constexpr int kMergeSmem = (kWarps * NV * kDP + 2 * kWarps * 8) * 4;
+  static constexpr int kMergeSmem = kWarps * NV * kDP * 4;  // each warp's output staging
   // stages: what two CTAs per SM leave after the tables and the merge buffer (228 KB per SM,
   // 1 KB reserved and ~2 KB of alignment slack and barriers per CTA), 2 to 6 per warp
   static constexpr int kStageBudget = (233472 / 2 - 3072 - kLutV - kLutK - kMergeSmem) / kWarps;
@@ -226,9 +228,10 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 2)
   }
   __syncwarp();
 
-  // ---- the warp's pages over the CTA's partitions, copied kStages ahead of the compute
-  IssueCursor<kWarps> cur;
-  cur.init(a, b, L, p_begin, p_end, w, lane);
+  // ---- the warp's partitions (p_begin + w, p_begin + w + kWarps, ...) and all their pages,
+  //      copied kStages ahead of the compute
+  IssueCursor cur;
+  cur.init(a, b, L, p_begin + w, kWarps, p_end, 0, 1, lane);
   uint32_t valid_mask = 0;  // bit s: the page in stage s has a valid block (warp-uniform)
   unsigned issued = 0;
   int is = 0;  // stage of the next copy (issued % kStages)
@@ -362,9 +365,7 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 2)
     pos_c[j] = L - a.T + (((2 * tig + j) % NV) % V) / G;
     lo_w[j] = window_start(pos_c[j], a.window);
   }
-  float* ep_o = reinterpret_cast<float*>(smem_gen + C::kOffMerge);  // [kWarps][NV][DP]
-  float* ep_m = ep_o + kWarps * NV * DP;                             // [kWarps][8]
-  float* ep_l = ep_m + kWarps * 8;                                   // [kWarps][8]
+  float* ep_o = reinterpret_cast<float*>(smem_gen + C::kOffMerge) + w * NV * DP;  // this warp's [NV][DP]
 
   __syncthreads();  // lookup tables written
 
@@ -374,11 +375,10 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 2)
   uint32_t cphase = 0;   // its mbarrier phase parity ((consumed / kStages) & 1)
   bool stalled = false;  // a copy never arrived: no more waits, copies or compute
 
-  for (int p = p_begin; p < p_end; ++p) {
+  for (int p = p_begin + w; p < p_end; p += kWarps) {
   const Range r = partition_range(L, a.T, p, a.window, a.psize, a.thresh);
-  int first_page, npages;
-  range_pages(r, first_page, npages);
-  const int nw = warp_pages(npages, w, kWarps);
+  int first_page, nw;
+  range_pages(r, first_page, nw);
   // tokens each column attends in this partition, and the pages that need no mask in any
   // column: [lo_all, hi_all) (warp-uniform)
   int lo_c[2], hi_c[2];
@@ -418,7 +418,7 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 2)
     }
     if (!stalled && (valid_mask & (1u << s))) {
       const uint32_t kb = stage0 + s * C::kStageBytes, vb = kb + C::kOffV;
-      const int tok0 = (first_page + w + kWarps * i) * kPage;
+      const int tok0 = (first_page + i) * kPage;
       // -- S^T = K . Q^T
       float sc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
       if constexpr (KS == kSideFP8) {
@@ -565,9 +565,9 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 2)
     if (!stalled && cur.more) issue_next();
   }
 
-  // ---- partition epilogue: each warp's (o, m, l) per virtual head into shared memory (hi
-  //      and lo columns added, O^T back to absolute units), then the warps merged into the
-  //      partition's partial
+  // ---- partition epilogue: the warp's (o, m, l) is the partition's partial. O^T (hi and lo
+  //      columns added, back to absolute units) goes through the warp's staging buffer so
+  //      the stores are whole 16-byte vectors along D
   const float o_unit = ldexpf(1.0f, ev_run - 127);
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
@@ -587,37 +587,26 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 2)
       const int col = 2 * tig + (e & 1);
       // O^T rows gid and gid + 8 of m-tile mt: the two coordinates of byte (D/16) gid + mt
       const int rowd = 2 * ((D / 16) * gid + mt) + (e >> 1);
-      if (col < V) ep_o[(w * NV + col) * DP + rowd] = v * o_unit;
+      if (col < V) ep_o[col * DP + rowd] = v * o_unit;
     }
   if (gid == 0) {
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
-      ep_m[w * 8 + 2 * tig + j] = m_run[j];
-      ep_l[w * 8 + 2 * tig + j] = l_run[j];
+      const int col = 2 * tig + j;
+      if (col < V) {
+        const size_t pi = (((size_t)b * a.T + col / G) * a.Hq + g * G + col % G) * a.P + p;
+        a.part_m[pi] = m_run[j];
+        a.part_l[pi] = l_run[j];
+      }
     }
   }
-  __syncthreads();
-  for (int idx = tid; idx < V * D; idx += kThreads) {
-    const int v = idx / D, d = idx % D;
-    float M = -INFINITY;
-#pragma unroll
-    for (int ww = 0; ww < kWarps; ++ww) M = fmaxf(M, ep_m[ww * 8 + v]);
-    float acc = 0.0f, l = 0.0f;
-#pragma unroll
-    for (int ww = 0; ww < kWarps; ++ww) {
-      const float mw = ep_m[ww * 8 + v];
-      const float wt = mw == -INFINITY ? 0.0f : exp2f(mw - M);
-      acc += wt * ep_o[(ww * NV + v) * DP + d];
-      l += wt * ep_l[ww * 8 + v];
-    }
+  __syncwarp();
+  for (int idx = lane; idx < V * D / 4; idx += 32) {
+    const int v = idx / (D / 4), d = 4 * (idx % (D / 4));
     const size_t pi = (((size_t)b * a.T + v / G) * a.Hq + g * G + v % G) * a.P + p;
-    a.part_o[pi * D + d] = acc;
-    if (d == 0) {
-      a.part_m[pi] = M;
-      a.part_l[pi] = l;
-    }
+    *reinterpret_cast<float4*>(a.part_o + pi * D + d) = *reinterpret_cast<const float4*>(ep_o + v * DP + d);
   }
-  __syncthreads();  // the merge buffer is rewritten by the next partition
+  __syncwarp();  // the staging buffer is rewritten by the warp's next partition
   }  // partitions
 
   if (stalled) {
@@ -674,8 +663,9 @@ cudaError_t launch_fixed(const Args& a, cudaStream_t s) {
   if (per_sm == 0 &&
       (e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, C::kThreads, C::kSmem)) != cudaSuccess)
     return e;
+  // each warp owns whole partitions: a CTA takes kWarps (or a multiple) consecutive ones
   Args b = a;
-  b.ppc = partitions_per_cta(a, per_sm, sms);
+  b.ppc = C::kWarps * ((partitions_per_cta(a, per_sm, sms) + C::kWarps - 1) / C::kWarps);
   kern<<<dim3((a.P + b.ppc - 1) / b.ppc, a.Hkv, a.B), C::kThreads, C::kSmem, s>>>(b, km, vm);
   return cudaGetLastError();
 }

@@ -134,8 +134,8 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 3 : 2)
   __syncwarp();
 
   // ---- the warp's pages over the CTA's partitions, copied kStages ahead of the compute
-  IssueCursor<kWarps> cur;
-  cur.init(a, b, L, p_begin, p_end, w, lane);
+  IssueCursor cur;
+  cur.init(a, b, L, p_begin, 1, p_end, w, kWarps, lane);
   uint32_t valid_mask = 0;  // bit s: the page in stage s has a valid block (warp-uniform)
   unsigned issued = 0;
   int is = 0;  // stage of the next copy (issued % kStages)

@@ -35,6 +35,10 @@ struct Args {
   int window, psize, thresh;
   int P;                      // partitions the grid and the workspace are sized for
   int ppc;                    // partitions a partition-kernel CTA walks (set by its launcher)
+  int schedule;               // da_params.partition_schedule (0 automatic, 1 shared, 2 owned)
+  int ppc_req;                // da_params.partitions_per_cta (0 automatic)
+  int owner;                  // 1: each warp of a partition kernel owns whole partitions, 0: the
+                              // warps of a CTA share each partition (set by its launcher)
   // workspace pieces
   uint32_t* err;              // device error word (DA_DEVERR_* bits)
   float* q_rot;               // [B][T][Hq][D] (formats whose keys are on the rotated basis)
@@ -171,20 +175,35 @@ int run_phases(int phases, const void* q, const void* k, const void* v, const fl
                const float* cb, const float* sign, const int32_t* bt, const int32_t* lens, float* out,
                const da_params* p, void* stream);
 
-// Partitions per CTA for a partition kernel with `per_sm` resident CTAs per SM: the CTAs
-// walk consecutive partitions of one (sequence, kv head) so their pipelines stay full across
-// partition boundaries, while the grid keeps about eight waves of CTAs. Cached per device.
+// Partitions per CTA for a partition kernel with `per_sm` resident CTAs per SM: as requested,
+// else enough that the CTAs walk consecutive partitions of one (sequence, kv head) with their
+// pipelines full across partition boundaries, while the grid keeps about eight waves of CTAs.
+// Also caches the device's SM count.
 inline int partitions_per_cta(const Args& a, int per_sm, int* cached_sms) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return a.ppc_req > 0 ? a.ppc_req : 1;
   if (cached_sms[dev] == 0) {
     int sms = 0;
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) return 1;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+      return a.ppc_req > 0 ? a.ppc_req : 1;
     cached_sms[dev] = sms;
   }
+  if (a.ppc_req > 0) return a.ppc_req;
   const long long units = (long long)a.P * a.Hkv * a.B;
   const long long waves = units / (8ll * cached_sms[dev] * (per_sm > 0 ? per_sm : 1));
   return waves < 1 ? 1 : (waves > 8 ? 8 : (int)waves);
+}
+
+// Whether a partition kernel's warps own whole partitions: as requested, else only when
+// there are at least two partitions for every warp the GPU holds at once (else sharing each
+// partition among a CTA's warps keeps more warps busy).
+inline bool warps_own_partitions(const Args& a, int per_sm, int warps_per_cta, const int* cached_sms) {
+  if (a.schedule == 1) return false;
+  if (a.schedule == 2) return true;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || cached_sms[dev] <= 0) return false;
+  const long long units = (long long)a.P * a.Hkv * a.B;
+  return units >= 2ll * cached_sms[dev] * (per_sm > 0 ? per_sm : 1) * warps_per_cta;
 }
 
 // Launchers (one translation unit each). They return cudaGetLastError() of their launch.

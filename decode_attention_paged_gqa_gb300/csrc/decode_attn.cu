@@ -24,7 +24,8 @@ int check_params(const da_params* p) {
   if (p->batch < 0 || p->query_len < 0 || p->num_q_heads <= 0 || p->num_kv_heads <= 0 || p->head_dim <= 0 ||
       p->block_size <= 0 ||
       p->num_blocks <= 0 || p->max_blocks_per_seq <= 0 || p->max_context_len < 0 || p->window < 0 ||
-      p->partition_size < 0 || p->split_threshold < 0)
+      p->partition_size < 0 || p->split_threshold < 0 || p->partition_schedule < 0 || p->partition_schedule > 2 ||
+      p->partitions_per_cta < 0 || p->partitions_per_cta > 64)
     return DA_ERR_INVALID_ARG;
   if (p->num_q_heads % p->num_kv_heads) return DA_ERR_INVALID_ARG;
   if (!std::isfinite(p->softmax_scale) || !std::isfinite(p->softcap) || p->softcap < 0.0f) return DA_ERR_INVALID_ARG;
@@ -95,6 +96,9 @@ Args make_args(const void* q, const void* k, const void* v, const float* ks, con
   a.thresh = p->split_threshold;
   a.P = host_max_partitions(*p);
   a.ppc = 1;
+  a.schedule = p->partition_schedule;
+  a.ppc_req = p->partitions_per_cta;
+  a.owner = 0;
   const Layout l = workspace_layout(*p);
   char* ws = static_cast<char*>(p->workspace);
   a.err = reinterpret_cast<uint32_t*>(ws + l.err);

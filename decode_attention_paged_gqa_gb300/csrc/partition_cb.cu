@@ -88,7 +88,8 @@ struct Cb {
   static constexpr int kLutV = 256 * 32 * 4;  // 4-bit pair table, 32 copies
   static constexpr int kLutK = KS == kSideCB3 ? 64 * 32 * 4 : 0;
   static constexpr int kDP = D + 4;  // padded row of the merge buffer
-  static constexpr int kMergeSmem = kWarps * NV * kDP * 4;  // each warp's output staging
+  // each warp's output staging (a warp owns the partition), or the cross-warp merge buffer
+  static constexpr int kMergeSmem = (kWarps * NV * kDP + 2 * kWarps * 8) * 4;
   // stages: what two CTAs per SM leave after the tables and the merge buffer (228 KB per SM,
   // 1 KB reserved and ~2 KB of alignment slack and barriers per CTA), 2 to 6 per warp
   static constexpr int kStageBudget = (233472 / 2 - 3072 - kLutV - kLutK - kMergeSmem) / kWarps;
@@ -228,10 +229,14 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 2)
   }
   __syncwarp();
 
-  // ---- the warp's partitions (p_begin + w, p_begin + w + kWarps, ...) and all their pages,
-  //      copied kStages ahead of the compute
+  // ---- the warp's partitions and pages, copied kStages ahead of the compute: with
+  //      a.owner, partitions p_begin + w, p_begin + w + kWarps, ... and all their pages; else
+  //      every partition of the CTA and pages w, w + kWarps, ... of each
+  const bool owner = a.owner != 0;
+  const int p_first = owner ? p_begin + w : p_begin, p_step = owner ? kWarps : 1;
+  const int pg_off = owner ? 0 : w, pg_step = owner ? 1 : kWarps;
   IssueCursor cur;
-  cur.init(a, b, L, p_begin + w, kWarps, p_end, 0, 1, lane);
+  cur.init(a, b, L, p_first, p_step, p_end, pg_off, pg_step, lane);
   uint32_t valid_mask = 0;  // bit s: the page in stage s has a valid block (warp-uniform)
   unsigned issued = 0;
   int is = 0;  // stage of the next copy (issued % kStages)
@@ -365,7 +370,9 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 2)
     pos_c[j] = L - a.T + (((2 * tig + j) % NV) % V) / G;
     lo_w[j] = window_start(pos_c[j], a.window);
   }
-  float* ep_o = reinterpret_cast<float*>(smem_gen + C::kOffMerge) + w * NV * DP;  // this warp's [NV][DP]
+  float* ep_o = reinterpret_cast<float*>(smem_gen + C::kOffMerge);  // [kWarps][NV][DP]
+  float* ep_m = ep_o + kWarps * NV * DP;                             // [kWarps][8]
+  float* ep_l = ep_m + kWarps * 8;                                   // [kWarps][8]
 
   __syncthreads();  // lookup tables written
 
@@ -375,10 +382,11 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 2)
   uint32_t cphase = 0;   // its mbarrier phase parity ((consumed / kStages) & 1)
   bool stalled = false;  // a copy never arrived: no more waits, copies or compute
 
-  for (int p = p_begin + w; p < p_end; p += kWarps) {
+  for (int p = p_first; p < p_end; p += p_step) {
   const Range r = partition_range(L, a.T, p, a.window, a.psize, a.thresh);
-  int first_page, nw;
-  range_pages(r, first_page, nw);
+  int first_page, npages;
+  range_pages(r, first_page, npages);
+  const int nw = warp_pages(npages, pg_off, pg_step);
   // tokens each column attends in this partition, and the pages that need no mask in any
   // column: [lo_all, hi_all) (warp-uniform)
   int lo_c[2], hi_c[2];
@@ -418,7 +426,7 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 2)
     }
     if (!stalled && (valid_mask & (1u << s))) {
       const uint32_t kb = stage0 + s * C::kStageBytes, vb = kb + C::kOffV;
-      const int tok0 = (first_page + i) * kPage;
+      const int tok0 = (first_page + pg_off + pg_step * i) * kPage;
       // -- S^T = K . Q^T
       float sc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
       if constexpr (KS == kSideFP8) {
@@ -565,9 +573,7 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 2)
     if (!stalled && cur.more) issue_next();
   }
 
-  // ---- partition epilogue: the warp's (o, m, l) is the partition's partial. O^T (hi and lo
-  //      columns added, back to absolute units) goes through the warp's staging buffer so
-  //      the stores are whole 16-byte vectors along D
+  // ---- partition epilogue (O^T: hi and lo columns added, back to absolute units)
   const float o_unit = ldexpf(1.0f, ev_run - 127);
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
@@ -575,6 +581,7 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 2)
     l_run[j] += __shfl_xor_sync(kFull, l_run[j], 8);
     l_run[j] += __shfl_xor_sync(kFull, l_run[j], 16);
   }
+  float* ep_w = ep_o + w * NV * DP;
 #pragma unroll
   for (int mt = 0; mt < C::kMT; ++mt)
 #pragma unroll
@@ -587,26 +594,61 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 2)
       const int col = 2 * tig + (e & 1);
       // O^T rows gid and gid + 8 of m-tile mt: the two coordinates of byte (D/16) gid + mt
       const int rowd = 2 * ((D / 16) * gid + mt) + (e >> 1);
-      if (col < V) ep_o[col * DP + rowd] = v * o_unit;
+      if (col < V) ep_w[col * DP + rowd] = v * o_unit;
     }
+  if (owner) {
+    // the warp's (o, m, l) is the partition's partial: m and l from the column owners, O^T
+    // from the staging buffer in 16-byte stores
+    if (gid == 0) {
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int col = 2 * tig + j;
+        if (col < V) {
+          const size_t pi = (((size_t)b * a.T + col / G) * a.Hq + g * G + col % G) * a.P + p;
+          a.part_m[pi] = m_run[j];
+          a.part_l[pi] = l_run[j];
+        }
+      }
+    }
+    __syncwarp();
+    for (int idx = lane; idx < V * D / 4; idx += 32) {
+      const int v = idx / (D / 4), d = 4 * (idx % (D / 4));
+      const size_t pi = (((size_t)b * a.T + v / G) * a.Hq + g * G + v % G) * a.P + p;
+      *reinterpret_cast<float4*>(a.part_o + pi * D + d) = *reinterpret_cast<const float4*>(ep_w + v * DP + d);
+    }
+    __syncwarp();  // the staging buffer is rewritten by the warp's next partition
+    continue;
+  }
+  // shared partition: the warps' (o, m, l) merged into the partition's partial
   if (gid == 0) {
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
-      const int col = 2 * tig + j;
-      if (col < V) {
-        const size_t pi = (((size_t)b * a.T + col / G) * a.Hq + g * G + col % G) * a.P + p;
-        a.part_m[pi] = m_run[j];
-        a.part_l[pi] = l_run[j];
-      }
+      ep_m[w * 8 + 2 * tig + j] = m_run[j];
+      ep_l[w * 8 + 2 * tig + j] = l_run[j];
     }
   }
-  __syncwarp();
-  for (int idx = lane; idx < V * D / 4; idx += 32) {
-    const int v = idx / (D / 4), d = 4 * (idx % (D / 4));
+  __syncthreads();
+  for (int idx = tid; idx < V * D; idx += kThreads) {
+    const int v = idx / D, d = idx % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int ww = 0; ww < kWarps; ++ww) M = fmaxf(M, ep_m[ww * 8 + v]);
+    float acc = 0.0f, l = 0.0f;
+#pragma unroll
+    for (int ww = 0; ww < kWarps; ++ww) {
+      const float mw = ep_m[ww * 8 + v];
+      const float wt = mw == -INFINITY ? 0.0f : exp2f(mw - M);
+      acc += wt * ep_o[(ww * NV + v) * DP + d];
+      l += wt * ep_l[ww * 8 + v];
+    }
     const size_t pi = (((size_t)b * a.T + v / G) * a.Hq + g * G + v % G) * a.P + p;
-    *reinterpret_cast<float4*>(a.part_o + pi * D + d) = *reinterpret_cast<const float4*>(ep_o + v * DP + d);
+    a.part_o[pi * D + d] = acc;
+    if (d == 0) {
+      a.part_m[pi] = M;
+      a.part_l[pi] = l;
+    }
   }
-  __syncwarp();  // the staging buffer is rewritten by the warp's next partition
+  __syncthreads();  // the merge buffer is rewritten by the next partition
   }  // partitions
 
   if (stalled) {
@@ -663,9 +705,12 @@ cudaError_t launch_fixed(const Args& a, cudaStream_t s) {
   if (per_sm == 0 &&
       (e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, C::kThreads, C::kSmem)) != cudaSuccess)
     return e;
-  // each warp owns whole partitions: a CTA takes kWarps (or a multiple) consecutive ones
+  // where there are partitions enough, each warp owns whole partitions and a CTA takes kWarps
+  // (or a multiple) consecutive ones
   Args b = a;
-  b.ppc = C::kWarps * ((partitions_per_cta(a, per_sm, sms) + C::kWarps - 1) / C::kWarps);
+  b.ppc = partitions_per_cta(a, per_sm, sms);
+  b.owner = warps_own_partitions(a, per_sm, C::kWarps, sms);
+  if (b.owner) b.ppc = C::kWarps * ((b.ppc + C::kWarps - 1) / C::kWarps);
   kern<<<dim3((a.P + b.ppc - 1) / b.ppc, a.Hkv, a.B), C::kThreads, C::kSmem, s>>>(b, km, vm);
   return cudaGetLastError();
 }

@@ -133,9 +133,14 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 3 : 2)
   }
   __syncwarp();
 
-  // ---- the warp's pages over the CTA's partitions, copied kStages ahead of the compute
+  // ---- the warp's partitions and pages, copied kStages ahead of the compute: with
+  //      a.owner, partitions p_begin + w, p_begin + w + kWarps, ... and all their pages; else
+  //      every partition of the CTA and pages w, w + kWarps, ... of each
+  const bool owner = a.owner != 0;
+  const int p_first = owner ? p_begin + w : p_begin, p_step = owner ? kWarps : 1;
+  const int pg_off = owner ? 0 : w, pg_step = owner ? 1 : kWarps;
   IssueCursor cur;
-  cur.init(a, b, L, p_begin, 1, p_end, w, kWarps, lane);
+  cur.init(a, b, L, p_first, p_step, p_end, pg_off, pg_step, lane);
   uint32_t valid_mask = 0;  // bit s: the page in stage s has a valid block (warp-uniform)
   unsigned issued = 0;
   int is = 0;  // stage of the next copy (issued % kStages)
@@ -221,11 +226,11 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 3 : 2)
   uint32_t cphase = 0;   // its mbarrier phase parity ((consumed / kStages) & 1)
   bool stalled = false;  // a copy never arrived: no more waits, copies or compute
 
-  for (int p = p_begin; p < p_end; ++p) {
+  for (int p = p_first; p < p_end; p += p_step) {
   const Range r = partition_range(L, a.T, p, a.window, a.psize, a.thresh);
   int first_page, npages;
   range_pages(r, first_page, npages);
-  const int nw = warp_pages(npages, w, kWarps);
+  const int nw = warp_pages(npages, pg_off, pg_step);
   // tokens each column attends in this partition, and the pages that need no mask in any
   // column: [lo_all, hi_all) (warp-uniform)
   int lo_c[2], hi_c[2];
@@ -261,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 3 : 2)
     }
     if (!stalled && (valid_mask & (1u << s))) {
       const uint32_t kb = stage0 + s * T::kStageBytes, vb = kb + T::kPageBytes;
-      const int tok0 = (first_page + w + kWarps * i) * kPage;
+      const int tok0 = (first_page + pg_off + pg_step * i) * kPage;
       // -- S^T = K . Q^T
       float sc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
       if constexpr (FMT == DA_KV_BF16) {
@@ -361,15 +366,62 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 3 : 2)
     if (!stalled && cur.more) issue_next();
   }
 
-  // ---- partition epilogue: each warp's (o, m, l) per virtual head into shared memory (hi
-  //      and lo columns added), then the warps merged into the partial (split sequence) or
-  //      the normalised output (unsplit)
+  // ---- partition epilogue
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
     l_run[j] += __shfl_xor_sync(kFull, l_run[j], 4);
     l_run[j] += __shfl_xor_sync(kFull, l_run[j], 8);
     l_run[j] += __shfl_xor_sync(kFull, l_run[j], 16);
   }
+  const bool direct = np == 1;
+  if (owner) {
+    // the warp's (o, m, l) is the partition's result: O^T (hi and lo columns added; divided
+    // by l for an unsplit sequence) through the warp's staging buffer, then 16-byte stores
+    float* ep_w = ep_o + w * NV * DP;
+#pragma unroll
+    for (int mt = 0; mt < T::kMT; ++mt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float v = o[0][mt][e];
+        if constexpr (NV == 8) v += o[T::kNT - 1][mt][e];
+        if constexpr (NV == 4) v += __shfl_xor_sync(kFull, v, 2);  // columns c, c + 4
+        if constexpr (NV == 2) v += __shfl_xor_sync(kFull, v, 1);  // columns c, c + 2
+        if constexpr (NV == 1) v += (e & 1) ? 0.0f : o[0][mt][e + 1];  // columns 0, 1
+        const int col = 2 * tig + (e & 1);
+        const float l = l_run[e & 1];
+        if (direct) v = l > 0.0f ? v * out_scale / l : 0.0f;
+        const int rowd = FMT == DA_KV_BF16 ? 16 * mt + gid + ((e >> 1) ? 8 : 0) : 16 * mt + 2 * gid + (e >> 1);
+        if (col < V) ep_w[col * DP + rowd] = v;
+      }
+    if (!direct && gid == 0) {
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int col = 2 * tig + j;
+        if (col < V) {
+          const size_t pi = (((size_t)b * a.T + col / G) * a.Hq + g * G + col % G) * a.P + p;
+          a.part_m[pi] = m_run[j];
+          a.part_l[pi] = l_run[j];
+        }
+      }
+    }
+    __syncwarp();
+    for (int idx = lane; idx < V * D / 4; idx += 32) {
+      const int v = idx / (D / 4), d = 4 * (idx % (D / 4));
+      const size_t bh = ((size_t)b * a.T + v / G) * a.Hq + g * G + v % G;
+      const float4 x = *reinterpret_cast<const float4*>(ep_w + v * DP + d);
+      if (direct) {  // the caller's output is only 4-byte aligned
+        float* dst = a.out + bh * D + d;
+        dst[0] = x.x, dst[1] = x.y, dst[2] = x.z, dst[3] = x.w;
+      } else {
+        *reinterpret_cast<float4*>(a.part_o + (bh * a.P + p) * D + d) = x;
+      }
+    }
+    __syncwarp();  // the staging buffer is rewritten by the warp's next partition
+    continue;
+  }
+  // shared partition: each warp's (o, m, l) per virtual head into shared memory (hi and lo
+  // columns added), then the warps merged into the partial (split sequence) or the
+  // normalised output (unsplit)
 #pragma unroll
   for (int mt = 0; mt < T::kMT; ++mt)
 #pragma unroll
@@ -391,7 +443,6 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 3 : 2)
     }
   }
   __syncthreads();
-  const bool direct = np == 1;
   for (int idx = tid; idx < V * D; idx += kThreads) {
     const int v = idx / D, d = idx % D;
     float M = -INFINITY;
@@ -474,6 +525,8 @@ cudaError_t launch_fixed(const Args& a, cudaStream_t s) {
     return e;
   Args b = a;
   b.ppc = partitions_per_cta(a, per_sm, sms);
+  b.owner = warps_own_partitions(a, per_sm, kWarps, sms);
+  if (b.owner) b.ppc = kWarps * ((b.ppc + kWarps - 1) / kWarps);
   kern<<<dim3((a.P + b.ppc - 1) / b.ppc, a.Hkv, a.B), kThreads, T::kSmem, s>>>(b, km, vm);
   return cudaGetLastError();
 }

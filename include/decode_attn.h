@@ -104,6 +104,14 @@ typedef struct da_params {
   int32_t window;             /* 0 = off; else attend only the last `window` tokens (t >= L - window) */
   int32_t partition_size;     /* tokens per split-K partition (512); 0 = never split */
   int32_t split_threshold;    /* split a sequence iff its attended length >= this (1024) */
+  int32_t partition_schedule; /* how a partition kernel's warps share the work (results are the same
+                                 up to rounding): 0 = chosen per call from the number of partitions,
+                                 1 = the warps of a CTA share each partition, 2 = each warp owns whole
+                                 partitions (no cross-warp merge; best when there are partitions
+                                 for every warp the GPU holds at once). Other values are rejected. */
+  int32_t partitions_per_cta; /* consecutive partitions of one (sequence, kv head) a CTA of a partition
+                                 kernel takes, 0 = chosen per call, else 1 .. 64 (rounded up to a
+                                 multiple of the CTA's warps when each warp owns partitions) */
   void* workspace;            /* device memory, 256-byte aligned, decode_attn_workspace_bytes() long,
                                  zeroed once by decode_attn_workspace_init before first use */
   size_t workspace_bytes;     /* size of `workspace` in bytes */
@@ -113,8 +121,7 @@ typedef struct da_params {
  * The workspace holds the error word, the rotated queries of the codebook formats
  * ([B][T][Hq][D] f32), the split-K partials -- output [B][T][Hq][P][D] f32 (unnormalised),
  * running max and running sum [B][T][Hq][P] f32, where P is the partition count of a
- * sequence of length max_context_len (the page's partial buffers, sized for a batch) -- and
- * one completion counter per (sequence, kv head). */
+ * sequence of length max_context_len (the page's partial buffers, sized for a batch). */
 size_t decode_attn_workspace_bytes(const da_params* p);
 
 /* Zero the workspace (in particular its error word) on `stream`. Call once after

@@ -62,6 +62,10 @@ def test_workspace_bytes_and_partitions():
     (dict(softcap=-1.0), da._binding.DA_ERR_INVALID_ARG),
     (dict(softmax_scale=float("nan")), da._binding.DA_ERR_INVALID_ARG),
     (dict(window=-5), da._binding.DA_ERR_INVALID_ARG),
+    (dict(partition_schedule=3), da._binding.DA_ERR_INVALID_ARG),
+    (dict(partition_schedule=-1), da._binding.DA_ERR_INVALID_ARG),
+    (dict(partitions_per_cta=65), da._binding.DA_ERR_INVALID_ARG),
+    (dict(partitions_per_cta=-2), da._binding.DA_ERR_INVALID_ARG),
     (dict(max_context_len=1 << 30), da._binding.DA_ERR_UNSUPPORTED),  # more partitions than built
 ])
 def test_bad_params_are_rejected(kw, status):

@@ -59,6 +59,24 @@ def test_window_and_softcap(fmt, window, softcap):
     assert_close(run_gpu(c), run_oracle(c), f"{fmt} window={window} softcap={softcap}")
 
 
+@pytest.mark.parametrize("fmt", ["bf16", "fp8", "cb4", "fp8k_cb4v", "cb3k_cb4v"])
+@pytest.mark.parametrize("schedule", [1, 2])
+@pytest.mark.parametrize("D,G,T,window", [(128, 4, 1, 0), (256, 2, 1, 700), (128, 2, 3, 0), (128, 8, 1, 0)])
+def test_partition_schedules(fmt, schedule, D, G, T, window):
+    """Both ways of dealing a CTA's partitions to its warps (shared by the warps, or each warp
+    owning whole partitions), with the automatic and with three partitions per CTA (rounded up
+    to the warps when they own partitions), unsplit and split sequences, windows, multi-token
+    queries and eight columns."""
+    lens = [0, 1, 17, 1023, 1024, 1500, 2053, 4097, 5000, 9000]
+    spec = wl.WorkloadSpec(f"sched_{fmt}", len(lens), 2 * G, 2, D, fmt, 0, max(lens), seed=31 + D + G + T,
+                           window=window, query_len=T)
+    c = make_case(spec, wl.make_layout(spec, lens=lens))
+    ref = run_oracle(c)
+    for ppc in (0, 3):
+        assert_close(run_gpu(c, partition_schedule=schedule, partitions_per_cta=ppc), ref,
+                     f"{fmt} schedule {schedule}, {ppc} partitions per CTA")
+
+
 @pytest.mark.parametrize("psize,thresh", [(0, 1024), (16, 1), (48, 64), (512, 1), (4096, 1024)])
 def test_partition_sizes(psize, thresh):
     spec, lay = small_spec("bf16", 128, 4, lens=EDGE_LENS, seed=psize + 3)
@@ -68,7 +86,7 @@ def test_partition_sizes(psize, thresh):
 
 
 @pytest.mark.parametrize("name,n", [("llama3_8b_bf16", 32), ("fp8_long_32k", 24), ("gemma_window_softcap", 24),
-                                    ("cb4_long_32k", 16)])
+                                    ("cb4_long_32k", 16), ("fp8k_cb4v_long_32k", 12), ("cb3k_cb4v_long_32k", 12)])
 def test_full_size_workloads_sampled(name, n):
     spec = wl.WORKLOADS[name]
     c = make_case(spec)

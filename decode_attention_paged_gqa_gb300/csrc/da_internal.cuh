@@ -35,6 +35,7 @@ struct Args {
   int window, psize, thresh;
   int P;                      // partitions the grid and the workspace are sized for
   int ppc;                    // partitions a partition-kernel CTA walks (set by its launcher)
+  uint32_t lut_stride;        // 128: entry stride of the codebook kernel's lookup tables (bytes)
   int schedule;               // da_params.partition_schedule (0 automatic, 1 shared, 2 owned)
   int ppc_req;                // da_params.partitions_per_cta (0 automatic)
   int owner;                  // 1: each warp of a partition kernel owns whole partitions, 0: the

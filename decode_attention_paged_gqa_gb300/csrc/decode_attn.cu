@@ -96,6 +96,7 @@ Args make_args(const void* q, const void* k, const void* v, const float* ks, con
   a.thresh = p->split_threshold;
   a.P = host_max_partitions(*p);
   a.ppc = 1;
+  a.lut_stride = 128;
   a.schedule = p->partition_schedule;
   a.ppc_req = p->partitions_per_cta;
   a.owner = 0;

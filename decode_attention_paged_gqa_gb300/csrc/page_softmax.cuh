@@ -38,30 +38,40 @@ __device__ __forceinline__ void mask_page(float (&sc)[4], int tok0, int gid, con
 // One page: updates (m, l) of the thread's two columns and returns the page's
 // probabilities pr (relative to the new reference) and the factor alpha[j] the column's
 // running output must be multiplied by. Returns true if any column of the warp moved its
-// reference (alpha != 1 somewhere).
+// reference (alpha != 1 somewhere). A column's page max is only needed when it exceeds the
+// reference by more than kLazyLog2, which a warp vote on the threads' own scores decides: the
+// usual page skips the max reduction altogether.
 __device__ __forceinline__ bool page_softmax(const float (&sc)[4], float (&m)[2], float (&l)[2], float (&alpha)[2],
                                              float (&pr)[4]) {
-  bool moved = false;
+  alpha[0] = alpha[1] = 1.0f;
+  bool moved_any = false;
+  // m = -inf (nothing seen yet): -inf + kLazyLog2 = -inf, so the first finite score counts as over
+  const bool over = fmaxf(sc[0], sc[2]) > m[0] + kLazyLog2 || fmaxf(sc[1], sc[3]) > m[1] + kLazyLog2;
+  if (__any_sync(0xffffffffu, over)) {
+    bool moved = false;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      float mx = fmaxf(sc[j], sc[j + 2]);
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+      const bool move = mx > m[j] + kLazyLog2;
+      const float mn = move ? mx : m[j];
+      alpha[j] = move ? exp2_fast(m[j] - mn) : 1.0f;  // 2^-inf = 0 clears the (zero) state
+      moved |= move;
+      m[j] = mn;
+    }
+    moved_any = __any_sync(0xffffffffu, moved);
+  }
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
-    float mx = fmaxf(sc[j], sc[j + 2]);
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-    // m = -inf (nothing seen yet) moves to the first finite max; 2^(-inf) = 0 then clears
-    // the (zero) state
-    const bool move = mx > m[j] + kLazyLog2;
-    const float mn = move ? mx : m[j];
-    alpha[j] = move ? exp2_fast(m[j] - mn) : 1.0f;
-    moved |= move;
     // with no finite score yet every score is -inf: any finite reference gives 2^-inf = 0
-    const float ref = mn == -INFINITY ? 0.0f : mn;
+    const float ref = m[j] == -INFINITY ? 0.0f : m[j];
     pr[j] = exp2_fast(sc[j] - ref);
     pr[j + 2] = exp2_fast(sc[j + 2] - ref);
     l[j] = l[j] * alpha[j] + pr[j] + pr[j + 2];
-    m[j] = mn;
   }
-  return __any_sync(0xffffffffu, moved);
+  return moved_any;
 }
 
 }  // namespace da

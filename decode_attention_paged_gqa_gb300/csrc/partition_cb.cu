@@ -132,8 +132,14 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
 }
 __device__ __forceinline__ float ldsf(uint32_t addr) { return __uint_as_float(lds32(addr)); }
 
-// Table lookup: entry e of a table whose copy for this lane starts at `lane_base`.
-__device__ __forceinline__ uint32_t lut(uint32_t lane_base, uint32_t e) { return lds32(lane_base + e * 128u); }
+// A lookup table as seen by one lane: its copy's first word, and the entry stride (128 bytes,
+// given at run time so the address is one multiply-add on the FMA pipe rather than a shift
+// and an add on the busier integer ALU pipe).
+struct LutRef {
+  uint32_t base, stride;  // shared-memory address of the lane's copy; entry stride in bytes (128)
+};
+// Entry e of the lane's copy of a table.
+__device__ __forceinline__ uint32_t lut(const LutRef& t, uint32_t e) { return lds32(t.base + e * t.stride); }
 // byte j of a little-endian word array
 template <int J>
 __device__ __forceinline__ uint32_t byte_of(const uint32_t* w) {
@@ -151,7 +157,7 @@ __device__ __forceinline__ uint32_t field6(const uint32_t* w) {
 
 // A fragments of S^T for k-step KS_ from the thread's key bytes (rows gid: k0, gid + 8: k1).
 template <int KS, int D, int S>
-__device__ __forceinline__ void key_frag(uint32_t (&af)[4], const uint32_t* k0, const uint32_t* k1, uint32_t lutk) {
+__device__ __forceinline__ void key_frag(uint32_t (&af)[4], const uint32_t* k0, const uint32_t* k1, const LutRef& lutk) {
   if constexpr (KS == kSideCB4) {
     af[0] = lut(lutk, byte_of<2 * S>(k0));
     af[1] = lut(lutk, byte_of<2 * S>(k1));
@@ -168,7 +174,7 @@ __device__ __forceinline__ void key_frag(uint32_t (&af)[4], const uint32_t* k0, 
 template <int S, int N, int KS, int D, int NV>
 struct KeySteps {
   // S^T += A(k-step S) . Q^T for S = S .. N-1 (compile-time unrolled so byte offsets are constants)
-  __device__ static __forceinline__ void run(float (&sc)[4], const uint32_t* k0, const uint32_t* k1, uint32_t lutk,
+  __device__ static __forceinline__ void run(float (&sc)[4], const uint32_t* k0, const uint32_t* k1, const LutRef& lutk,
                                              const uint32_t (*qf)[2], const uint32_t (*ql)[2]) {
     if constexpr (S < N) {
       uint32_t af[4];
@@ -185,7 +191,7 @@ struct ValueTiles {
   // O^T[m-tile M] += V^T(m-tile M) . P^T for M = M .. N-1. vx[r]: table indices, byte M of
   // word array r: r = 0 / 1: the low / high nibbles of tokens (2 tig, 2 tig + 1) paired, r =
   // 2 / 3 the same for tokens (2 tig + 8, 2 tig + 9); one lookup gives an A register.
-  __device__ static __forceinline__ void run(float (&o)[NT][D / 16][4], const uint32_t (*vx)[D / 64], uint32_t lutv,
+  __device__ static __forceinline__ void run(float (&o)[NT][D / 16][4], const uint32_t (*vx)[D / 64], const LutRef& lutv,
                                              const uint32_t (&pb)[NT][2]) {
     if constexpr (M < N) {
       const uint32_t af[4] = {lut(lutv, byte_of<M>(vx[0])), lut(lutv, byte_of<M>(vx[1])),
@@ -205,7 +211,8 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 2)
   using C = Cb<KS, D, NV>;
   constexpr int kWarps = C::kWarps, kThreads = C::kThreads, DP = C::kDP;
   const int g = blockIdx.y, b = blockIdx.z;
-  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  // the warp index through a shuffle from lane 0, which the compiler then treats as uniform
+  const int tid = threadIdx.x, lane = tid & 31, w = __shfl_sync(kFull, tid >> 5, 0);
   const int gid = lane >> 2, tig = lane & 3;
   const int G = a.Hq / a.Hkv, V = a.T * G;
   const int L = load_len(a, b, blockIdx.x == 0 && g == 0 && tid == 0);
@@ -290,8 +297,8 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 2)
       }
     }
   }
-  const uint32_t lutv = smem + lane * 4u;
-  const uint32_t lutk = KS == kSideCB3 ? lutv + C::kLutV : lutv;
+  const LutRef lutv{smem + lane * 4u, a.lut_stride};
+  const LutRef lutk{KS == kSideCB3 ? lutv.base + C::kLutV : lutv.base, a.lut_stride};
 
   // ---- query fragments (B operand of S^T). Column n scores virtual head (n % NV) % V.
   const int qv = (gid % NV) % V;
@@ -492,10 +499,10 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 2)
       bool rescale = page_softmax(sc, m_run, l_run, alpha, pr);
       const float vn0 = ldsf(kb + C::kOffVN + 4 * gid), vn1 = ldsf(kb + C::kOffVN + 4 * (gid + 8));
       int ev = (int)(__float_as_uint(fmaxf(fabsf(vn0), fabsf(vn1))) >> 23);
-      ev = max(ev, __shfl_xor_sync(kFull, ev, 4));
-      ev = max(ev, __shfl_xor_sync(kFull, ev, 8));
-      ev = max(ev, __shfl_xor_sync(kFull, ev, 16));
-      if (ev > ev_run) {  // warp-uniform
+      if (__any_sync(kFull, ev > ev_run)) {  // a larger exponent on this page: the warp's max
+        ev = max(ev, __shfl_xor_sync(kFull, ev, 4));
+        ev = max(ev, __shfl_xor_sync(kFull, ev, 8));
+        ev = max(ev, __shfl_xor_sync(kFull, ev, 16));
         const float f = ldexpf(1.0f, ev_run - ev);
         alpha[0] *= f;
         alpha[1] *= f;

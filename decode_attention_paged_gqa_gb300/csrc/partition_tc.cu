@@ -109,7 +109,8 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 3 : 2)
   using T = Tc<FMT, D, NV>;
   constexpr int DP = T::kDP;
   const int g = blockIdx.y, b = blockIdx.z;
-  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  // the warp index through a shuffle from lane 0, which the compiler then treats as uniform
+  const int tid = threadIdx.x, lane = tid & 31, w = __shfl_sync(kFull, tid >> 5, 0);
   const int gid = lane >> 2, tig = lane & 3;
   const int G = a.Hq / a.Hkv, V = a.T * G;  // group size; virtual heads in use (<= NV)
   const int L = load_len(a, b, blockIdx.x == 0 && g == 0 && tid == 0);

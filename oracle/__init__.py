@@ -100,8 +100,8 @@ def _open(path: str):
         "or_partition_bounds": (I, [I, I, I, I, P, P, I]),
         "or_partition_bounds_multi": (I, [I, I, I, I, I, P, P, I]),
         "or_default_threads": (I, []),
-        "or_decode_attention": (I, [I, I, I, I, I, I, I, I, I, P, P, P, P, P, P, P, P, P, D, D, I, I, I, P, P, I,
-                                    ctypes.POINTER(ctypes.c_int)]),
+        "or_decode_attention": (I, [I, I, I, I, I, I, I, I, I, P, P, P, P, P, P, P, P, P, D, D, P, I, I, I, P, P,
+                                    I, ctypes.POINTER(ctypes.c_int)]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -263,13 +263,15 @@ def partition_bounds(L: int, window: int = 0, partition_size: int = 512, split_t
 def decode_attention(q_bits, k_cache, v_cache, block_tables, context_lens, *, kv_format: str, num_kv_heads: int,
                      softmax_scale: float, softcap: float = 0.0, window: int = 0, partition_size: int = 0,
                      split_threshold: int = 1024, k_scales=None, v_scales=None, codebook=None, sign_pattern=None,
-                     select=None, threads: int = 0, return_threads: bool = False):
+                     alibi_slopes=None, select=None, threads: int = 0, return_threads: bool = False):
     """fp64 paged GQA decode attention.
 
     q_bits: uint16 bf16 bit patterns [B, Hq, D], or [B, T, Hq, D] for T query tokens per
     sequence (positions L-T .. L-1, causal). Caches: [num_blocks, Hkv, bs, D] uint16
     (bf16 bits) or uint8 (E4M3 codes), or [num_blocks, Hkv, bs, D/2] uint8 (packed 4-bit).
     k_scales/v_scales: fp8 -> one value each; cb4 -> [num_blocks, Hkv, bs] fp32.
+    alibi_slopes: optional [Hq] slopes; the score of key position t for a query at position
+    pos gets slope_h * (t - pos) added after scaling and softcap.
     select: optional list of (b, h) (or (b, j, h) with T query tokens); then the result is
     [len(select), D] in that order, else [B, Hq, D] (or [B, T, Hq, D]). partition_size 0
     computes without partitions.
@@ -303,12 +305,17 @@ def decode_attention(q_bits, k_cache, v_cache, block_tables, context_lens, *, kv
                 raise ValueError("duplicate entry in select")
             rows[r] = i
         out = np.zeros((len(select), D), dtype=np.float64)
+    slopes = None
+    if alibi_slopes is not None:
+        slopes = _c(alibi_slopes, np.float32)
+        if slopes.shape != (Hq,):
+            raise ValueError("alibi_slopes must hold one slope per query head")
     used = ctypes.c_int(0)
     rc = _load().or_decode_attention(
         B, T, Hq, num_kv_heads, D, bs, kf, num_blocks, bt.shape[1], _ptr(q), _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs),
         _ptr(_c(codebook, np.float32)), _ptr(_c(sign_pattern, np.float32)), _ptr(bt), _ptr(cl),
-        float(softmax_scale), float(softcap), int(window), int(partition_size), int(split_threshold), _ptr(rows),
-        _ptr(out), int(threads), ctypes.byref(used))
+        float(softmax_scale), float(softcap), _ptr(slopes), int(window), int(partition_size), int(split_threshold),
+        _ptr(rows), _ptr(out), int(threads), ctypes.byref(used))
     if rc:
         raise ValueError(f"oracle: {ERRORS.get(rc, rc)}")
     if select is None and not multi:

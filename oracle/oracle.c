@@ -482,6 +482,7 @@ typedef struct {
   const int32_t* block_tables; /* [B][max_blocks] */
   const int32_t* context_lens; /* [B] */
   double scale, softcap;
+  const float* alibi;     /* [Hq] ALiBi slopes, or NULL */
   int window, partition_size, split_threshold;
   const int32_t* out_row; /* [B*T*Hq]: output row of (b, j, h), or -1 when not requested */
   double* out;            /* [rows][D] */
@@ -581,12 +582,16 @@ static void or_attn_task(void* ctx, int64_t u) {
       for (d = 0; d < D; ++d) out[d] = 0.0; /* nothing attended: zero output */
       if (pos < 0 || n == 0) continue;
       for (d = 0; d < D; ++d) qh[d] = or_bf16_decode(j->q[qi * D + d]);
-      /* (2) scores s_t = scale * q . k_t, then the optional softcap cap * tanh(s / cap) */
+      /* (2) scores s_t = scale * q . k_t, then the optional softcap cap * tanh(s / cap), then
+       * the optional ALiBi bias slope_h * (t - pos): zero at the query's own position and
+       * falling linearly with the distance (reading: the bias of the ALiBi method, added to
+       * the finished score; the slopes are inputs) */
       for (t = a; t < e; ++t) {
         double acc = 0.0;
         for (d = 0; d < D; ++d) acc += qh[d] * K[(int64_t)(t - s0) * D + d];
         s[t - s0] = j->scale * acc;
         if (j->softcap > 0.0) s[t - s0] = j->softcap * tanh(s[t - s0] / j->softcap);
+        if (j->alibi) s[t - s0] += (double)j->alibi[h] * (double)(t - pos);
       }
       /* (3) out = softmax(s) V over [a, e), in one piece or through per-partition partials */
       {
@@ -641,8 +646,8 @@ int or_decode_attention(int B, int T, int Hq, int Hkv, int D, int block_size, in
                         int max_blocks, const uint16_t* q, const void* k_cache, const void* v_cache,
                         const float* k_scales, const float* v_scales, const float* codebook, const float* sign,
                         const int32_t* block_tables, const int32_t* context_lens, double scale, double softcap,
-                        int window, int partition_size, int split_threshold, const int32_t* out_row, double* out,
-                        int threads, int* threads_used) {
+                        const float* alibi_slopes, int window, int partition_size, int split_threshold,
+                        const int32_t* out_row, double* out, int threads, int* threads_used) {
   or_attn_job j;
   int32_t* rows = NULL;
   double* H = NULL;
@@ -702,6 +707,7 @@ int or_decode_attention(int B, int T, int Hq, int Hkv, int D, int block_size, in
   j.context_lens = context_lens;
   j.scale = scale;
   j.softcap = softcap;
+  j.alibi = alibi_slopes;
   j.window = window;
   j.partition_size = partition_size;
   j.split_threshold = split_threshold;

@@ -8,6 +8,7 @@ import pytest
 import oracle
 import test_oracle_attention as A
 import test_oracle_encoders as E
+import test_oracle_alibi as AL
 import test_oracle_multitoken as M
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
@@ -44,6 +45,10 @@ MUTATIONS = [
     ("lloyd-max threshold not the midpoint", "for (i = 1; i < L; ++i) t[i] = 0.5 * (c[i - 1] + c[i]);",
      "for (i = 1; i < L; ++i) t[i] = c[i];"),
     ("bf16 decoded from the wrong half", "uint32_t w = (uint32_t)bits << 16;", "uint32_t w = (uint32_t)bits << 15;"),
+    ("alibi bias with the wrong sign", "s[t - s0] += (double)j->alibi[h] * (double)(t - pos);",
+     "s[t - s0] += (double)j->alibi[h] * (double)(pos - t);"),
+    ("alibi slope of the kv head", "s[t - s0] += (double)j->alibi[h] * (double)(t - pos);",
+     "s[t - s0] += (double)j->alibi[g] * (double)(t - pos);"),
 ]
 
 PINS = [
@@ -59,6 +64,7 @@ PINS = [
     (A.test_partition_bounds_follow_pages, None),
     (M.test_multitoken_matches_sdpa_with_mask, dict(T=4, window=0)),
     (M.test_multitoken_matches_sdpa_with_mask, dict(T=3, window=20)),
+    (AL.test_alibi_matches_sdpa_with_bias, dict(T=3, window=0, softcap=0.0)),
     (E.test_e4m3_decode_fixed_points, {}),
     (E.test_e4m3_decode_matches_torch, {}),
     (E.test_e4m3_encode_matches_torch_cast, {}),

@@ -48,6 +48,7 @@ class da_params(ctypes.Structure):
         ("split_threshold", ctypes.c_int32),
         ("partition_schedule", ctypes.c_int32),
         ("partitions_per_cta", ctypes.c_int32),
+        ("alibi_slopes", ctypes.c_void_p),
         ("workspace", ctypes.c_void_p),
         ("workspace_bytes", ctypes.c_size_t),
     ]
@@ -56,7 +57,7 @@ class da_params(ctypes.Structure):
 def make_params(*, batch, num_q_heads, num_kv_heads, head_dim, num_blocks, max_blocks_per_seq, max_context_len,
                 kv_format, softmax_scale, softcap=0.0, window=0, partition_size=512, split_threshold=1024,
                 block_size=16, query_len=1, partition_schedule=0, partitions_per_cta=0,
-                workspace=None) -> da_params:
+                alibi_slopes=None, workspace=None) -> da_params:
     p = da_params()
     p.batch, p.num_q_heads, p.num_kv_heads, p.head_dim = batch, num_q_heads, num_kv_heads, head_dim
     p.query_len = int(query_len)
@@ -66,6 +67,7 @@ def make_params(*, batch, num_q_heads, num_kv_heads, head_dim, num_blocks, max_b
     p.softmax_scale, p.softcap, p.window = float(softmax_scale), float(softcap), int(window)
     p.partition_size, p.split_threshold = int(partition_size), int(split_threshold)
     p.partition_schedule, p.partitions_per_cta = int(partition_schedule), int(partitions_per_cta)
+    p.alibi_slopes = _ptr(alibi_slopes)  # a device tensor of Hq float32 slopes, or None
     if workspace is not None:
         attach_workspace(p, workspace)
     return p

@@ -27,6 +27,7 @@ struct Args {
   const float* v_scales;
   const float* codebook;      // cb4: [16]
   const float* sign;          // cb4: [D]
+  const float* alibi;         // [Hq] ALiBi slopes, or null
   const int32_t* block_tables;  // [B][max_blocks]
   const int32_t* context_lens;  // [B]
   float* out;                 // [B][T][Hq][D]

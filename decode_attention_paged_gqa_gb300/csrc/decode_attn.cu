@@ -60,6 +60,7 @@ int check_tensors(const void* q, const void* k, const void* v, const float* ks, 
   if (!aligned(k, 16) || !aligned(v, 16) || !aligned(q, 16) || !aligned(out, 4) || !aligned(bt, 4) ||
       !aligned(lens, 4))
     return DA_ERR_INVALID_ARG;
+  if (p->alibi_slopes && !aligned(p->alibi_slopes, 4)) return DA_ERR_INVALID_ARG;
   // per-token norms of a codebook side are copied 16 tokens (64 bytes) at a time
   if ((is_codebook(k_side(p->kv_format)) && !aligned(ks, 16)) || (is_codebook(v_side(p->kv_format)) && !aligned(vs, 16)))
     return DA_ERR_INVALID_ARG;
@@ -97,6 +98,7 @@ Args make_args(const void* q, const void* k, const void* v, const float* ks, con
   a.P = host_max_partitions(*p);
   a.ppc = 1;
   a.lut_stride = 128;
+  a.alibi = p->alibi_slopes;
   a.schedule = p->partition_schedule;
   a.ppc_req = p->partitions_per_cta;
   a.owner = 0;

@@ -377,6 +377,13 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 2)
     pos_c[j] = L - a.T + (((2 * tig + j) % NV) % V) / G;
     lo_w[j] = window_start(pos_c[j], a.window);
   }
+  // ALiBi: the slope of each column's query head, in the log2 domain of the scores
+  const bool alibi = a.alibi != nullptr;
+  float slope_c[2] = {0.0f, 0.0f};
+  if (alibi) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) slope_c[j] = __ldg(a.alibi + g * G + (((2 * tig + j) % NV) % V) % G) * kLog2e;
+  }
   float* ep_o = reinterpret_cast<float*>(smem_gen + C::kOffMerge);  // [kWarps][NV][DP]
   float* ep_m = ep_o + kWarps * NV * DP;                             // [kWarps][8]
   float* ep_l = ep_m + kWarps * 8;                                   // [kWarps][8]
@@ -491,6 +498,11 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 2)
       for (int e = 0; e < 4; ++e) {
         const float y = sc[e] * ((e >> 1) ? ss1 : ss0);
         sc[e] = CAP ? cap_post * tanhf(y * cap_pre) : y;
+      }
+      if (alibi) {  // + slope * (t - pos) for token t of each element
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          sc[e] += slope_c[e & 1] * (float)(tok0 + gid + (e >> 1) * 8 - pos_c[e & 1]);
       }
       if (tok0 < lo_all || tok0 + kPage > hi_all) mask_page(sc, tok0, gid, lo_c, hi_c);
       // -- online softmax per column (lazily moved reference max); a larger value-norm

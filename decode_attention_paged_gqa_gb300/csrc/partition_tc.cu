@@ -217,6 +217,13 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 3 : 2)
     pos_c[j] = L - a.T + (((2 * tig + j) % NV) % V) / G;
     lo_w[j] = window_start(pos_c[j], a.window);
   }
+  // ALiBi: the slope of each column's query head, in the log2 domain of the scores
+  const bool alibi = a.alibi != nullptr;
+  float slope_c[2] = {0.0f, 0.0f};
+  if (alibi) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) slope_c[j] = __ldg(a.alibi + g * G + (((2 * tig + j) % NV) % V) % G) * kLog2e;
+  }
   float* ep_o = reinterpret_cast<float*>(smem_gen + T::kStageSmem);  // [kWarps][NV][DP]
   float* ep_m = ep_o + kWarps * NV * DP;                              // [kWarps][8]
   float* ep_l = ep_m + kWarps * 8;                                    // [kWarps][8]
@@ -295,6 +302,11 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 3 : 2)
       // -- scale (log2 domain), softcap, mask; sc[0], sc[1]: token gid; sc[2], sc[3]: token gid + 8
 #pragma unroll
       for (int e = 0; e < 4; ++e) sc[e] = CAP ? cap_post * tanhf(sc[e] * cap_pre) : sc[e] * score_scale;
+      if (alibi) {  // + slope * (t - pos) for token t of each element
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          sc[e] += slope_c[e & 1] * (float)(tok0 + gid + (e >> 1) * 8 - pos_c[e & 1]);
+      }
       if (tok0 < lo_all || tok0 + kPage > hi_all) mask_page(sc, tok0, gid, lo_c, hi_c);
       // -- online softmax per column (lazily moved reference max)
       float alpha[2], pr[4];

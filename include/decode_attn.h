@@ -112,6 +112,10 @@ typedef struct da_params {
   int32_t partitions_per_cta; /* consecutive partitions of one (sequence, kv head) a CTA of a partition
                                  kernel takes, 0 = chosen per call, else 1 .. 64 (rounded up to a
                                  multiple of the CTA's warps when each warp owns partitions) */
+  const float* alibi_slopes;  /* NULL = off; else DEVICE pointer to [Hq] f32 ALiBi slopes: the score of
+                                 key position t for a query at position pos gets slope_h * (t - pos)
+                                 added after scaling and softcap (attention.rs README, feature list:
+                                 ALiBi slopes). 4-byte aligned. */
   void* workspace;            /* device memory, 256-byte aligned, decode_attn_workspace_bytes() long,
                                  zeroed once by decode_attn_workspace_init before first use */
   size_t workspace_bytes;     /* size of `workspace` in bytes */

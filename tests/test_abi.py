@@ -113,6 +113,10 @@ def test_null_and_misaligned_tensors_are_rejected():
     with pytest.raises(da.DecodeAttnError) as e:  # cb4 needs codebook and signs
         da.decode_attn_paged(256, 256, 256, 256, 256, None, None, 256, 256, 256, cb4, stream=0)
     assert e.value.status == da._binding.DA_ERR_INVALID_ARG
+    p.alibi_slopes = 258  # ALiBi slopes not 4-byte aligned
+    with pytest.raises(da.DecodeAttnError) as e:
+        da.decode_attn_paged(256, 256, 256, None, None, None, None, 256, 256, 256, p, stream=0)
+    assert e.value.status == da._binding.DA_ERR_INVALID_ARG
 
 
 def test_empty_batch_enqueues_nothing():

@@ -77,6 +77,22 @@ def test_partition_schedules(fmt, schedule, D, G, T, window):
                      f"{fmt} schedule {schedule}, {ppc} partitions per CTA")
 
 
+@pytest.mark.parametrize("fmt", ["bf16", "fp8", "cb4", "fp8k_cb4v", "cb3k_cb4v"])
+@pytest.mark.parametrize("T,window,softcap,schedule", [(1, 0, 0.0, 0), (1, 700, 30.0, 2), (2, 0, 0.0, 1),
+                                                       (3, 0, 0.0, 2)])
+def test_alibi(fmt, T, window, softcap, schedule):
+    """ALiBi slopes (one per query head, the usual geometric choice), with one and several
+    query tokens, a window and softcap, under both partition schedules."""
+    lens = [1, 17, 600, 1030, 2500, 4100]
+    G = 2
+    spec = wl.WorkloadSpec(f"alibi_{fmt}", len(lens), 4 * G, 4, 128, fmt, 0, max(lens), seed=50 + T + window,
+                           window=window, softcap=softcap, query_len=T)
+    c = make_case(spec, wl.make_layout(spec, lens=lens))
+    slopes = np.array([2.0 ** (-8.0 * (h + 1) / 8) for h in range(8)], np.float32)
+    gpu = run_gpu(c, alibi_slopes=torch.from_numpy(slopes).cuda(), partition_schedule=schedule)
+    assert_close(gpu, run_oracle(c, alibi_slopes=slopes), f"{fmt} alibi T{T} W{window} cap{softcap}")
+
+
 @pytest.mark.parametrize("psize,thresh", [(0, 1024), (16, 1), (48, 64), (512, 1), (4096, 1024)])
 def test_partition_sizes(psize, thresh):
     spec, lay = small_spec("bf16", 128, 4, lens=EDGE_LENS, seed=psize + 3)

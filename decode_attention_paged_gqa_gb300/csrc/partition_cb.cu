@@ -3,12 +3,13 @@
 // 4-bit V, 3-bit K + 4-bit V. Tensor-core MMAs on operands dequantised through a shared-
 // memory lookup table.
 //
-// A CTA of four or eight warps takes consecutive partitions of one (sequence, kv head); each
-// warp owns whole partitions (p_begin + w, p_begin + w + W, ...), so it writes its partition's
-// partial itself and no warp ever waits for another after the tables are built. Each warp
-// runs its own pipeline of shared-memory stages filled by TMA / bulk copies (a page's K
-// codes, V codes and their per-token norms) and signalled on an mbarrier, continuing across
-// its partitions. Per page a warp computes, in the rotated basis (the keys' and values' own
+// A CTA of four or eight warps takes consecutive partitions of one (sequence, kv head). With
+// the owned schedule (chosen when there are partitions enough) each warp owns whole
+// partitions (p_begin + w, p_begin + w + W, ...), so it writes its partition's partial itself
+// and no warp waits for another after the tables are built; with the shared schedule the
+// warps deal each partition's pages round-robin and merge at its end. Each warp runs its own
+// pipeline of shared-memory stages filled by TMA / bulk copies (a page's K codes, V codes and
+// their per-token norms) and signalled on an mbarrier, continuing across its partitions. Per page a warp computes, in the rotated basis (the keys' and values' own
 // basis, no dequantisation to the original one):
 //   S^T[16 tokens x 8 cols] = K_rot[16 x D] . Q_rot^T     then  s_t *= ||k_t||
 //   O^T[D x 8 cols]        += V_rot^T[D x 16] . (P ||v||)^T

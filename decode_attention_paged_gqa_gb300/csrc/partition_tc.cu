@@ -1,24 +1,26 @@
 // partition_tc.cu -- split-K partition kernel for the BF16 and FP8 E4M3 caches:
 // TMA page staging + warp-level tensor-core MMA for the GQA group's tiles.
 //
-// One CTA per (partition p, kv head g, sequence b), four warps. The partition's pages are
-// dealt round-robin to the warps; every warp runs its own pipeline of kStages shared-memory
-// stages, each holding one page (16 tokens) of K and of V for kv head g, loaded by TMA
-// (cp.async.bulk.tensor, 128-byte swizzle) and signalled on an mbarrier. Per page a warp
-// computes, on the tensor cores (mma.m16n8k16, fp32 accumulators):
+// A CTA of four warps takes `ppc` consecutive partitions of one (sequence, kv head). Either
+// the warps share each partition (pages dealt round-robin, the warps' results merged at the
+// partition's end) or each warp owns whole partitions; the launcher chooses per call. Every
+// warp runs its own pipeline of kStages shared-memory stages, each holding one page (16
+// tokens) of K and of V for the kv head, loaded by TMA (cp.async.bulk.tensor, 128-byte
+// swizzle) and signalled on an mbarrier, continuing across partition boundaries. Per page a
+// warp computes, on the tensor cores (mma.m16n8k16, fp32 accumulators):
 //   S^T[16 tokens x 8 cols] = K[16 x D] . Q^T[D x 8]      (the group's query heads as columns)
 //   O^T[D x 8 cols]       += V^T[D x 16]  . P^T[16 x 8]
 // Tokens are the MMA's M dimension, so a group of G = 4 heads uses 4 of the 8 columns for
 // its scores; the other 4 repeat the same heads and carry the low half of a hi/lo split of
 // the probabilities (p = hi + lo, both in the MMA's 16-bit type), which keeps P.V accurate
 // to ~2^-17 relative. The thread that owns a score column also owns that column of O^T, so
-// the online-softmax rescale needs no data exchange. At the end the four warps' (m, l, o)
-// are merged through shared memory and the partition's partial is written (or, for an
-// unsplit sequence, the normalised output directly).
+// the online-softmax rescale needs no data exchange. At a partition's end its partial is
+// written (or, for an unsplit sequence, the normalised output directly).
 //
 // Multi-token decode (T query tokens per sequence at positions L-T .. L-1): the columns are
 // the group's (query token, head) pairs, each masked at its own token's causal (and window)
-// limit; T * G <= 8.
+// limit; T * G <= 8. ALiBi slopes, when given, add slope_h * (t - pos) to each column's
+// scores.
 //
 // (attention.rs README: split-K decode kernels per KV format and m16n8k16 tensor-core MMA
 // with async copies on SM100-class GPUs; turboquant-rs 0.4.1, src/cache/cuda/attention.rs:

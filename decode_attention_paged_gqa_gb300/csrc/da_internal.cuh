@@ -38,6 +38,10 @@ struct Args {
   int ppc;                    // partitions a partition-kernel CTA walks (set by its launcher)
   uint32_t lut_stride;        // 128: entry stride of the codebook kernel's lookup tables (bytes)
   int schedule;               // da_params.partition_schedule (0 automatic, 1 shared, 2 owned)
+  // Paired copies (set by a partition kernel's launcher): one 3-D tensor map spans both the K
+  // and the V cache (or both per-token norm arrays), the third coordinate choosing the side,
+  // so one copy fetches a page of both; *_zk is the side index of K (0 when K lies lower).
+  int kv_pair, kv_zk, kn_pair, kn_zk;
   int ppc_req;                // da_params.partitions_per_cta (0 automatic)
   int owner;                  // 1: each warp of a partition kernel owns whole partitions, 0: the
                               // warps of a CTA share each partition (set by its launcher)

@@ -100,6 +100,7 @@ Args make_args(const void* q, const void* k, const void* v, const float* ks, con
   a.lut_stride = 128;
   a.alibi = p->alibi_slopes;
   a.schedule = p->partition_schedule;
+  a.kv_pair = a.kv_zk = a.kn_pair = a.kn_zk = 0;
   a.ppc_req = p->partitions_per_cta;
   a.owner = 0;
   const Layout l = workspace_layout(*p);

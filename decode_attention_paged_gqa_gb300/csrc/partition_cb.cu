@@ -73,13 +73,12 @@ struct Cb {
   static constexpr int kKBytes = kPage * kKRow;
   static constexpr int kVBytes = kPage * kVRow;
   static constexpr bool kKNorms = KS != kSideFP8;  // per-token key norms
-  // keys by TMA: FP8 in 128-byte swizzled slabs (read with ldmatrix), 4-bit D = 256 with the
-  // 128-byte swizzle; 4-bit D = 128 and 3-bit keys by a plain bulk copy (rows read unswizzled)
-  static constexpr bool kKTma = KS == kSideFP8 || (KS == kSideCB4 && D == 256);
-  static constexpr int kKAlign = kKTma ? 1024 : 128;
   // values by TMA: 64-byte rows with the 64-byte swizzle (D = 128), 128-byte rows with the
-  // 128-byte swizzle (D = 256)
+  // 128-byte swizzle (D = 256). Keys by TMA: FP8 in 128-byte swizzled slabs (read with
+  // ldmatrix), 4-bit with the values' swizzle (one copy can then fetch both, the values right
+  // behind the keys); 3-bit keys by a plain bulk copy (rows read unswizzled)
   static constexpr int kVAlign = D == 256 ? 1024 : 512;
+  static constexpr int kKAlign = KS == kSideFP8 ? 1024 : KS == kSideCB4 ? kVAlign : 128;
   static constexpr int kOffV = align_up(kKBytes, kVAlign);
   static constexpr int kOffKN = kOffV + kVBytes;
   static constexpr int kOffVN = kOffKN + (kKNorms ? 64 : 0);
@@ -208,7 +207,7 @@ struct ValueTiles {
 template <int KS, int D, int NV, bool CAP>
 __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 2)
     partition_cb_kernel(const Args a, const __grid_constant__ CUtensorMap kmap,
-                        const __grid_constant__ CUtensorMap vmap) {
+                        const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap nmap) {
   using C = Cb<KS, D, NV>;
   constexpr int kWarps = C::kWarps, kThreads = C::kThreads, DP = C::kDP;
   const int g = blockIdx.y, b = blockIdx.z;
@@ -230,13 +229,20 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 2)
   const uint32_t stage0 = smem + C::kOffStages + w * C::kStages * C::kStageBytes;
 
   if (lane == 0) {
-    if constexpr (C::kKTma) ptx::prefetch_tensor_map(&kmap);
-    ptx::prefetch_tensor_map(&vmap);
+    ptx::prefetch_tensor_map(&kmap);
+    if (!a.kv_pair) ptx::prefetch_tensor_map(&vmap);
+    if (a.kn_pair) ptx::prefetch_tensor_map(&nmap);
     for (int s = 0; s < C::kStages; ++s) ptx::mbar_init(bar0 + 8 * s, 1);
     ptx::fence_mbar_init();
   }
   __syncwarp();
 
+  // offsets within a stage of the 4-bit K and V codes and of the two norm vectors (the side with
+  // the lower address first when one map spans both)
+  const uint32_t koff = (KS == kSideCB4 && a.kv_zk) ? C::kOffV : 0;
+  const uint32_t voff = KS == kSideCB4 ? C::kOffV - koff : C::kOffV;
+  const uint32_t knoff = a.kn_zk ? 64 : 0;
+  const uint32_t vnoff = C::kKNorms ? 64 - knoff : 0;
   // ---- the warp's partitions and pages, copied kStages ahead of the compute: with
   //      a.owner, partitions p_begin + w, p_begin + w + kWarps, ... and all their pages; else
   //      every partition of the CTA and pages w, w + kWarps, ... of each
@@ -263,17 +269,32 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 2)
         ptx::mbar_arrive_expect_tx(bar, C::kTxBytes);
         const size_t unit = (size_t)phys * a.Hkv + g;  // (block, kv head): 16 consecutive rows
         const int y = (int)unit * kPage;
-        if constexpr (KS == kSideFP8) {
-#pragma unroll
-          for (int u = 0; u < D / 128; ++u) ptx::tma_load_2d(dst + u * 2048, &kmap, u * 128, y, bar);
-        } else if constexpr (C::kKTma) {
-          ptx::tma_load_2d(dst, &kmap, 0, y, bar);
+        if constexpr (KS == kSideCB4) {  // codes of K and V: one copy when one map spans both
+          if (a.kv_pair) {
+            ptx::tma_load_3d(dst, &kmap, 0, y, 0, bar);
+          } else {
+            ptx::tma_load_2d(dst + koff, &kmap, 0, y, bar);
+            ptx::tma_load_2d(dst + voff, &vmap, 0, y, bar);
+          }
         } else {
-          ptx::bulk_load(dst, static_cast<const uint8_t*>(a.k_cache) + unit * C::kKBytes, C::kKBytes, bar);
+          if constexpr (KS == kSideFP8) {
+#pragma unroll
+            for (int u = 0; u < D / 128; ++u) ptx::tma_load_2d(dst + u * 2048, &kmap, u * 128, y, bar);
+          } else {
+            ptx::bulk_load(dst, static_cast<const uint8_t*>(a.k_cache) + unit * C::kKBytes, C::kKBytes, bar);
+          }
+          ptx::tma_load_2d(dst + C::kOffV, &vmap, 0, y, bar);
         }
-        ptx::tma_load_2d(dst + C::kOffV, &vmap, 0, y, bar);
-        if constexpr (C::kKNorms) ptx::bulk_load(dst + C::kOffKN, a.k_scales + unit * kPage, 64, bar);
-        ptx::bulk_load(dst + C::kOffVN, a.v_scales + unit * kPage, 64, bar);
+        if constexpr (C::kKNorms) {  // per-token norms of K and V: one copy when one map spans both
+          if (a.kn_pair) {
+            ptx::tma_load_3d(dst + C::kOffKN, &nmap, 0, (int)unit, 0, bar);
+          } else {
+            ptx::bulk_load(dst + C::kOffKN + knoff, a.k_scales + unit * kPage, 64, bar);
+            ptx::bulk_load(dst + C::kOffKN + vnoff, a.v_scales + unit * kPage, 64, bar);
+          }
+        } else {
+          ptx::bulk_load(dst + C::kOffVN, a.v_scales + unit * kPage, 64, bar);
+        }
       }
     }
   };
@@ -440,7 +461,7 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 2)
       cphase ^= 1u;
     }
     if (!stalled && (valid_mask & (1u << s))) {
-      const uint32_t kb = stage0 + s * C::kStageBytes, vb = kb + C::kOffV;
+      const uint32_t sb = stage0 + s * C::kStageBytes, kb = sb + koff, vb = sb + voff;
       const int tok0 = (first_page + pg_off + pg_step * i) * kPage;
       // -- S^T = K . Q^T
       float sc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
@@ -463,7 +484,9 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 2)
         uint32_t k0[kWords + 1], k1[kWords + 1];
         k0[kWords] = k1[kWords] = 0u;
         if constexpr (KS == kSideCB4 && D == 128) {
-          const uint4 x0 = lds128(kb + gid * 64 + 16 * tig), x1 = lds128(kb + (gid + 8) * 64 + 16 * tig);
+          // 64-byte rows, 64-byte swizzle: 16-byte chunk c of row r at c ^ ((r >> 1) & 3)
+          const uint32_t ch = (tig ^ ((gid >> 1) & 3)) << 4;  // the same for rows gid and gid + 8
+          const uint4 x0 = lds128(kb + gid * 64 + ch), x1 = lds128(kb + (gid + 8) * 64 + ch);
           k0[0] = x0.x, k0[1] = x0.y, k0[2] = x0.z, k0[3] = x0.w;
           k1[0] = x1.x, k1[1] = x1.y, k1[2] = x1.z, k1[3] = x1.w;
         } else if constexpr (KS == kSideCB4) {  // D = 256, 128-byte swizzle: chunks 2 tig, 2 tig + 1
@@ -491,8 +514,8 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 2)
       // -- scale (and key norms), softcap, mask; sc[0], sc[1]: token gid; sc[2], sc[3]: gid + 8
       float kn0 = 1.0f, kn1 = 1.0f;
       if constexpr (C::kKNorms) {
-        kn0 = ldsf(kb + C::kOffKN + 4 * gid);
-        kn1 = ldsf(kb + C::kOffKN + 4 * (gid + 8));
+        kn0 = ldsf(sb + C::kOffKN + knoff + 4 * gid);
+        kn1 = ldsf(sb + C::kOffKN + knoff + 4 * (gid + 8));
       }
       const float ss0 = score_scale * kn0, ss1 = score_scale * kn1;
 #pragma unroll
@@ -510,7 +533,8 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 2)
       //    exponent on this page rescales O^T by the same exact power of two
       float alpha[2], pr[4];
       bool rescale = page_softmax(sc, m_run, l_run, alpha, pr);
-      const float vn0 = ldsf(kb + C::kOffVN + 4 * gid), vn1 = ldsf(kb + C::kOffVN + 4 * (gid + 8));
+      const uint32_t vnb = sb + C::kOffKN + vnoff;  // = kOffVN with separate norm copies
+      const float vn0 = ldsf(vnb + 4 * gid), vn1 = ldsf(vnb + 4 * (gid + 8));
       int ev = (int)(__float_as_uint(fmaxf(fabsf(vn0), fabsf(vn1))) >> 23);
       if (__any_sync(kFull, ev > ev_run)) {  // a larger exponent on this page: the warp's max
         ev = max(ev, __shfl_xor_sync(kFull, ev, 4));
@@ -707,16 +731,49 @@ bool encode_map(CUtensorMap* map, const void* base, int row, int box, CUtensorMa
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// One 3-D view of two equally shaped arrays (a K and a V side): (row element, row, side), the
+// side stride being the distance between them, so one box fetches the same rows of both. The
+// side with the lower address is side 0; *zk receives the side of the first array. Fails (the
+// caller then uses one copy per side) when the arrays coincide or the distance is not a
+// usable stride.
+bool encode_pair(CUtensorMap* map, const void* k, const void* v, CUtensorMapDataType type, int elem_bytes, int row,
+                 int box_rows, CUtensorMapSwizzle swz, long long rows, int* zk) {
+  auto fn = encode_fn();
+  if (!fn || k == v) return false;
+  const uintptr_t ka = reinterpret_cast<uintptr_t>(k), va = reinterpret_cast<uintptr_t>(v);
+  const uintptr_t lo = ka < va ? ka : va, diff = ka < va ? va - ka : ka - va;
+  if (diff % 16 || diff >= (uintptr_t(1) << 40)) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)row, (cuuint64_t)rows, 2};
+  const cuuint64_t strides[2] = {(cuuint64_t)row * elem_bytes, (cuuint64_t)diff};
+  const cuuint32_t boxd[3] = {(cuuint32_t)row, (cuuint32_t)box_rows, 2};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  *zk = ka > va;
+  return fn(map, type, 3, reinterpret_cast<void*>(lo), dims, strides, boxd, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int KS, int D, int NV, bool CAP>
 cudaError_t launch_fixed(const Args& a, cudaStream_t s) {
   using C = Cb<KS, D, NV>;
-  CUtensorMap km{}, vm{};
+  CUtensorMap km{}, vm{}, nm{};
   const long long rows = (long long)a.num_blocks * a.Hkv * kPage;
-  if (C::kKTma && !encode_map(&km, a.k_cache, C::kKRow, 128, CU_TENSOR_MAP_SWIZZLE_128B, rows))
-    return cudaErrorInvalidValue;
-  if (!encode_map(&vm, a.v_cache, C::kVRow, C::kVRow,
-                  D == 128 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B, rows))
-    return cudaErrorInvalidValue;
+  const CUtensorMapSwizzle vswz = D == 128 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
+  Args b = a;
+  int zk = 0;
+  // 4-bit keys and values have the same rows: one copy per page for both where possible
+  b.kv_pair = KS == kSideCB4 &&
+              encode_pair(&km, a.k_cache, a.v_cache, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, C::kVRow, kPage, vswz, rows, &zk);
+  b.kv_zk = b.kv_pair ? zk : 0;
+  if (!b.kv_pair) {
+    if (KS == kSideFP8 && !encode_map(&km, a.k_cache, C::kKRow, 128, CU_TENSOR_MAP_SWIZZLE_128B, rows))
+      return cudaErrorInvalidValue;
+    if (KS == kSideCB4 && !encode_map(&km, a.k_cache, C::kKRow, C::kKRow, vswz, rows)) return cudaErrorInvalidValue;
+    if (!encode_map(&vm, a.v_cache, C::kVRow, C::kVRow, vswz, rows)) return cudaErrorInvalidValue;
+  }
+  // the per-token norms of codebook keys and values: [num_blocks * Hkv] rows of 16 floats each
+  b.kn_pair = C::kKNorms && encode_pair(&nm, a.k_scales, a.v_scales, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, kPage, 1,
+                                        CU_TENSOR_MAP_SWIZZLE_NONE, (long long)a.num_blocks * a.Hkv, &zk);
+  b.kn_zk = b.kn_pair ? zk : 0;
   auto kern = partition_cb_kernel<KS, D, NV, CAP>;
   static DeviceFlags attr;
   cudaError_t e = ensure_dynamic_smem(kern, C::kSmem, attr);
@@ -727,11 +784,10 @@ cudaError_t launch_fixed(const Args& a, cudaStream_t s) {
     return e;
   // where there are partitions enough, each warp owns whole partitions and a CTA takes kWarps
   // (or a multiple) consecutive ones
-  Args b = a;
   b.ppc = partitions_per_cta(a, per_sm, sms);
   b.owner = warps_own_partitions(a, per_sm, C::kWarps, sms);
   if (b.owner) b.ppc = C::kWarps * ((b.ppc + C::kWarps - 1) / C::kWarps);
-  kern<<<dim3((a.P + b.ppc - 1) / b.ppc, a.Hkv, a.B), C::kThreads, C::kSmem, s>>>(b, km, vm);
+  kern<<<dim3((a.P + b.ppc - 1) / b.ppc, a.Hkv, a.B), C::kThreads, C::kSmem, s>>>(b, km, vm, nm);
   return cudaGetLastError();
 }
 

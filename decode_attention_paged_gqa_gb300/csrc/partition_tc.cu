@@ -57,7 +57,7 @@ struct Tc {
   static constexpr int kSubs = D * kElemBytes / 128;       // 128-byte swizzled column slabs per row
   static constexpr int kSubBytes = kPage * 128;             // one slab of one page: 2 KB
   static constexpr int kPageBytes = kSubs * kSubBytes;      // one page of K (or V), one kv head
-  static constexpr int kStageBytes = 2 * kPageBytes;        // K + V
+  static constexpr int kStageBytes = 2 * kPageBytes;        // K + V: slab u of K and of V side by side
   static constexpr int kStages = 16384 / kStageBytes > 0 ? 16384 / kStageBytes : 1;  // 64 KB of stages per CTA
   static constexpr int kNT = NV <= 4 ? 1 : 2;               // P.V column tiles (8 columns each)
   static constexpr int kMT = D / 16;                        // O^T row tiles
@@ -136,6 +136,9 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 3 : 2)
   }
   __syncwarp();
 
+  // offsets of K and V within a slab pair of a stage (the side with the lower address first
+  // when one map spans both caches)
+  const uint32_t koff = a.kv_zk ? T::kSubBytes : 0, voff = T::kSubBytes - koff;
   // ---- the warp's partitions and pages, copied kStages ahead of the compute: with
   //      a.owner, partitions p_begin + w, p_begin + w + kWarps, ... and all their pages; else
   //      every partition of the CTA and pages w, w + kWarps, ... of each
@@ -163,8 +166,14 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 3 : 2)
         const int y = (phys * a.Hkv + g) * kPage;
 #pragma unroll
         for (int u = 0; u < T::kSubs; ++u) {
-          ptx::tma_load_2d(dst + u * T::kSubBytes, &kmap, u * (128 / T::kElemBytes), y, bar);
-          ptx::tma_load_2d(dst + T::kPageBytes + u * T::kSubBytes, &vmap, u * (128 / T::kElemBytes), y, bar);
+          // slab u of the page: K and V side by side (one copy when one map spans both caches)
+          const uint32_t d = dst + u * 2 * T::kSubBytes;
+          if (a.kv_pair) {
+            ptx::tma_load_3d(d, &kmap, u * (128 / T::kElemBytes), y, 0, bar);
+          } else {
+            ptx::tma_load_2d(d + koff, &kmap, u * (128 / T::kElemBytes), y, bar);
+            ptx::tma_load_2d(d + voff, &vmap, u * (128 / T::kElemBytes), y, bar);
+          }
         }
       }
     }
@@ -275,7 +284,7 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 3 : 2)
       cphase ^= 1u;
     }
     if (!stalled && (valid_mask & (1u << s))) {
-      const uint32_t kb = stage0 + s * T::kStageBytes, vb = kb + T::kPageBytes;
+      const uint32_t kb = stage0 + s * T::kStageBytes + koff, vb = stage0 + s * T::kStageBytes + voff;
       const int tok0 = (first_page + pg_off + pg_step * i) * kPage;
       // -- S^T = K . Q^T
       float sc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
@@ -284,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 3 : 2)
         for (int ks = 0; ks < T::kKS; ++ks) {
           const int row = ri + 8 * (mi & 1), chunk = 2 * ks + (mi >> 1);
           uint32_t af[4];
-          ptx::ldmatrix_x4(af, swz(kb + (chunk >> 3) * T::kSubBytes, row, chunk & 7));
+          ptx::ldmatrix_x4(af, swz(kb + (chunk >> 3) * 2 * T::kSubBytes, row, chunk & 7));
           mma<FMT>(sc, af, qf[ks][0], qf[ks][1]);
         }
       } else {
@@ -292,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 3 : 2)
         for (int j2 = 0; j2 < T::kKS / 2; ++j2) {
           const int row = ri + 8 * (mi & 1), chunk = 2 * j2 + (mi >> 1);
           uint32_t rr[4];
-          ptx::ldmatrix_x4(rr, swz(kb + (chunk >> 3) * T::kSubBytes, row, chunk & 7));
+          ptx::ldmatrix_x4(rr, swz(kb + (chunk >> 3) * 2 * T::kSubBytes, row, chunk & 7));
           const uint32_t a0[4] = {e4m3x2_to_f16x2(rr[0]), e4m3x2_to_f16x2(rr[1]), e4m3x2_to_f16x2(rr[0] >> 16),
                                   e4m3x2_to_f16x2(rr[1] >> 16)};
           mma<FMT>(sc, a0, qf[2 * j2][0], qf[2 * j2][1]);
@@ -353,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 3 : 2)
         for (int mt = 0; mt < T::kMT; ++mt) {
           const int row = ri + 8 * (mi >> 1), chunk = 2 * mt + (mi & 1);
           uint32_t af[4];
-          ptx::ldmatrix_x4_trans(af, swz(vb + (chunk >> 3) * T::kSubBytes, row, chunk & 7));
+          ptx::ldmatrix_x4_trans(af, swz(vb + (chunk >> 3) * 2 * T::kSubBytes, row, chunk & 7));
 #pragma unroll
           for (int t = 0; t < T::kNT; ++t) mma<FMT>(o[t][mt], af, pb[t][0], pb[t][1]);
         }
@@ -362,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 3 : 2)
         for (int j2 = 0; j2 < T::kMT / 2; ++j2) {
           const int row = ri + 8 * (mi >> 1), chunk = 2 * j2 + (mi & 1);
           uint32_t rr[4];
-          ptx::ldmatrix_x4_trans(rr, swz(vb + (chunk >> 3) * T::kSubBytes, row, chunk & 7));
+          ptx::ldmatrix_x4_trans(rr, swz(vb + (chunk >> 3) * 2 * T::kSubBytes, row, chunk & 7));
           const uint32_t x0 = __byte_perm(rr[0], 0, 0x3120), x1 = __byte_perm(rr[1], 0, 0x3120);
           const uint32_t x2 = __byte_perm(rr[2], 0, 0x3120), x3 = __byte_perm(rr[3], 0, 0x3120);
           const uint32_t a0[4] = {e4m3x2_to_f16x2(x0), e4m3x2_to_f16x2(x0 >> 16), e4m3x2_to_f16x2(x2),
@@ -523,13 +532,39 @@ bool encode_cache_map(CUtensorMap* map, const void* base, int elem_bytes, int D,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// One 3-D view of both caches: (row element, row, side), the side stride being the distance
+// between the two caches, so one box of 16 rows x 128 bytes x 2 sides fetches a page slab of
+// K and of V. The side with the lower address is side 0; *zk receives the side of K. Fails
+// (the caller then uses one map per cache) when the caches coincide or the distance is not a
+// usable stride.
+bool encode_pair_map(CUtensorMap* map, const void* k, const void* v, int elem_bytes, int D, long long rows, int* zk) {
+  auto fn = encode_fn();
+  if (!fn || k == v) return false;
+  const uintptr_t ka = reinterpret_cast<uintptr_t>(k), va = reinterpret_cast<uintptr_t>(v);
+  const uintptr_t lo = ka < va ? ka : va, diff = ka < va ? va - ka : ka - va;
+  if (diff % 16 || diff >= (uintptr_t(1) << 40)) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)rows, 2};
+  const cuuint64_t strides[2] = {(cuuint64_t)D * elem_bytes, (cuuint64_t)diff};
+  const cuuint32_t box[3] = {(cuuint32_t)(128 / elem_bytes), (cuuint32_t)kPage, 2};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  *zk = ka > va;
+  return fn(map, elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 3,
+            reinterpret_cast<void*>(lo), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int FMT, int D, int NV, bool CAP>
 cudaError_t launch_fixed(const Args& a, cudaStream_t s) {
   using T = Tc<FMT, D, NV>;
-  CUtensorMap km, vm;
+  CUtensorMap km{}, vm{};
   const long long rows = (long long)a.num_blocks * a.Hkv * kPage;
-  if (!encode_cache_map(&km, a.k_cache, T::kElemBytes, D, rows) ||
-      !encode_cache_map(&vm, a.v_cache, T::kElemBytes, D, rows))
+  Args b = a;
+  int zk = 0;
+  b.kv_pair = encode_pair_map(&km, a.k_cache, a.v_cache, T::kElemBytes, D, rows, &zk);
+  b.kv_zk = b.kv_pair ? zk : 0;
+  if (!b.kv_pair && (!encode_cache_map(&km, a.k_cache, T::kElemBytes, D, rows) ||
+                     !encode_cache_map(&vm, a.v_cache, T::kElemBytes, D, rows)))
     return cudaErrorInvalidValue;
   auto kern = partition_tc_kernel<FMT, D, NV, CAP>;
   static DeviceFlags attr;
@@ -538,7 +573,6 @@ cudaError_t launch_fixed(const Args& a, cudaStream_t s) {
   static int per_sm = 0, sms[64] = {};
   if (per_sm == 0 && (e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, T::kSmem)) != cudaSuccess)
     return e;
-  Args b = a;
   b.ppc = partitions_per_cta(a, per_sm, sms);
   b.owner = warps_own_partitions(a, per_sm, kWarps, sms);
   if (b.owner) b.ppc = kWarps * ((b.ppc + kWarps - 1) / kWarps);

@@ -11,7 +11,7 @@ import pytest
 import torch
 
 from decode_attention_paged_gqa_gb300 import workloads as wl
-from paged_cases import assert_close, make_case, run_gpu, run_oracle, sample_heads
+from paged_cases import assert_close, make_case, run_gpu, run_oracle, sample_heads, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -91,6 +91,37 @@ def test_alibi(fmt, T, window, softcap, schedule):
     slopes = np.array([2.0 ** (-8.0 * (h + 1) / 8) for h in range(8)], np.float32)
     gpu = run_gpu(c, alibi_slopes=torch.from_numpy(slopes).cuda(), partition_schedule=schedule)
     assert_close(gpu, run_oracle(c, alibi_slopes=slopes), f"{fmt} alibi T{T} W{window} cap{softcap}")
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "fp8", "cb4", "fp8k_cb4v", "cb3k_cb4v"])
+@pytest.mark.parametrize("placement", ["k_below_v", "v_below_k", "one_buffer"])
+def test_cache_placement(fmt, placement):
+    """The kernels fetch a page of K and of V (and of their norms) with one copy through a
+    map spanning both arrays when it can, whichever lies lower in memory, and with one copy
+    per array otherwise (here: K and V given as the same buffer, so the values are the keys)."""
+    spec, lay = small_spec(fmt, 128, 4, lens=[5, 600, 1500, 2100], seed=61)
+    c = make_case(spec, lay)
+    dev = to_device(c)
+    if placement == "one_buffer":
+        if c["k"].shape != c["v"].shape or c["k"].dtype != c["v"].dtype:
+            pytest.skip("K and V rows differ in size for this format")
+        c = dict(c, v=c["k"], v_scales=c["k_scales"])
+        dev["v"], dev["v_scales"] = dev["k"], dev["k_scales"]
+    else:
+        def pair(k, v):  # both in one allocation, in the requested order, 256-byte aligned
+            nk = (k.numel() * k.element_size() + 255) // 256 * 256
+            nv = (v.numel() * v.element_size() + 255) // 256 * 256
+            buf = torch.empty(nk + nv, dtype=torch.uint8, device="cuda")
+            lo, hi = (buf[:nk], buf[nk:]) if placement == "k_below_v" else (buf[nv:], buf[:nv])
+            k2 = lo[:k.numel() * k.element_size()].view(k.dtype).view(k.shape)
+            v2 = hi[:v.numel() * v.element_size()].view(v.dtype).view(v.shape)
+            k2.copy_(k)
+            v2.copy_(v)
+            return k2, v2
+        dev["k"], dev["v"] = pair(dev["k"], dev["v"])
+        if dev["k_scales"] is not None and dev["k_scales"].numel() > 1:
+            dev["k_scales"], dev["v_scales"] = pair(dev["k_scales"], dev["v_scales"])
+    assert_close(run_gpu(c, dev=dev), run_oracle(c), f"{fmt} {placement}")
 
 
 @pytest.mark.parametrize("psize,thresh", [(0, 1024), (16, 1), (48, 64), (512, 1), (4096, 1024)])

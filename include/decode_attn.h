@@ -159,12 +159,15 @@ int decode_attn_paged(const void* q, const void* k_cache, const void* v_cache, c
 
 /* The phases of decode_attn_paged, for callers that schedule or time them one by one.
  * Same arguments and checks as decode_attn_paged; they must run in this order on one stream:
- *   decode_attn_rotate_q   CB4 only (returns DA_OK and does nothing for the other formats):
+ *   decode_attn_rotate_q   formats whose keys are codebook codes (DA_KV_CB4, DA_KV_CB3K_CB4V;
+ *                          returns DA_OK and does nothing for the others):
  *                          q_rot = H diag(sign) q / sqrt(D) into the workspace.
- *   decode_attn_partition  one CTA per (partition, kv head, sequence): partial output, max,
- *                          sum of each partition into the workspace.
- *   decode_attn_reduce     combines the partials of each (sequence, head) into out
- *                          (and un-rotates it for CB4). */
+ *   decode_attn_partition  each CTA walks consecutive partitions of one (sequence, kv head)
+ *                          (p->partition_schedule, p->partitions_per_cta): partial output, max
+ *                          and sum of each partition into the workspace, or the normalised
+ *                          output of an unsplit sequence whose values are not codebook codes.
+ *   decode_attn_reduce     combines the partials of each (sequence, query token, head) into out
+ *                          (and un-rotates it when the values are codebook codes). */
 int decode_attn_rotate_q(const void* q, const void* k_cache, const void* v_cache, const float* k_scales,
                          const float* v_scales, const float* codebook, const float* sign_pattern,
                          const int32_t* block_tables, const int32_t* context_lens, float* out, const da_params* p,

@@ -8,6 +8,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <type_traits>
 
 #include <cuda_runtime.h>
 
@@ -210,6 +211,29 @@ inline bool warps_own_partitions(const Args& a, int per_sm, int warps_per_cta, c
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || cached_sms[dev] <= 0) return false;
   const long long units = (long long)a.P * a.Hkv * a.B;
   return units >= 2ll * cached_sms[dev] * (per_sm > 0 ? per_sm : 1) * warps_per_cta;
+}
+
+// Launch with programmatic stream serialisation: the kernel's CTAs may be scheduled while the
+// previous kernel on the stream finishes (the kernel waits in-kernel, grid_dependency_wait,
+// before reading what that kernel writes), hiding the launch gap between the phases.
+// The arguments are passed by address, so their types must be the kernel's parameter types.
+template <typename... KArgs, typename... Params>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       const Params&... params) {
+  static_assert(sizeof...(KArgs) == sizeof...(Params) && (std::is_same_v<std::remove_cv_t<KArgs>, Params> && ...),
+                "launch_pdl: argument types must match the kernel's parameters");
+  void* args[] = {const_cast<void*>(static_cast<const void*>(&params))...};
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(kern), args);
 }
 
 // Launchers (one translation unit each). They return cudaGetLastError() of their launch.

@@ -115,6 +115,8 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 3 : 2)
   const int tid = threadIdx.x, lane = tid & 31, w = __shfl_sync(kFull, tid >> 5, 0);
   const int gid = lane >> 2, tig = lane & 3;
   const int G = a.Hq / a.Hkv, V = a.T * G;  // group size; virtual heads in use (<= NV)
+  ptx::grid_dependency_wait();   // what the kernel before this one writes (q, the rotated q, ...)
+  ptx::grid_dependents_launch();  // the reduce may be scheduled once every CTA has started
   const int L = load_len(a, b, blockIdx.x == 0 && g == 0 && tid == 0);
   const int np = seq_partitions(L, a.T, a.window, a.psize, a.thresh);
   // this CTA's partitions of (b, g)
@@ -576,8 +578,9 @@ cudaError_t launch_fixed(const Args& a, cudaStream_t s) {
   b.ppc = partitions_per_cta(a, per_sm, sms);
   b.owner = warps_own_partitions(a, per_sm, kWarps, sms);
   if (b.owner) b.ppc = kWarps * ((b.ppc + kWarps - 1) / kWarps);
-  kern<<<dim3((a.P + b.ppc - 1) / b.ppc, a.Hkv, a.B), kThreads, T::kSmem, s>>>(b, km, vm);
-  return cudaGetLastError();
+  // scheduled during the previous kernel's last CTAs (the query rotation, for codebook keys);
+  // waits in-kernel before its first read
+  return launch_pdl(kern, dim3((a.P + b.ppc - 1) / b.ppc, a.Hkv, a.B), dim3(kThreads), T::kSmem, s, b, km, vm);
 }
 
 template <int FMT, int D, bool CAP>

@@ -5,6 +5,8 @@
 //
 // For sequence b, head h with partials (o_p, m_p, l_p), p < P_b (m in log2 units):
 //   M = max_p m_p,  w_p = 2^(m_p - M),  out = sum_p w_p o_p / sum_p w_p l_p.
+// One CTA of 128 threads per (row, head); the partials' loads are issued together: m_p and l_p
+// in one round, the float4 columns of o_p in a few more, with partitions spread over thread groups.
 // An empty sequence (or a query token that attends nothing) gets an all-zero row. An
 // unsplit sequence of a format without a codebook value side was written by the partition
 // kernel and is skipped here. When the values are stored on the rotated basis the result
@@ -17,55 +19,96 @@
 #include "da_internal.cuh"
 #include "fwht.cuh"
 #include "kv_formats.cuh"
+#include "ptx.cuh"
 
 namespace da {
 namespace {
 
+// Folds the partial (M, s) into (M, s): s <- s 2^(M - M') + s_o 2^(M_o - M'), M' = max(M, M_o);
+// an empty side (M = -inf, s = 0) contributes nothing.
+__device__ __forceinline__ void fold(float& M, float& s, float Mo, float so) {
+  const float Mn = fmaxf(M, Mo);
+  if (Mn == -INFINITY) return;
+  s = s * exp2f(M - Mn) + so * exp2f(Mo - Mn);
+  M = Mn;
+}
+
 template <int D, bool kUnrotate>
 __global__ void __launch_bounds__(128) reduce_kernel(const Args a) {
-  const int h = blockIdx.x, row = blockIdx.y, tid = threadIdx.x, lane = tid & 31;  // row = b * T + query token
+  constexpr int kThreads = 128, kCols = D / 4, kGroups = kThreads / kCols;  // float4 columns; partition groups
+  const int h = blockIdx.x, row = blockIdx.y, tid = threadIdx.x, lane = tid & 31, w = tid >> 5;  // row = b * T + query token
   const int b = row / a.T;
-  extern __shared__ float w_s[];  // [P] weights
-  __shared__ float x_s[D];
-  __shared__ float inv_l_s;
+  ptx::grid_dependency_wait();  // the partials of the partition kernel before this one
+  extern __shared__ float w_s[];  // [P]: m_p, then the weights 2^(m_p - M)
+  __shared__ float4 red_o[kGroups][kCols];
+  __shared__ float red_m[kThreads / 32], red_s[kThreads / 32];
+  __shared__ float x_s[kUnrotate ? D : 1];
   const int L = load_len(a, b, false);
   const int np = seq_partitions(L, a.T, a.window, a.psize, a.thresh);
   float* out = a.out + ((size_t)row * a.Hq + h) * D;
   if (np == 0) {
-    for (int d = tid; d < D; d += blockDim.x) out[d] = 0.0f;
+    for (int d = tid; d < D; d += kThreads) out[d] = 0.0f;
     return;
   }
   if (np == 1 && !kUnrotate) return;
   const size_t base = ((size_t)row * a.Hq + h) * a.P;
-  if (tid < 32) {
-    float M = -INFINITY;
-    for (int p = lane; p < np; p += 32) M = fmaxf(M, a.part_m[base + p]);
+
+  // M = max_p m_p and s = sum_p 2^(m_p - M) l_p, each thread folding its partitions
+  // p = tid, tid + 128, ... (m_p and l_p loaded together), then across the block
+  float M = -INFINITY, s = 0.0f;
+  for (int p = tid; p < np; p += kThreads) {
+    const float m = a.part_m[base + p], l = a.part_l[base + p];
+    w_s[p] = m;
+    fold(M, s, m, l);
+  }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    float lsum = 0.0f;
-    for (int p = lane; p < np; p += 32) {
-      const float w = M == -INFINITY ? 0.0f : exp2f(a.part_m[base + p] - M);
-      w_s[p] = w;
-      lsum += w * a.part_l[base + p];
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
-    if (lane == 0) inv_l_s = lsum > 0.0f ? 1.0f / lsum : 0.0f;
+  for (int o = 16; o > 0; o >>= 1) {
+    const float Mo = __shfl_xor_sync(0xffffffffu, M, o), so = __shfl_xor_sync(0xffffffffu, s, o);
+    fold(M, s, Mo, so);
+  }
+  if (lane == 0) {
+    red_m[w] = M;
+    red_s[w] = s;
   }
   __syncthreads();
-  const float inv_l = inv_l_s * (v_side(a.fmt) == kSideFP8 ? __ldg(a.v_scales) : 1.0f);
-  for (int d = tid; d < D; d += blockDim.x) {
-    float acc = 0.0f;
-    for (int p = 0; p < np; ++p) acc = fmaf(w_s[p], a.part_o[(base + p) * D + d], acc);
+  M = red_m[0];
+  s = red_s[0];
+#pragma unroll
+  for (int i = 1; i < kThreads / 32; ++i) fold(M, s, red_m[i], red_s[i]);
+  for (int p = tid; p < np; p += kThreads) w_s[p] = M == -INFINITY ? 0.0f : exp2f(w_s[p] - M);
+  __syncthreads();
+
+  // sum_p w_p o_p: thread (group, column) takes float4 column `col` of partitions
+  // group, group + kGroups, ...; the groups are then added up
+  const int col = tid % kCols, group = tid / kCols;
+  const float4* src = reinterpret_cast<const float4*>(a.part_o + base * D) + col;
+  float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll 8
+  for (int p = group; p < np; p += kGroups) {
+    const float wp = w_s[p];
+    const float4 o = src[(size_t)p * kCols];
+    acc.x = fmaf(wp, o.x, acc.x);
+    acc.y = fmaf(wp, o.y, acc.y);
+    acc.z = fmaf(wp, o.z, acc.z);
+    acc.w = fmaf(wp, o.w, acc.w);
+  }
+  red_o[group][col] = acc;
+  __syncthreads();
+  const float inv_l = (s > 0.0f ? 1.0f / s : 0.0f) * (v_side(a.fmt) == kSideFP8 ? __ldg(a.v_scales) : 1.0f);
+  const float* red = reinterpret_cast<const float*>(red_o);
+  for (int d = tid; d < D; d += kThreads) {
+    float v = red[d];
+#pragma unroll
+    for (int g = 1; g < kGroups; ++g) v += red[g * D + d];
     if (kUnrotate)
-      x_s[d] = acc * inv_l;
+      x_s[d] = v * inv_l;
     else
-      out[d] = acc * inv_l;
+      out[d] = v * inv_l;
   }
   if (kUnrotate) {
     fwht_shared<D>(x_s);
     const float inv_sqrt_d = 1.0f / sqrtf((float)D);
-    for (int d = tid; d < D; d += blockDim.x) out[d] = __ldg(a.sign + d) * x_s[d] * inv_sqrt_d;
+    for (int d = tid; d < D; d += kThreads) out[d] = __ldg(a.sign + d) * x_s[d] * inv_sqrt_d;
   }
 }
 
@@ -73,11 +116,9 @@ template <int D>
 cudaError_t launch_d(const Args& a, cudaStream_t s) {
   dim3 grid(a.Hq, a.B * a.T);
   const size_t smem = sizeof(float) * (size_t)a.P;  // P <= kMaxPartitions: within the default 48 KB
-  if (is_codebook(v_side(a.fmt)))
-    reduce_kernel<D, true><<<grid, 128, smem, s>>>(a);
-  else
-    reduce_kernel<D, false><<<grid, 128, smem, s>>>(a);
-  return cudaGetLastError();
+  // scheduled during the partition kernel's last CTAs; waits for its partials in-kernel
+  if (is_codebook(v_side(a.fmt))) return launch_pdl(reduce_kernel<D, true>, grid, dim3(128), smem, s, a);
+  return launch_pdl(reduce_kernel<D, false>, grid, dim3(128), smem, s, a);
 }
 
 }  // namespace

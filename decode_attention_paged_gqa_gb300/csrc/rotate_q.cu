@@ -10,6 +10,7 @@
 
 #include "da_internal.cuh"
 #include "fwht.cuh"
+#include "ptx.cuh"
 
 namespace da {
 namespace {
@@ -18,6 +19,7 @@ template <int D>
 __global__ void __launch_bounds__(128) rotate_q_kernel(const Args a) {
   const int h = blockIdx.x, row = blockIdx.y;  // row = b * T + query token
   __shared__ float x[D];
+  ptx::grid_dependents_launch();  // the partition kernel may be scheduled meanwhile
   const size_t base = ((size_t)row * a.Hq + h) * D;
   for (int d = threadIdx.x; d < D; d += blockDim.x) x[d] = bf16_to_f32(a.q[base + d]) * __ldg(a.sign + d);
   fwht_shared<D>(x);

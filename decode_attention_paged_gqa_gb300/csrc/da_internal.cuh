@@ -201,16 +201,22 @@ inline int partitions_per_cta(const Args& a, int per_sm, int* cached_sms) {
   return waves < 1 ? 1 : (waves > 8 ? 8 : (int)waves);
 }
 
-// Whether a partition kernel's warps own whole partitions: as requested, else only when
-// there are at least two partitions for every warp the GPU holds at once (else sharing each
-// partition among a CTA's warps keeps more warps busy).
-inline bool warps_own_partitions(const Args& a, int per_sm, int warps_per_cta, const int* cached_sms) {
+// Whether a partition kernel's warps own whole partitions: as requested, else when the
+// batch has at least `min_fill_x2` / 2 partitions (counted at the longest possible span) for
+// every warp the GPU holds at once. Below that, sharing each partition among a CTA's warps
+// keeps more warps busy; above it, the owned schedule saves the per-partition merge. The
+// break-even depends on the kernel: for the codebook kernel (eight warps sharing a partition
+// at D = 128) it lies near half a warp per partition, for the tensor-core kernel between one
+// and two (batches of varied lengths have fewer partitions than counted, so the latter errs
+// high).
+inline bool warps_own_partitions(const Args& a, int per_sm, int warps_per_cta, int min_fill_x2,
+                                 const int* cached_sms) {
   if (a.schedule == 1) return false;
   if (a.schedule == 2) return true;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || cached_sms[dev] <= 0) return false;
   const long long units = (long long)a.P * a.Hkv * a.B;
-  return units >= 2ll * cached_sms[dev] * (per_sm > 0 ? per_sm : 1) * warps_per_cta;
+  return 2ll * units >= (long long)min_fill_x2 * cached_sms[dev] * (per_sm > 0 ? per_sm : 1) * warps_per_cta;
 }
 
 // Launch with programmatic stream serialisation: the kernel's CTAs may be scheduled while the

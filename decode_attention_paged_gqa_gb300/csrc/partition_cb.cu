@@ -787,7 +787,7 @@ cudaError_t launch_fixed(const Args& a, cudaStream_t s) {
   // where there are partitions enough, each warp owns whole partitions and a CTA takes kWarps
   // (or a multiple) consecutive ones
   b.ppc = partitions_per_cta(a, per_sm, sms);
-  b.owner = warps_own_partitions(a, per_sm, C::kWarps, sms);
+  b.owner = warps_own_partitions(a, per_sm, C::kWarps, 1, sms);  // from half a partition per resident warp
   if (b.owner) b.ppc = C::kWarps * ((b.ppc + C::kWarps - 1) / C::kWarps);
   // scheduled during the previous kernel's last CTAs (the query rotation, for codebook keys);
   // waits in-kernel before its first read

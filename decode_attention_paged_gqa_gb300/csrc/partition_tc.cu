@@ -576,7 +576,7 @@ cudaError_t launch_fixed(const Args& a, cudaStream_t s) {
   if (per_sm == 0 && (e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, T::kSmem)) != cudaSuccess)
     return e;
   b.ppc = partitions_per_cta(a, per_sm, sms);
-  b.owner = warps_own_partitions(a, per_sm, kWarps, sms);
+  b.owner = warps_own_partitions(a, per_sm, kWarps, 3, sms);  // from 1.5 partitions per resident warp
   if (b.owner) b.ppc = kWarps * ((b.ppc + kWarps - 1) / kWarps);
   // scheduled during the previous kernel's last CTAs (the query rotation, for codebook keys);
   // waits in-kernel before its first read

@@ -5,8 +5,9 @@
 //
 // For sequence b, head h with partials (o_p, m_p, l_p), p < P_b (m in log2 units):
 //   M = max_p m_p,  w_p = 2^(m_p - M),  out = sum_p w_p o_p / sum_p w_p l_p.
-// One CTA of 128 threads per (row, head); the partials' loads are issued together: m_p and l_p
-// in one round, the float4 columns of o_p in a few more, with partitions spread over thread groups.
+// One CTA per (row, head); the partials' loads are issued together: m_p and l_p in one round,
+// the float4 columns of o_p in one or two more, with the partitions spread over thread groups
+// (128 threads: 4 groups at D = 128, 2 at D = 256; 256 threads, for 32 or more partitions: 8 / 4).
 // An empty sequence (or a query token that attends nothing) gets an all-zero row. An
 // unsplit sequence of a format without a codebook value side was written by the partition
 // kernel and is skipped here. When the values are stored on the rotated basis the result
@@ -33,9 +34,9 @@ __device__ __forceinline__ void fold(float& M, float& s, float Mo, float so) {
   M = Mn;
 }
 
-template <int D, bool kUnrotate>
-__global__ void __launch_bounds__(128) reduce_kernel(const Args a) {
-  constexpr int kThreads = 128, kCols = D / 4, kGroups = kThreads / kCols;  // float4 columns; partition groups
+template <int D, bool kUnrotate, int kThreads>
+__global__ void __launch_bounds__(kThreads) reduce_kernel(const Args a) {
+  constexpr int kCols = D / 4, kGroups = kThreads / kCols;  // float4 columns; partition groups
   const int h = blockIdx.x, row = blockIdx.y, tid = threadIdx.x, lane = tid & 31, w = tid >> 5;  // row = b * T + query token
   const int b = row / a.T;
   ptx::grid_dependency_wait();  // the partials of the partition kernel before this one
@@ -54,7 +55,7 @@ __global__ void __launch_bounds__(128) reduce_kernel(const Args a) {
   const size_t base = ((size_t)row * a.Hq + h) * a.P;
 
   // M = max_p m_p and s = sum_p 2^(m_p - M) l_p, each thread folding its partitions
-  // p = tid, tid + 128, ... (m_p and l_p loaded together), then across the block
+  // p = tid, tid + kThreads, ... (m_p and l_p loaded together), then across the block
   float M = -INFINITY, s = 0.0f;
   for (int p = tid; p < np; p += kThreads) {
     const float m = a.part_m[base + p], l = a.part_l[base + p];
@@ -116,9 +117,15 @@ template <int D>
 cudaError_t launch_d(const Args& a, cudaStream_t s) {
   dim3 grid(a.Hq, a.B * a.T);
   const size_t smem = sizeof(float) * (size_t)a.P;  // P <= kMaxPartitions: within the default 48 KB
-  // scheduled during the partition kernel's last CTAs; waits for its partials in-kernel
-  if (is_codebook(v_side(a.fmt))) return launch_pdl(reduce_kernel<D, true>, grid, dim3(128), smem, s, a);
-  return launch_pdl(reduce_kernel<D, false>, grid, dim3(128), smem, s, a);
+  // scheduled during the partition kernel's last CTAs; waits for its partials in-kernel. Many
+  // partitions per row: 256 threads, so each thread's loads are one round; few: 128, so that a
+  // large batch's rows stay within one wave of CTAs.
+  const bool rot = is_codebook(v_side(a.fmt));
+  if (a.P >= 32)
+    return rot ? launch_pdl(reduce_kernel<D, true, 256>, grid, dim3(256), smem, s, a)
+               : launch_pdl(reduce_kernel<D, false, 256>, grid, dim3(256), smem, s, a);
+  return rot ? launch_pdl(reduce_kernel<D, true, 128>, grid, dim3(128), smem, s, a)
+             : launch_pdl(reduce_kernel<D, false, 128>, grid, dim3(128), smem, s, a);
 }
 
 }  // namespace

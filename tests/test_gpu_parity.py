@@ -124,6 +124,44 @@ def test_cache_placement(fmt, placement):
     assert_close(run_gpu(c, dev=dev), run_oracle(c), f"{fmt} {placement}")
 
 
+@pytest.mark.parametrize("fmt", ["bf16", "fp8", "cb4", "cb3k_cb4v"])
+@pytest.mark.parametrize("schedule", [1, 2])
+def test_back_to_back_calls_see_fresh_inputs(fmt, schedule):
+    """Calls queued back to back on one stream, sharing one workspace, with the query and the
+    context lengths rewritten by stream-ordered copies between them and no host sync: each
+    phase is launched early (programmatic dependent launch) and must still read what the
+    copies and the previous call left, and each call's partials must not mix with the next's."""
+    import decode_attention_paged_gqa_gb300 as da
+    from paged_cases import params_for
+
+    lens = [0, 17, 1023, 1500, 2053, 4097]
+    spec = wl.WorkloadSpec(f"b2b_{fmt}", len(lens), 8, 2, 128, fmt, 0, max(lens), seed=77)
+    c = make_case(spec, wl.make_layout(spec, lens=lens))
+    dev = to_device(c)
+    p = params_for(c, partition_schedule=schedule)
+    ws = torch.empty(da.decode_attn_workspace_bytes(p), dtype=torch.uint8, device="cuda")
+    da.attach_workspace(p, ws)
+    da.decode_attn_workspace_init(p)
+    variants = []
+    for i in range(4):
+        q_i = torch.roll(c["q"], shifts=i, dims=-2)  # heads rotated: every output row changes
+        lens_i = np.maximum(c["lens"] - 301 * i, 0).astype(c["lens"].dtype)
+        variants.append((q_i, lens_i))
+    q_src = [q.cuda() for q, _ in variants]
+    len_src = [torch.from_numpy(ln).cuda() for _, ln in variants]
+    outs = [torch.full(tuple(c["q"].shape), float("nan"), dtype=torch.float32, device="cuda") for _ in variants]
+    torch.cuda.synchronize()
+    for i in range(len(variants)):
+        dev["q"].copy_(q_src[i])
+        dev["lens"].copy_(len_src[i])
+        da.decode_attn_paged(dev["q"], dev["k"], dev["v"], dev["k_scales"], dev["v_scales"], dev["codebook"],
+                             dev["sign"], dev["bt"], dev["lens"], outs[i], p)
+    torch.cuda.synchronize()
+    assert da.decode_attn_get_device_error(p) == 0
+    for i, (q_i, lens_i) in enumerate(variants):
+        assert_close(outs[i].cpu().numpy(), run_oracle(dict(c, q=q_i, lens=lens_i)), f"{fmt} call {i}")
+
+
 @pytest.mark.parametrize("psize,thresh", [(0, 1024), (16, 1), (48, 64), (512, 1), (4096, 1024)])
 def test_partition_sizes(psize, thresh):
     spec, lay = small_spec("bf16", 128, 4, lens=EDGE_LENS, seed=psize + 3)

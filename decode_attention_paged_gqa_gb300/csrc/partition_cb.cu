@@ -173,15 +173,17 @@ __device__ __forceinline__ void key_frag(uint32_t (&af)[4], const uint32_t* k0, 
 
 template <int S, int N, int KS, int D, int NV>
 struct KeySteps {
-  // S^T += A(k-step S) . Q^T for S = S .. N-1 (compile-time unrolled so byte offsets are constants)
-  __device__ static __forceinline__ void run(float (&sc)[4], const uint32_t* k0, const uint32_t* k1, const LutRef& lutk,
-                                             const uint32_t (*qf)[2], const uint32_t (*ql)[2]) {
+  // S^T += A(k-step S) . Q^T for S = S .. N-1 (compile-time unrolled so byte offsets are
+  // constants), odd k-steps into sc1 so that the two dependent MMA chains are half as long
+  __device__ static __forceinline__ void run(float (&sc0)[4], float (&sc1)[4], const uint32_t* k0, const uint32_t* k1,
+                                             const LutRef& lutk, const uint32_t (*qf)[2], const uint32_t (*ql)[2]) {
     if constexpr (S < N) {
       uint32_t af[4];
       key_frag<KS, D, S>(af, k0, k1, lutk);
+      float(&sc)[4] = (S & 1) ? sc1 : sc0;
       ptx::mma_f16(sc, af, qf[S][0], qf[S][1]);
       if constexpr (NV == 8) ptx::mma_f16(sc, af, ql[S][0], ql[S][1]);
-      KeySteps<S + 1, N, KS, D, NV>::run(sc, k0, k1, lutk, qf, ql);
+      KeySteps<S + 1, N, KS, D, NV>::run(sc0, sc1, k0, k1, lutk, qf, ql);
     }
   }
 };
@@ -465,8 +467,9 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 2)
     if (!stalled && (valid_mask & (1u << s))) {
       const uint32_t sb = stage0 + s * C::kStageBytes, kb = sb + koff, vb = sb + voff;
       const int tok0 = (first_page + pg_off + pg_step * i) * kPage;
-      // -- S^T = K . Q^T
-      float sc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      // -- S^T = K . Q^T, the k-steps alternating between two accumulators (two dependent MMA
+      //    chains of half the length), added at the end
+      float sc[4] = {0.0f, 0.0f, 0.0f, 0.0f}, sc2[4] = {0.0f, 0.0f, 0.0f, 0.0f};
       if constexpr (KS == kSideFP8) {
 #pragma unroll
         for (int j2 = 0; j2 < C::kKS / 2; ++j2) {
@@ -478,8 +481,10 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 2)
           ptx::mma_f16(sc, a0, qf[2 * j2][0], qf[2 * j2][1]);
           const uint32_t a1[4] = {e4m3x2_to_f16x2(rr[2]), e4m3x2_to_f16x2(rr[3]), e4m3x2_to_f16x2(rr[2] >> 16),
                                   e4m3x2_to_f16x2(rr[3] >> 16)};
-          ptx::mma_f16(sc, a1, qf[2 * j2 + 1][0], qf[2 * j2 + 1][1]);
+          ptx::mma_f16(sc2, a1, qf[2 * j2 + 1][0], qf[2 * j2 + 1][1]);
         }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sc[e] += sc2[e];
       } else {
         // the thread's key bytes: D/8 per row (4-bit) or 3D/32 (3-bit), rows gid and gid + 8
         constexpr int kWords = KS == kSideCB4 ? D / 32 : 3 * D / 128;
@@ -507,7 +512,9 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 2)
             k1[c] = lds32(kb + (gid + 8) * C::kKRow + (3 * D / 32) * tig + 4 * c);
           }
         }
-        KeySteps<0, C::kKS, KS, D, NV>::run(sc, k0, k1, lutk, qf, ql);
+        KeySteps<0, C::kKS, KS, D, NV>::run(sc, sc2, k0, k1, lutk, qf, ql);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sc[e] += sc2[e];
         if constexpr (NV <= 4) {
 #pragma unroll
           for (int e = 0; e < 4; ++e) sc[e] += __shfl_xor_sync(kFull, sc[e], 2);  // hi + lo columns

@@ -288,15 +288,16 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 3 : 2)
     if (!stalled && (valid_mask & (1u << s))) {
       const uint32_t kb = stage0 + s * T::kStageBytes + koff, vb = stage0 + s * T::kStageBytes + voff;
       const int tok0 = (first_page + pg_off + pg_step * i) * kPage;
-      // -- S^T = K . Q^T
-      float sc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      // -- S^T = K . Q^T, the k-steps alternating between two accumulators (two dependent MMA
+      //    chains of half the length), added at the end
+      float sc[4] = {0.0f, 0.0f, 0.0f, 0.0f}, sc2[4] = {0.0f, 0.0f, 0.0f, 0.0f};
       if constexpr (FMT == DA_KV_BF16) {
 #pragma unroll
         for (int ks = 0; ks < T::kKS; ++ks) {
           const int row = ri + 8 * (mi & 1), chunk = 2 * ks + (mi >> 1);
           uint32_t af[4];
           ptx::ldmatrix_x4(af, swz(kb + (chunk >> 3) * 2 * T::kSubBytes, row, chunk & 7));
-          mma<FMT>(sc, af, qf[ks][0], qf[ks][1]);
+          mma<FMT>((ks & 1) ? sc2 : sc, af, qf[ks][0], qf[ks][1]);
         }
       } else {
 #pragma unroll
@@ -309,9 +310,11 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 3 : 2)
           mma<FMT>(sc, a0, qf[2 * j2][0], qf[2 * j2][1]);
           const uint32_t a1[4] = {e4m3x2_to_f16x2(rr[2]), e4m3x2_to_f16x2(rr[3]), e4m3x2_to_f16x2(rr[2] >> 16),
                                   e4m3x2_to_f16x2(rr[3] >> 16)};
-          mma<FMT>(sc, a1, qf[2 * j2 + 1][0], qf[2 * j2 + 1][1]);
+          mma<FMT>(sc2, a1, qf[2 * j2 + 1][0], qf[2 * j2 + 1][1]);
         }
       }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sc[e] += sc2[e];
       // -- scale (log2 domain), softcap, mask; sc[0], sc[1]: token gid; sc[2], sc[3]: token gid + 8
 #pragma unroll
       for (int e = 0; e < 4; ++e) sc[e] = CAP ? cap_post * tanhf(sc[e] * cap_pre) : sc[e] * score_scale;

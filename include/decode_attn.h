@@ -24,6 +24,12 @@
  *   - Work is enqueued on `stream` (a cudaStream_t passed as void*; NULL = legacy default
  *     stream) and runs asynchronously. No entry point synchronises, except
  *     decode_attn_get_device_error, which says so.
+ *   - The partition kernel and the reduce are launched with programmatic stream
+ *     serialisation: their CTAs may be scheduled while the previous kernel on `stream` is
+ *     still running, and they wait inside the kernel, before their first read of any input
+ *     or workspace, until that kernel has completed and its writes are visible. Stream order
+ *     is therefore kept as for ordinary launches; only
+ *     the launch gap between kernels is hidden.
  *   - Return value: DA_OK (0) or a negative DA_ERR_* code. Argument checks happen on the
  *     host before anything is enqueued: a call that returns DA_ERR_INVALID_ARG,
  *     DA_ERR_UNSUPPORTED or DA_ERR_WORKSPACE has enqueued nothing.

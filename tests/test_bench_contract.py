@@ -1,0 +1,39 @@
+"""bench.py's JSON contract on the CPU: the reference arm (the fp64 oracle timed on the host
+cores) prints one line with the contract's keys, and the GPU arm refuses to run without a
+GPU instead of falling back to the CPU."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _bench(*args, timeout=300):
+    return subprocess.run([sys.executable, "bench.py", *args], cwd=ROOT, capture_output=True, text=True,
+                          timeout=timeout)
+
+
+def test_reference_arm_line():
+    r = _bench("--impl", "reference", "--workload", "tiny_bf16", "--steps", "1", "--warmup", "0")
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["unit"] == "GB/s" and d["higher_is_better"] is True
+    assert d["value"] > 0 and d["steps"] == 1 and d["warmup"] == 0 and d["n_gpus"] == 1
+    assert d["config"]["workload"] == "tiny_bf16"
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU refusal")
+def test_gpu_arm_refuses_without_gpu():
+    r = _bench("--workload", "tiny_bf16", "--steps", "1", "--warmup", "0", timeout=120)
+    assert r.returncode != 0
+    assert "needs a CUDA GPU" in (r.stdout + r.stderr)
+    assert not [ln for ln in r.stdout.splitlines() if ln.startswith("{")]

@@ -162,6 +162,47 @@ def test_back_to_back_calls_see_fresh_inputs(fmt, schedule):
         assert_close(outs[i].cpu().numpy(), run_oracle(dict(c, q=q_i, lens=lens_i)), f"{fmt} call {i}")
 
 
+@pytest.mark.parametrize("fmt", ["bf16", "fp8", "cb4"])
+def test_cuda_graph_capture_and_replay(fmt):
+    """decode_attn_paged captured into a CUDA graph (its phases launched with programmatic
+    stream serialisation become graph nodes) and replayed with new query contents gives the
+    oracle's result on every replay."""
+    import decode_attention_paged_gqa_gb300 as da
+    from paged_cases import params_for
+
+    lens = [0, 17, 1500, 4097]
+    spec = wl.WorkloadSpec(f"graph_{fmt}", len(lens), 8, 2, 128, fmt, 0, max(lens), seed=91)
+    c = make_case(spec, wl.make_layout(spec, lens=lens))
+    dev = to_device(c)
+    p = params_for(c)
+    ws = torch.empty(da.decode_attn_workspace_bytes(p), dtype=torch.uint8, device="cuda")
+    da.attach_workspace(p, ws)
+    da.decode_attn_workspace_init(p)
+    out = torch.full(tuple(c["q"].shape), float("nan"), dtype=torch.float32, device="cuda")
+
+    def call():
+        da.decode_attn_paged(dev["q"], dev["k"], dev["v"], dev["k_scales"], dev["v_scales"], dev["codebook"],
+                             dev["sign"], dev["bt"], dev["lens"], out, p)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):  # one call outside the capture: the launchers' one-time set-up
+        call()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        call()
+    for i in range(3):
+        q_i = torch.roll(c["q"], shifts=i + 1, dims=-2)
+        dev["q"].copy_(q_i.cuda())
+        out.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert_close(out.cpu().numpy(), run_oracle(dict(c, q=q_i)), f"{fmt} replay {i}")
+    assert da.decode_attn_get_device_error(p) == 0
+
+
 @pytest.mark.parametrize("psize,thresh", [(0, 1024), (16, 1), (48, 64), (512, 1), (4096, 1024)])
 def test_partition_sizes(psize, thresh):
     spec, lay = small_spec("bf16", 128, 4, lens=EDGE_LENS, seed=psize + 3)

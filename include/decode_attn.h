@@ -29,8 +29,7 @@
  *     still running, and they wait inside the kernel, before their first read of any input
  *     or workspace, until that kernel has completed and its writes are visible. Stream order
  *     is therefore kept as for ordinary launches, also when the calls are captured into a
- *     CUDA graph; only
- *     the launch gap between kernels is hidden.
+ *     CUDA graph; only the launch gap between kernels is hidden.
  *   - Return value: DA_OK (0) or a negative DA_ERR_* code. Argument checks happen on the
  *     host before anything is enqueued: a call that returns DA_ERR_INVALID_ARG,
  *     DA_ERR_UNSUPPORTED or DA_ERR_WORKSPACE has enqueued nothing.

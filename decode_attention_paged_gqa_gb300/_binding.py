@@ -68,15 +68,18 @@ def make_params(*, batch, num_q_heads, num_kv_heads, head_dim, num_blocks, max_b
     p.partition_size, p.split_threshold = int(partition_size), int(split_threshold)
     p.partition_schedule, p.partitions_per_cta = int(partition_schedule), int(partitions_per_cta)
     p.alibi_slopes = _ptr(alibi_slopes)  # a device tensor of Hq float32 slopes, or None
+    p._alibi_ref = alibi_slopes  # the params hold the tensors they point at
     if workspace is not None:
         attach_workspace(p, workspace)
     return p
 
 
 def attach_workspace(p: da_params, workspace) -> da_params:
-    """Point the params at a device buffer (torch tensor) used as the call's workspace."""
+    """Point the params at a device buffer (torch tensor) used as the call's workspace. The
+    params keep a reference to the tensor, so it lives at least as long as they do."""
     p.workspace = workspace.data_ptr()
     p.workspace_bytes = workspace.numel() * workspace.element_size()
+    p._workspace_ref = workspace
     return p
 
 

@@ -144,3 +144,22 @@ def test_library_codebook_equals_oracle_codebook(D):
     assert np.array_equal(ours, ref)
     with pytest.raises(da.DecodeAttnError):
         da.decode_attn_codebook_lloyd_max(1, 1.0)
+
+
+def test_params_keep_their_tensors_alive():
+    """The params hold references to the workspace and slope tensors whose addresses they
+    carry, so dropping the caller's names does not free memory a later call would use."""
+    import gc
+    import weakref
+
+    import torch
+
+    ws, slopes = torch.empty(1024, dtype=torch.uint8), torch.zeros(32, dtype=torch.float32)
+    refs = weakref.ref(ws), weakref.ref(slopes)
+    p = base(alibi_slopes=slopes)
+    da.attach_workspace(p, ws)
+    addr = ws.data_ptr()
+    del ws, slopes
+    gc.collect()
+    assert all(r() is not None for r in refs)
+    assert p.workspace == addr and p.workspace_bytes == 1024

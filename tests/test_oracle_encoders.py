@@ -62,10 +62,12 @@ def _midpoints():
 
 def test_e4m3_encode_matches_torch_cast(oracle):
     rng = np.random.default_rng(7)
+    bits = rng.integers(0, 2 ** 32, 2_000_000, dtype=np.uint64).astype(np.uint32).view(np.float32)
     x = np.concatenate([
-        rng.standard_normal(400_000).astype(np.float32) * np.float32(60.0),
-        rng.standard_normal(200_000).astype(np.float32) * np.float32(0.01),
-        (rng.random(200_000).astype(np.float32) - np.float32(0.5)) * np.float32(900.0),
+        rng.standard_normal(5_000_000).astype(np.float32) * np.float32(60.0),
+        rng.standard_normal(1_500_000).astype(np.float32) * np.float32(0.01),
+        (rng.random(1_500_000).astype(np.float32) - np.float32(0.5)) * np.float32(900.0),
+        bits[np.isfinite(bits)],  # every binary32 exponent, subnormals included
         _midpoints(),
         np.array([0.0, -0.0, 2.0 ** -10, -(2.0 ** -10), 2.0 ** -11, 3 * 2.0 ** -10, 448.0, 463.99], np.float32),
     ]).astype(np.float32)

@@ -10,6 +10,7 @@ import test_oracle_attention as A
 import test_oracle_encoders as E
 import test_oracle_alibi as AL
 import test_oracle_multitoken as M
+import test_oracle_mixed_formats as X
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
 
@@ -49,6 +50,14 @@ MUTATIONS = [
      "s[t - s0] += (double)j->alibi[h] * (double)(pos - t);"),
     ("alibi slope of the kv head", "s[t - s0] += (double)j->alibi[h] * (double)(t - pos);",
      "s[t - s0] += (double)j->alibi[g] * (double)(t - pos);"),
+    ("fp8 scale for a different maximum", "j.scale = amax > 0.0f ? amax / 448.0f : 1.0f;",
+     "j.scale = amax > 0.0f ? amax / 240.0f : 1.0f;"),
+    ("3-bit-key format decodes values with the key levels",
+     "((j->fmt == OR_FMT_CB3K_CB4V && which) ? 8 : 0)", "0"),
+    ("norm of the neighbouring token", "float sc = (which ? j->v_scales : j->k_scales)[row];",
+     "float sc = (which ? j->v_scales : j->k_scales)[row ^ 1];"),
+    ("query tokens in reverse order", "int64_t qi = ((int64_t)b * T + jq) * j->Hq + h;",
+     "int64_t qi = ((int64_t)b * T + (T - 1 - jq)) * j->Hq + h;"),
 ]
 
 PINS = [
@@ -65,6 +74,9 @@ PINS = [
     (M.test_multitoken_matches_sdpa_with_mask, dict(T=4, window=0)),
     (M.test_multitoken_matches_sdpa_with_mask, dict(T=3, window=20)),
     (AL.test_alibi_matches_sdpa_with_bias, dict(T=3, window=0, softcap=0.0)),
+    (X.test_fp8_keys_codebook_values_matches_route, {}),
+    (X.test_three_bit_keys_codebook_values_matches_route, {}),
+    (E.test_fp8_quantize_scale_and_error_bound, {}),
     (E.test_e4m3_decode_fixed_points, {}),
     (E.test_e4m3_decode_matches_torch, {}),
     (E.test_e4m3_encode_matches_torch_cast, {}),

@@ -48,6 +48,8 @@ def test_workspace_bytes_and_partitions():
     assert da.decode_attn_max_partitions(base(max_context_len=32768)) == 64
     assert da.decode_attn_max_partitions(base(max_context_len=16384, window=4096)) == 8
     assert da.decode_attn_max_partitions(base(max_context_len=32768, partition_size=0)) == 1
+    at_limit = base(max_context_len=8192 * 16, max_blocks_per_seq=8192, partition_size=16, split_threshold=1)
+    assert da.decode_attn_max_partitions(at_limit) == 8192 and da.decode_attn_workspace_bytes(at_limit) > 0
     cb4 = da.decode_attn_workspace_bytes(base(kv_format="cb4"))
     assert cb4 >= n + 4 * 32 * 128 * 4  # plus the rotated queries
 
@@ -67,6 +69,8 @@ def test_workspace_bytes_and_partitions():
     (dict(partitions_per_cta=65), da._binding.DA_ERR_INVALID_ARG),
     (dict(partitions_per_cta=-2), da._binding.DA_ERR_INVALID_ARG),
     (dict(max_context_len=1 << 30), da._binding.DA_ERR_UNSUPPORTED),  # more partitions than built
+    (dict(max_context_len=8192 * 16 + 1, max_blocks_per_seq=8193, partition_size=16, split_threshold=1),
+     da._binding.DA_ERR_UNSUPPORTED),  # 8193 partitions: one past the limit
 ])
 def test_bad_params_are_rejected(kw, status):
     p = base(**kw)

@@ -203,6 +203,17 @@ def test_cuda_graph_capture_and_replay(fmt):
     assert da.decode_attn_get_device_error(p) == 0
 
 
+@pytest.mark.parametrize("fmt", ["bf16", "cb4"])
+def test_maximum_partition_count(fmt):
+    """The largest grid the library takes: 8192 partitions of 16 tokens for a 131072-token
+    sequence (the reduce then combines 8192 partials per row), next to a ragged shorter one."""
+    lens = [131072, 70001]
+    spec = wl.WorkloadSpec(f"maxp_{fmt}", len(lens), 8, 2, 128, fmt, 0, max(lens), seed=123)
+    c = make_case(spec, wl.make_layout(spec, lens=lens))
+    ref = run_oracle(c, partition_size=0)
+    assert_close(run_gpu(c, partition_size=16, split_threshold=1), ref, f"{fmt}, 8192 partitions")
+
+
 @pytest.mark.parametrize("psize,thresh", [(0, 1024), (16, 1), (48, 64), (512, 1), (4096, 1024)])
 def test_partition_sizes(psize, thresh):
     spec, lay = small_spec("bf16", 128, 4, lens=EDGE_LENS, seed=psize + 3)

@@ -123,18 +123,40 @@ def test_lloyd_max_fixed_point_conditions(oracle):
         assert abs(mom / mass - lv[i]) < 1e-10 * sigma
 
 
-def test_lloyd_max_matches_classical_table(oracle):
-    g = json.load(open(os.path.join(GOLDEN, "lloyd_max_gaussian_16.json")))
-    lv, _, _ = oracle.lloyd_max(16, 1.0)
-    pos = lv[8:]
-    assert np.allclose(pos, g["output_levels"], atol=g["tolerance"], rtol=0)
-    thr = (lv[8:] + np.concatenate([[-lv[8]], lv[8:-1]])) / 2
-    assert np.allclose(thr, g["thresholds"], atol=g["tolerance"], rtol=0)
-    # distortion of the quantiser, by numerical integration over its cells
-    t = np.concatenate([[-np.inf], (lv[:-1] + lv[1:]) / 2, [np.inf]])
-    pdf = scipy.stats.norm().pdf
-    mse = sum(scipy.integrate.quad(lambda z: (z - lv[i]) ** 2 * pdf(z), t[i], t[i + 1])[0] for i in range(16))
-    assert abs(mse - g["mean_squared_error"]) < g["mse_tolerance"]
+def _gaussian_quantiser_distortion(pos):
+    """Mean squared error of the symmetric quantiser of N(0, 1) with positive levels `pos`
+    (sorted) and cell boundaries at the midpoints, in closed form, with its gradient. Over a
+    cell [a, b] with level c: int (x - c)^2 phi = (1 + c^2)(Phi(b) - Phi(a)) - 2c(phi(a) - phi(b))
+    + (a phi(a) - b phi(b)); d/dc = 2(c (Phi(b) - Phi(a)) - (phi(a) - phi(b))), the boundary
+    terms cancelling at midpoints."""
+    import scipy.stats
+
+    c = np.concatenate([-pos[::-1], pos])
+    t = np.concatenate([[-np.inf], (c[:-1] + c[1:]) / 2, [np.inf]])
+    a, b = t[:-1], t[1:]
+    Pa, Pb = scipy.stats.norm.cdf(a), scipy.stats.norm.cdf(b)
+    fa, fb = scipy.stats.norm.pdf(a), scipy.stats.norm.pdf(b)
+    afa = np.where(np.isfinite(a), a, 0.0) * fa  # x phi(x) -> 0 at +-inf
+    bfb = np.where(np.isfinite(b), b, 0.0) * fb
+    mse = np.sum((1 + c ** 2) * (Pb - Pa) - 2 * c * (fa - fb) + (afa - bfb))
+    g = 2 * (c * (Pb - Pa) - (fa - fb))
+    n = len(pos)
+    return mse, g[n:] - g[:n][::-1]  # d/d pos_i: the level +pos_i and its mirror -pos_i
+
+
+@pytest.mark.parametrize("levels", [8, 16])
+def test_lloyd_max_is_the_distortion_minimum(oracle, levels):
+    """The oracle's levels (a fixed-point iteration) against a different algorithm: direct
+    minimisation of the closed-form distortion (scipy BFGS from evenly spaced levels)."""
+    import scipy.optimize
+
+    lv, _, _ = oracle.lloyd_max(levels, 1.0)
+    x0 = np.linspace(0.2, 2.0, levels // 2)
+    res = scipy.optimize.minimize(lambda p: _gaussian_quantiser_distortion(np.sort(p)), x0, jac=True,
+                                  method="BFGS", options={"gtol": 1e-13, "maxiter": 10000})
+    best = np.sort(res.x)
+    assert np.abs(lv[levels // 2:] - best).max() < 1e-7
+    assert abs(_gaussian_quantiser_distortion(lv[levels // 2:])[0] - res.fun) < 1e-13
 
 
 # ------------------------------------------------------------------ 4-bit codebook encode

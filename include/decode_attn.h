@@ -108,7 +108,9 @@ typedef struct da_params {
   float softmax_scale;        /* scale applied to q . k (e.g. 1/sqrt(D)) */
   float softcap;              /* 0 = off; else s <- softcap * tanh(s / softcap) after scaling */
   int32_t window;             /* 0 = off; else attend only the last `window` tokens (t >= L - window) */
-  int32_t partition_size;     /* tokens per split-K partition (512); 0 = never split */
+  int32_t partition_size;     /* tokens per split-K partition (512); 0 = never split. A span of
+                                 max_context_len tokens may have at most 8192 partitions
+                                 (decode_attn_max_partitions), else DA_ERR_UNSUPPORTED. */
   int32_t split_threshold;    /* split a sequence iff its attended length >= this (1024) */
   int32_t partition_schedule; /* how a partition kernel's warps share the work (results are the same
                                  up to rounding): 0 = chosen per call from the number of partitions,

@@ -51,6 +51,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clocks", action="store_true", help="skip the nvidia-smi clock sampling and its soak")
+    ap.add_argument("--no-per-workload", action="store_true",
+                    help="time only the chosen workload (skip the FP8, Gemma-style, 4-bit and tiny entries)")
     return ap.parse_args()
 
 
@@ -282,10 +284,11 @@ def oracle_inputs(spec, host, src, nseq):
     return q, k, v, sub_bt, lens, kw
 
 
-def oracle_sample(spec, host, src, target_s: float, max_seqs=None):
+def oracle_sample(spec, host, src, target_s: float, max_seqs=None, threads: int = 0):
     """Time the fp64 oracle on the first n sequences (all heads) of the workload, n chosen so
     that the timed sample takes about target_s; when the whole batch takes less than that,
-    the batch is repeated until target_s has passed. Returns (GB/s, seconds, n, threads, reps)."""
+    the batch is repeated until target_s has passed. threads: 0 = every host core, else that
+    many. Returns (GB/s, seconds, n, threads, reps)."""
     import oracle
     from decode_attention_paged_gqa_gb300.metrics import algorithmic_kv_bytes
 
@@ -295,7 +298,7 @@ def oracle_sample(spec, host, src, target_s: float, max_seqs=None):
         _, thr = oracle.decode_attention(q, k, v, bt, lens, kv_format=spec.kv_format, num_kv_heads=spec.num_kv_heads,
                                          softmax_scale=spec.scale, softcap=spec.softcap, window=spec.window,
                                          partition_size=spec.partition_size, split_threshold=spec.split_threshold,
-                                         return_threads=True, **kw)
+                                         threads=threads, return_threads=True, **kw)
         return time.perf_counter() - t0, thr, lens
 
     t1, _, _ = run(1)
@@ -341,6 +344,164 @@ def reference_arm(args, spec, rank, world):
 
 
 # ----------------------------------------------------------------------------- GPU arm
+# workloads timed beside the headline in the same process (one entry each in "per_workload"):
+# the FP8 long-context batch, the Gemma-style windowed batch, the 4-bit codebook batch, and the
+# tiny batch (L2-resident, latency-bound; its oracle is timed on every core and on one)
+EXTRA_WORKLOADS = ("fp8_long_32k", "gemma_window_softcap", "cb4_long_32k", "tiny_bf16")
+# kernels per call: the partition kernel and the reduce, plus the query rotation for formats
+# whose keys are stored on the rotated basis
+KERNELS_PER_CALL = {"bf16": 2, "fp8": 2, "cb4": 3, "fp8k_cb4v": 2, "cb3k_cb4v": 3}
+
+
+class Prepared:
+    """One workload resident on the device: inputs, params, workspace and output."""
+
+    def __init__(self, spec):
+        import torch
+
+        import decode_attention_paged_gqa_gb300 as da
+        from decode_attention_paged_gqa_gb300.metrics import algorithmic_kv_bytes
+
+        self.spec = spec
+        self.lay, self.host, self.src = build_inputs(spec)
+        self.dev = {k: (None if t is None else t.cuda()) for k, t in self.host.items()}
+        self.kv_bytes = algorithmic_kv_bytes(self.lay.context_lens, spec.window, spec.num_kv_heads, spec.kv_format,
+                                             spec.head_dim)
+        self.cache_bytes = sum(self.host[w].numel() * self.host[w].element_size() for w in ("k", "v"))
+        self.p = da.make_params(batch=spec.batch, num_q_heads=spec.num_q_heads, num_kv_heads=spec.num_kv_heads,
+                                head_dim=spec.head_dim, num_blocks=self.lay.num_blocks,
+                                max_blocks_per_seq=self.lay.block_tables.shape[1], max_context_len=spec.ctx_max,
+                                kv_format=spec.kv_format, softmax_scale=spec.scale, softcap=spec.softcap,
+                                window=spec.window, partition_size=spec.partition_size,
+                                split_threshold=spec.split_threshold)
+        self.ws = torch.empty(da.decode_attn_workspace_bytes(self.p), dtype=torch.uint8, device="cuda")
+        da.attach_workspace(self.p, self.ws)
+        da.decode_attn_workspace_init(self.p)
+        self.out = torch.empty((spec.batch, spec.num_q_heads, spec.head_dim), dtype=torch.float32, device="cuda")
+        self.stream = torch.cuda.current_stream()
+        d = self.dev
+        self.call = (d["q"], d["k"], d["v"], d["k_scales"], d["v_scales"], d["codebook"], d["sign"], d["bt"],
+                     d["lens"], self.out, self.p)
+
+    def step(self):
+        """One call of the public entry point: query rotation (codebook keys), partition kernel, reduce."""
+        import decode_attention_paged_gqa_gb300 as da
+
+        da.decode_attn_paged(*self.call, stream=self.stream)
+
+    def phased_step(self, ev):
+        """The same phases through their own entry points, with events around the partition
+        kernel (an event between two kernels stops the second from being scheduled during the
+        first's tail, so these steps time the dominant kernel, not the call)."""
+        import decode_attention_paged_gqa_gb300 as da
+
+        da.decode_attn_rotate_q(*self.call, stream=self.stream)
+        ev[0].record(self.stream)
+        da.decode_attn_partition(*self.call, stream=self.stream)
+        ev[1].record(self.stream)
+        da.decode_attn_reduce(*self.call, stream=self.stream)
+
+    def device_error(self):
+        import decode_attention_paged_gqa_gb300 as da
+
+        return da.decode_attn_get_device_error(self.p)
+
+    def time_calls(self, K, world=1):
+        """Device time of K back-to-back calls (CUDA events on the launching stream, barrier and
+        synchronize on both sides); ms per call, maxed over ranks."""
+        import torch
+
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize()
+        a.record(self.stream)
+        for _ in range(K):
+            self.step()
+        b.record(self.stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        return max_over_ranks(a.elapsed_time(b) / K, world)
+
+    def time_partition(self, K):
+        """Mean device time of the partition kernel over K phased calls (ms)."""
+        import torch
+
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        for k in range(K):
+            self.phased_step(evs[k])
+        torch.cuda.synchronize()
+        return statistics.mean(a.elapsed_time(b) for a, b in evs)
+
+
+def soak(prep, seconds):
+    """Untimed load so the clock samples bracket the timed region."""
+    import torch
+
+    end = time.time() + seconds
+    while time.time() < end:
+        for _ in range(20):
+            prep.step()
+        torch.cuda.synchronize()
+
+
+def cpu_baseline_entry(spec, prep, seconds, threads=0):
+    gbs, dt, n, thr, reps = oracle_sample(spec, prep.host, prep.src, seconds, threads=threads)
+    return {"value": gbs, "unit": UNIT, "cores": thr, "kind": "oracle",
+            "sample": f"first {n} of {spec.batch} sequences, all {spec.num_q_heads} heads, {reps} pass(es), "
+                      f"{dt:.1f} s"}
+
+
+def per_workload_entries(names, K, warmup, peak, local, with_cpu, cpu_seconds):
+    """The partition kernel and the whole call of each named workload, timed like the headline
+    (same K, warm-up, events), inside one clock-sampling window."""
+    import gc
+
+    import torch
+
+    import oracle
+    from decode_attention_paged_gqa_gb300 import workloads as wl
+
+    entries = {}
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.6)
+    clocks.mark_begin()
+    for name in names:
+        spec = wl.WORKLOADS[name]
+        prep = Prepared(spec)
+        for _ in range(max(3, warmup)):
+            prep.step()
+        torch.cuda.synchronize()
+        soak(prep, 0.3)
+        call_ms = prep.time_calls(K)
+        part_ms = prep.time_partition(K)
+        if prep.device_error():
+            raise SystemExit(f"device reported bad input on {name}")
+        kernel = partition_kernel(spec.kv_format)
+        gbs, part_gbs = prep.kv_bytes / (call_ms * 1e-3) / 1e9, prep.kv_bytes / (part_ms * 1e-3) / 1e9
+        e = {"kv_format": spec.kv_format, "us_per_call": call_ms * 1000, "value": gbs, "unit": UNIT,
+             "pct_of_hbm_peak": 100 * gbs / peak, "algorithmic_kv_bytes": prep.kv_bytes,
+             "roofline": {"bound": "hbm", "kernel": kernel, "achieved": part_gbs, "peak": peak, "unit": "GB/s",
+                          "frac": part_gbs / peak, "partition_us": part_ms * 1000,
+                          "traffic": recorded_traffic(kernel, spec.name)},
+             "gpu_launches": K * KERNELS_PER_CALL[spec.kv_format]}
+        if prep.cache_bytes <= L2_BYTES:
+            e["note"] = "L2-resident and latency-bound: not compared with the HBM peak"
+        if with_cpu and spec.name == "tiny_bf16":
+            oracle.build()
+            e["cpu_baseline"] = {"all_cores": cpu_baseline_entry(spec, prep, cpu_seconds),
+                                 "one_core": cpu_baseline_entry(spec, prep, cpu_seconds, threads=1)}
+        entries[name] = e
+        del prep
+        gc.collect()
+        torch.cuda.empty_cache()
+    clocks.mark_end()
+    clk = clocks.stop()
+    for e in entries.values():
+        e["clocks"] = clk
+    return entries
+
+
 def main():
     args = parse_args()
     from decode_attention_paged_gqa_gb300 import workloads as wl
@@ -351,107 +512,55 @@ def main():
         reference_arm(args, spec, rank, world)
         return
 
-    import numpy as np
     import torch
 
     import decode_attention_paged_gqa_gb300 as da
     from decode_attention_paged_gqa_gb300 import build as lib_build
-    from decode_attention_paged_gqa_gb300.metrics import algorithmic_kv_bytes
 
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA GPU (the product path has no CPU fallback)")
     lib_build.build()
     torch.cuda.set_device(local)
-    lay, host, src = build_inputs(spec)
-    dev = {k: (None if t is None else t.cuda()) for k, t in host.items()}
-    kv_bytes = algorithmic_kv_bytes(lay.context_lens, spec.window, spec.num_kv_heads, spec.kv_format, spec.head_dim)
-    cache_bytes = host["k"].numel() * host["k"].element_size() * 2
-    p = da.make_params(batch=spec.batch, num_q_heads=spec.num_q_heads, num_kv_heads=spec.num_kv_heads,
-                       head_dim=spec.head_dim, num_blocks=lay.num_blocks, max_blocks_per_seq=lay.block_tables.shape[1],
-                       max_context_len=spec.ctx_max, kv_format=spec.kv_format, softmax_scale=spec.scale,
-                       softcap=spec.softcap, window=spec.window, partition_size=spec.partition_size,
-                       split_threshold=spec.split_threshold)
-    ws = torch.empty(da.decode_attn_workspace_bytes(p), dtype=torch.uint8, device="cuda")
-    da.attach_workspace(p, ws)
-    da.decode_attn_workspace_init(p)
-    out = torch.empty((spec.batch, spec.num_q_heads, spec.head_dim), dtype=torch.float32, device="cuda")
-    stream = torch.cuda.current_stream()
-    call = (dev["q"], dev["k"], dev["v"], dev["k_scales"], dev["v_scales"], dev["codebook"], dev["sign"], dev["bt"],
-            dev["lens"], out, p)
-    # kernels per step: the partition kernel and the reduce, plus the query rotation for
-    # formats whose keys are stored on the rotated basis
-    kernels_per_step = {"bf16": 2, "fp8": 2, "cb4": 3, "fp8k_cb4v": 2, "cb3k_cb4v": 3}[spec.kv_format]
-
-    def step():
-        # one call of the public entry point: query rotation (codebook keys), partition kernel, reduce
-        da.decode_attn_paged(*call, stream=stream)
-
-    def phased_step(ev):
-        # the same phases through their own entry points, with events around the partition kernel
-        # (an event between two kernels stops the second from being scheduled during the first's
-        # tail, so these steps time the dominant kernel, not the call)
-        da.decode_attn_rotate_q(*call, stream=stream)
-        ev[0].record(stream)
-        da.decode_attn_partition(*call, stream=stream)
-        ev[1].record(stream)
-        da.decode_attn_reduce(*call, stream=stream)
-
+    prep = Prepared(spec)
     for _ in range(max(3, args.warmup)):
-        step()
+        prep.step()
     torch.cuda.synchronize()
-    if da.decode_attn_get_device_error(p):
+    if prep.device_error():
         raise SystemExit("device reported bad input during warm-up")
 
     clocks = None if args.no_clocks else ClockSampler(local)
     if clocks:
         clocks.start()
         time.sleep(0.6)  # nvidia-smi start-up
-        soak_end = time.time() + 1.0
         clocks.mark_begin()
-        while time.time() < soak_end:  # untimed load so the clock samples bracket the timed region
-            for _ in range(20):
-                step()
-            torch.cuda.synchronize()
+        soak(prep, 1.0)
     K = args.steps
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(world)
-    torch.cuda.synchronize()
-    t_start.record(stream)
-    for k in range(K):
-        step()
-    t_end.record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
+    step_ms = prep.time_calls(K, world)
     # the partition kernel's duration: a second pass of K steps, right after the timed one
-    for k in range(K):
-        phased_step(evs[k])
-    torch.cuda.synchronize()
+    part_ms = prep.time_partition(K)
     clk = None
     if clocks:
         time.sleep(0.3)
         clocks.mark_end()
         clk = clocks.stop()
-    step_ms = max_over_ranks(t_start.elapsed_time(t_end) / K, world)
-    part_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
-    if da.decode_attn_get_device_error(p):
+    if prep.device_error():
         raise SystemExit("device reported bad input during the timed steps")
 
     # end to end through decode_attn_paged with host buffers: every step copies all inputs
     # from pinned host memory and reads the output back
     e2e = None
     if not args.no_e2e:
-        pin = {k: (None if t is None else t.pin_memory()) for k, t in host.items()}
-        out_h = torch.empty(out.shape, dtype=torch.float32).pin_memory()
+        pin = {k: (None if t is None else t.pin_memory()) for k, t in prep.host.items()}
+        out_h = torch.empty(prep.out.shape, dtype=torch.float32).pin_memory()
         h2d = sum(t.numel() * t.element_size() for t in pin.values() if t is not None)
         d2h = out_h.numel() * 4
 
         def e2e_step():
             for k2, t in pin.items():
                 if t is not None:
-                    dev[k2].copy_(t, non_blocking=True)
-            da.decode_attn_paged(*call, stream=stream)
-            out_h.copy_(out, non_blocking=True)
+                    prep.dev[k2].copy_(t, non_blocking=True)
+            da.decode_attn_paged(*prep.call, stream=prep.stream)
+            out_h.copy_(prep.out, non_blocking=True)
 
         for _ in range(2):
             e2e_step()
@@ -459,16 +568,17 @@ def main():
         Ke = max(3, min(K, 20))
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         barrier(world)
-        a.record(stream)
+        a.record(prep.stream)
         for _ in range(Ke):
             e2e_step()
-        b.record(stream)
+        b.record(prep.stream)
         torch.cuda.synchronize()
         e2e_ms = max_over_ranks(a.elapsed_time(b) / Ke, world)
-        e2e = {"value": world * kv_bytes / (e2e_ms * 1e-3) / 1e9, "unit": UNIT, "ms_per_step": e2e_ms,
+        e2e = {"value": world * prep.kv_bytes / (e2e_ms * 1e-3) / 1e9, "unit": UNIT, "ms_per_step": e2e_ms,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
     peak, peak_src = hbm_peak()
+    kv_bytes, cache_bytes = prep.kv_bytes, prep.cache_bytes
     gbs = world * kv_bytes / (step_ms * 1e-3) / 1e9
     part_gbs = kv_bytes / (part_ms * 1e-3) / 1e9
     kernel = partition_kernel(spec.kv_format)
@@ -478,10 +588,16 @@ def main():
         import oracle
 
         oracle.build()
-        cgbs, cdt, cn, cthr, creps = oracle_sample(spec, host, src, args.cpu_seconds)
-        cpu = {"value": cgbs, "unit": UNIT, "cores": cthr, "kind": "oracle",
-               "sample": f"first {cn} of {spec.batch} sequences, all {spec.num_q_heads} heads, "
-                         f"{creps} pass(es), {cdt:.1f} s"}
+        cpu = cpu_baseline_entry(spec, prep, args.cpu_seconds)
+        if spec.name == "tiny_bf16":  # the tiny batch is also timed on one core
+            cpu["one_core"] = cpu_baseline_entry(spec, prep, args.cpu_seconds, threads=1)
+    per_workload = None
+    if world == 1 and not args.no_per_workload:
+        names = [n for n in EXTRA_WORKLOADS if n != spec.name]
+        del prep
+        torch.cuda.empty_cache()
+        per_workload = per_workload_entries(names, K, args.warmup, peak, local, not args.no_cpu_baseline,
+                                            min(args.cpu_seconds, 3.0))
     line = {
         "metric": METRIC, "value": gbs, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": step_ms, "us_per_call": step_ms * 1000, "pct_of_hbm_peak": 100 * gbs / world / peak,
@@ -499,8 +615,9 @@ def main():
                      "partition_us": part_ms * 1000, "bytes_per_launch": kv_bytes},
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": K * kernels_per_step,
+        "gpu_launches": K * KERNELS_PER_CALL[spec.kv_format],
         "clocks": clk,
+        "per_workload": per_workload,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -176,6 +176,11 @@ cudaError_t ensure_dynamic_smem(Kernel kern, size_t bytes, DeviceFlags& done) {
   return e;
 }
 
+// The host-side checks of a call's parameters and tensors, without the workspace (the same
+// checks and status codes as decode_attn_paged; decode_attn.cu).
+int check_call(const void* q, const void* k, const void* v, const float* ks, const float* vs, const float* cb,
+               const float* sign, const int32_t* bt, const int32_t* lens, const float* out, const da_params* p);
+
 // The checked launch sequence behind decode_attn_paged and its phases (decode_attn.cu).
 enum Phase { kRotate = 1, kPartition = 2, kReduce = 4, kAll = 7 };
 int run_phases(int phases, const void* q, const void* k, const void* v, const float* ks, const float* vs,

@@ -117,6 +117,12 @@ Args make_args(const void* q, const void* k, const void* v, const float* ks, con
 
 namespace da {
 
+int check_call(const void* q, const void* k, const void* v, const float* ks, const float* vs, const float* cb,
+               const float* sign, const int32_t* bt, const int32_t* lens, const float* out, const da_params* p) {
+  const int rc = check_params(p);
+  return rc ? rc : check_tensors(q, k, v, ks, vs, cb, sign, bt, lens, out, p);
+}
+
 int run_phases(int phases, const void* q, const void* k, const void* v, const float* ks, const float* vs,
                const float* cb, const float* sign, const int32_t* bt, const int32_t* lens, float* out,
                const da_params* p, void* stream) {

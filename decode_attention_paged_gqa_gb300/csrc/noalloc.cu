@@ -8,7 +8,9 @@
 // with no CUDA allocator of its own at all. This entry point takes the workspace from a
 // fixed-size array in device global memory that the library itself defines; it allocates
 // nothing and calls no allocating routine.
+#include <cuda.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include <cstddef>
 #include <cstdint>
@@ -25,19 +27,42 @@ constexpr size_t kStaticWorkspaceBytes = size_t(64) << 20;
 
 __device__ __align__(256) unsigned char g_static_workspace[kStaticWorkspaceBytes];
 
-// Device address of g_static_workspace, looked up once per device. In host code the
-// array's name is only a host-side stand-in, never a device address.
+// Device address of g_static_workspace, looked up once per device and context. In host code
+// the array's name is only a host-side stand-in, never a device address. The address belongs
+// to the context it was looked up in: when the device's current context changes (the primary
+// context destroyed by cudaDeviceReset and created anew, or another context made current
+// through the driver API), it is looked up again.
 std::mutex g_mu;
 void* g_addr[64] = {};
+CUcontext g_ctx[64] = {};
+
+PFN_cuCtxGetCurrent_v4000 ctx_get_current_fn() {
+  static PFN_cuCtxGetCurrent_v4000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(f);
+  });
+  return fn;
+}
 
 int static_workspace_address(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return DA_ERR_CUDA;
+  auto get_ctx = ctx_get_current_fn();
+  CUcontext ctx = nullptr;  // stays null while the runtime has made no context current yet
+  if (!get_ctx || get_ctx(&ctx) != CUDA_SUCCESS) return DA_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_addr[dev]) {
+  if (!ctx || !g_addr[dev] || g_ctx[dev] != ctx) {
+    // the lookup also makes the device's primary context current when none is
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_static_workspace) != cudaSuccess || !p) return DA_ERR_CUDA;
+    if (get_ctx(&ctx) != CUDA_SUCCESS || !ctx) return DA_ERR_CUDA;
     g_addr[dev] = p;
+    g_ctx[dev] = ctx;
   }
   *out = g_addr[dev];
   return DA_OK;
@@ -50,13 +75,14 @@ extern "C" int decode_attn_paged_static_workspace(const void* q, const void* k_c
                                                   const float* codebook, const float* sign_pattern,
                                                   const int32_t* block_tables, const int32_t* context_lens,
                                                   float* out, const da_params* p, void* stream) {
-  if (!p) return DA_ERR_INVALID_ARG;
-  const size_t need = decode_attn_workspace_bytes(p);
-  if (need == 0) return DA_ERR_INVALID_ARG;
-  if (need > kStaticWorkspaceBytes) return DA_ERR_STATIC_WORKSPACE;
-  void* ws = nullptr;
-  int rc = static_workspace_address(&ws);
+  // the checks of decode_attn_paged, with its status codes, before anything is enqueued
+  int rc = da::check_call(q, k_cache, v_cache, k_scales, v_scales, codebook, sign_pattern, block_tables,
+                          context_lens, out, p);
   if (rc) return rc;
+  if (p->batch == 0) return DA_OK;
+  if (da::workspace_layout(*p).total > kStaticWorkspaceBytes) return DA_ERR_STATIC_WORKSPACE;
+  void* ws = nullptr;
+  if ((rc = static_workspace_address(&ws))) return rc;
   da_params local = *p;
   local.workspace = ws;
   local.workspace_bytes = kStaticWorkspaceBytes;

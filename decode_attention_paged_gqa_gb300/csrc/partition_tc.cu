@@ -502,8 +502,11 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 3 : 2)
 
   if (stalled) {
     if (lane == 0) atomicOr(a.err, DA_DEVERR_TIMEOUT);
-    // give the copies still in flight into this warp's stages a bounded chance to land
-    for (unsigned k = stall_from; k < issued; ++k) ptx::mbar_wait(bar0 + 8 * (k % T::kStages), (k / T::kStages) & 1);
+    // give the copies still in flight into this warp's stages a bounded chance to land (one
+    // time limit shared by all of them)
+    uint64_t deadline = 0;
+    for (unsigned k = stall_from; k < issued; ++k)
+      ptx::mbar_wait_until(bar0 + 8 * (k % T::kStages), (k / T::kStages) & 1, deadline);
   }
 }
 

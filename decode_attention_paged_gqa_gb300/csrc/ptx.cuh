@@ -46,13 +46,35 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait for the phase with the given parity to complete. Each try_wait blocks for
-// a hardware-defined slice of time; the bound makes the whole wait end after seconds at
-// most. Returns false when the bound ran out.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  for (uint32_t it = 0; it < (1u << 22); ++it)
+// Nanoseconds of the GPU's global timer.
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Longest time a warp waits for its page copies before it gives up: copies land within
+// microseconds, so 200 ms only runs out when a copy never completes.
+constexpr uint64_t kWaitLimitNs = 200ull * 1000 * 1000;
+
+// Bounded wait for the phase with the given parity to complete. The first try_wait is the
+// fast path; after it the wait runs until `deadline` (global-timer ns; 0 = not set yet, then
+// set to now + kWaitLimitNs and kept by the caller, so consecutive waits of a drain share one
+// limit). Returns false when the deadline passed.
+__device__ __forceinline__ bool mbar_wait_until(uint32_t bar, uint32_t parity, uint64_t& deadline) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t now = global_ns();
+  if (deadline == 0) deadline = now + kWaitLimitNs;
+  for (;;) {
     if (mbar_try_wait(bar, parity)) return true;
-  return false;
+    if (global_ns() > deadline) return false;
+  }
+}
+
+// The same with a limit of its own: returns false after kWaitLimitNs without completion.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  uint64_t deadline = 0;
+  return mbar_wait_until(bar, parity, deadline);
 }
 
 // ---------------------------------------------------------------- TMA

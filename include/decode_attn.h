@@ -89,7 +89,7 @@ enum da_status {
 /* Bits of the device error word (decode_attn_get_device_error). */
 #define DA_DEVERR_BLOCK_ID 0x1u    /* a block-table entry used by the call was outside [0, num_blocks) */
 #define DA_DEVERR_CONTEXT_LEN 0x2u /* a context length was < 0 or above the limits in the header comment */
-#define DA_DEVERR_TIMEOUT 0x4u     /* a wait for a page copy gave up after its iteration bound (never expected) */
+#define DA_DEVERR_TIMEOUT 0x4u     /* a wait for a page copy gave up after 200 ms (never expected) */
 
 typedef struct da_params {
   int32_t batch;              /* B >= 0 sequences (B == 0: nothing to do) */
@@ -195,17 +195,19 @@ int decode_attn_reduce(const void* q, const void* k_cache, const void* v_cache, 
  * the allocator (cudaMalloc can synchronise the device and take unbounded time), or a caller
  * with no CUDA allocator of its own. (This entry point has no counterpart in the pages; it is
  * an addition of this library.)
- * Same arguments and results as decode_attn_paged, except that p->workspace and
- * p->workspace_bytes are ignored: the workspace is a fixed 64 MiB array in device global
- * memory defined by the library (every GPU that loads the library holds it until the process
- * exits). Calls whose decode_attn_workspace_bytes(p) exceeds 64 MiB return
- * DA_ERR_STATIC_WORKSPACE and enqueue nothing. Nothing is allocated and no allocating
- * routine is called; each call clears the array's error word on `stream` first.
+ * Same arguments, argument checks, status codes and results as decode_attn_paged, except
+ * that p->workspace and p->workspace_bytes are ignored: the workspace is a fixed 64 MiB array
+ * in device global memory defined by the library (every GPU that loads the library holds it
+ * until the process exits). A call that passes decode_attn_paged's checks but whose
+ * decode_attn_workspace_bytes(p) exceeds 64 MiB returns DA_ERR_STATIC_WORKSPACE. A rejected
+ * call has enqueued nothing. Nothing is allocated and no allocating routine is called; each
+ * accepted call clears the array's error word on `stream` first.
  * All calls share the one array: calls that overlap on the GPU (on different streams, or
  * from different host threads) race on it and must be serialised by the caller. The
  * device-side bad-input bits of these calls are not reported.
- * The first call on each device looks up the array's device address (cudaGetSymbolAddress,
- * with that device current); make that first call before any stream capture. */
+ * The first call on each device, and the first after the device's current context changed
+ * (e.g. after cudaDeviceReset), looks up the array's device address (cudaGetSymbolAddress,
+ * with that device current); make that call before any stream capture. */
 int decode_attn_paged_static_workspace(const void* q, const void* k_cache, const void* v_cache,
                                        const float* k_scales, const float* v_scales, const float* codebook,
                                        const float* sign_pattern, const int32_t* block_tables,

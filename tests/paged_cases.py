@@ -119,14 +119,3 @@ def assert_close(gpu: np.ndarray, ref: np.ndarray, what: str = ""):
     rel = float(np.linalg.norm(diff)) / nref if nref > 0 else float(np.linalg.norm(diff))
     assert max_abs <= MAX_ABS and rel <= REL_L2, f"{what}: max_abs={max_abs:.3e} rel_l2={rel:.3e}"
     return max_abs, rel
-
-
-def sample_heads(spec: wl.WorkloadSpec, lens: np.ndarray, n: int, seed: int = 0):
-    """(b, h) pairs to check at full size: the shortest and longest sequences, the first and
-    last sequence and head, and seeded random ones."""
-    rng = np.random.default_rng(seed)
-    B, Hq = spec.batch, spec.num_q_heads
-    picks = {(0, 0), (B - 1, Hq - 1), (int(np.argmin(lens)), Hq // 2), (int(np.argmax(lens)), 1 % Hq)}
-    while len(picks) < n:
-        picks.add((int(rng.integers(B)), int(rng.integers(Hq))))
-    return sorted(picks)

@@ -80,6 +80,32 @@ def test_bad_params_are_rejected(kw, status):
     assert e.value.status == status
 
 
+@pytest.mark.parametrize("kw", [dict(head_dim=96), dict(num_q_heads=24, num_kv_heads=2), dict(block_size=32),
+                                dict(max_context_len=1 << 30), dict(num_q_heads=30), dict(kv_format=7),
+                                dict(softcap=-1.0), dict(query_len=9)])
+def test_static_workspace_entry_returns_the_same_status(kw):
+    """decode_attn_paged_static_workspace runs decode_attn_paged's checks first, so a rejected
+    configuration gets the same status code from both entry points (and neither enqueues
+    anything, so no GPU is needed)."""
+    p = base(**kw)
+    args = (256, 256, 256, None, None, None, None, 256, 256, 256, p)
+    statuses = []
+    for fn in (da.decode_attn_paged, da.decode_attn_paged_static_workspace):
+        with pytest.raises(da.DecodeAttnError) as e:
+            fn(*args, stream=0)
+        statuses.append(e.value.status)
+    assert statuses[0] == statuses[1] != da._binding.DA_ERR_WORKSPACE
+
+
+def test_static_workspace_entry_checks_tensors_first():
+    p = base()
+    with pytest.raises(da.DecodeAttnError) as e:  # a NULL query: rejected before the array is touched
+        da.decode_attn_paged_static_workspace(None, 256, 256, None, None, None, None, 256, 256, 256, p, stream=0)
+    assert e.value.status == da._binding.DA_ERR_INVALID_ARG
+    p = base(batch=0)  # nothing to do: returns at once, no CUDA call made
+    da.decode_attn_paged_static_workspace(256, 256, 256, None, None, None, None, 256, 256, 256, p, stream=0)
+
+
 def test_workspace_checks():
     p = base()
     with pytest.raises(da.DecodeAttnError) as e:  # no workspace

@@ -27,27 +27,65 @@ def _built():
     build.build()
 
 
-def static_call(c):
+def static_call(c, out=None, dev=None):
     s = c["spec"]
-    dev = to_device(c)
+    dev = dev or to_device(c)
     p = params_for(c)  # no workspace attached: the entry point uses the library's own array
-    out = torch.full((s.batch, s.num_q_heads, s.head_dim), float("nan"), dtype=torch.float32, device="cuda")
+    if out is None:
+        out = torch.full(tuple(c["q"].shape), float("nan"), dtype=torch.float32, device="cuda")
     da.decode_attn_paged_static_workspace(dev["q"], dev["k"], dev["v"], dev["k_scales"], dev["v_scales"],
                                           dev["codebook"], dev["sign"], dev["bt"], dev["lens"], out, p)
     torch.cuda.synchronize()
     return out.cpu().numpy()
 
 
-@pytest.mark.parametrize("fmt", ["bf16", "cb4"])
-def test_static_workspace_matches_caller_workspace_twice(fmt):
+CASES = {
     # split and unsplit sequences, so the partials in the array are written and read
-    first = make_case(wl.WorkloadSpec("noalloc1", 4, 32, 8, 128, fmt, 300, 3000, seed=21))
-    second = make_case(wl.WorkloadSpec("noalloc2", 3, 16, 8, 128, fmt, 1000, 5000, seed=22))
-    for c in (first, second):
+    "bf16": [dict(batch=4, hq=32, hkv=8, lo=300, hi=3000, seed=21), dict(batch=3, hq=16, hkv=8, lo=1000, hi=5000,
+                                                                         seed=22)],
+    "cb4": [dict(batch=4, hq=32, hkv=8, lo=300, hi=3000, seed=21), dict(batch=3, hq=16, hkv=8, lo=1000, hi=5000,
+                                                                        seed=22)],
+    # FP8: the reduce applies the per-tensor value scale
+    "fp8": [dict(batch=4, hq=32, hkv=8, lo=300, hi=3000, seed=23), dict(batch=2, hq=8, hkv=2, lo=1500, hi=4000,
+                                                                        seed=24)],
+    # a sliding window with softcap, and two query tokens per sequence (multi-token decode)
+    "bf16_window_softcap": [dict(batch=3, hq=16, hkv=8, lo=2000, hi=6000, seed=25, window=1500, softcap=30.0),
+                            dict(batch=2, hq=8, hkv=4, lo=700, hi=3000, seed=26, window=1000, softcap=50.0)],
+    "cb4_two_tokens": [dict(batch=3, hq=8, hkv=4, lo=300, hi=3000, seed=27, query_len=2),
+                       dict(batch=2, hq=8, hkv=4, lo=1000, hi=2500, seed=28, query_len=2)],
+}
+
+
+def spec_for(name, fmt, d):
+    return wl.WorkloadSpec(name, d["batch"], d["hq"], d["hkv"], 128, fmt, d["lo"], d["hi"], seed=d["seed"],
+                           window=d.get("window", 0), softcap=d.get("softcap", 0.0), query_len=d.get("query_len", 1))
+
+
+@pytest.mark.parametrize("case", sorted(CASES))
+def test_static_workspace_matches_caller_workspace_twice(case):
+    fmt = case.split("_")[0]
+    for i, d in enumerate(CASES[case]):
+        c = make_case(spec_for(f"noalloc_{case}_{i}", fmt, d))
         ref = run_gpu(c)
         got = static_call(c)
-        max_abs, rel = assert_close(got, ref, f"{fmt} static vs caller workspace")
+        max_abs, rel = assert_close(got, ref, f"{case} call {i}: static vs caller workspace")
         assert max_abs <= MAX_ABS and rel <= REL_L2
+
+
+def test_static_workspace_call_allocates_nothing():
+    """After a first (warm) call, a call through the static workspace leaves both torch's
+    allocator and the device's free memory unchanged."""
+    c = make_case(spec_for("noalloc_mem", "cb4", CASES["cb4"][1]))
+    dev = to_device(c)
+    out = torch.empty(tuple(c["q"].shape), dtype=torch.float32, device="cuda")
+    first = static_call(c, out=out, dev=dev)
+    torch.cuda.synchronize()
+    allocated, free = torch.cuda.memory_allocated(), torch.cuda.mem_get_info()[0]
+    second = static_call(c, out=out, dev=dev)
+    torch.cuda.synchronize()
+    assert torch.cuda.memory_allocated() == allocated
+    assert torch.cuda.mem_get_info()[0] == free
+    assert np.array_equal(first, second)
 
 
 def test_too_large_a_call_is_rejected():

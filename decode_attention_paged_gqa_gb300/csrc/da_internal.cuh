@@ -18,6 +18,7 @@ namespace da {
 
 constexpr int kBlockSize = 16;      // tokens per page (the only page size built)
 constexpr int kMaxPartitions = 8192;
+constexpr int kMaxColumns = 32;     // most (query token, head) pairs of one kv head: T * G
 
 // Everything a kernel needs, passed by value (no pointers into host memory).
 struct Args {
@@ -37,6 +38,11 @@ struct Args {
   int window, psize, thresh;
   int P;                      // partitions the grid and the workspace are sized for
   int ppc;                    // partitions a partition-kernel CTA walks (set by its launcher)
+  int ncg;                    // column groups: CTAs per partition chunk, each taking 8 of the T * G
+                              // (query token, head) pairs when there are more than 8 (else 1)
+  int ksub;                   // partials per partition: sub-items a partition's pages are dealt to
+                              // by the codebook-value kernel when the batch has few partitions (a
+                              // power of two <= 8; always 1 for the BF16 / FP8 kernel)
   uint32_t lut_stride;        // 128: entry stride of the codebook kernel's lookup tables (bytes)
   int schedule;               // da_params.partition_schedule (0 automatic, 1 shared, 2 owned)
   // Paired copies (set by a partition kernel's launcher): one 3-D tensor map spans both the K
@@ -49,9 +55,9 @@ struct Args {
   // workspace pieces
   uint32_t* err;              // device error word (DA_DEVERR_* bits)
   float* q_rot;               // [B][T][Hq][D] (formats whose keys are on the rotated basis)
-  float* part_o;              // [B][T][Hq][P][D], unnormalised partial outputs
-  float* part_m;              // [B][T][Hq][P], running max in log2 units
-  float* part_l;              // [B][T][Hq][P], running sum of 2^(s - m)
+  float* part_o;              // [B][T][Hq][P * ksub][D], unnormalised partial outputs
+  float* part_m;              // [B][T][Hq][P * ksub], running max in log2 units
+  float* part_l;              // [B][T][Hq][P * ksub], running sum of 2^(s - m)
 };
 
 // First position attended by a query token at position `pos`: with a window of W tokens,
@@ -119,6 +125,15 @@ __device__ __forceinline__ int load_block(const Args& a, int b, int page) {
   return phys;
 }
 
+// Row of out and of the partials ([B][T][Hq] flattened) for virtual head vh = (query token) * G +
+// (head within the group) of kv head g of sequence b.
+__host__ __device__ __forceinline__ size_t query_row(const Args& a, int b, int g, int G, int vh) {
+  return ((size_t)b * a.T + vh / G) * a.Hq + (size_t)g * G + vh % G;
+}
+
+// Column groups of a partition kernel: one when the T * G pairs fit one 8-column MMA tile.
+__host__ __device__ __forceinline__ int column_groups(int T, int G) { return T * G > 8 ? (T * G + 7) / 8 : 1; }
+
 __device__ __forceinline__ float bf16_to_f32(uint16_t h) { return __uint_as_float((uint32_t)h << 16); }
 
 // Workspace layout; every piece starts on a 256-byte boundary.
@@ -138,10 +153,29 @@ inline int host_max_partitions(const da_params& p) {
   return np < 1 ? 1 : np;
 }
 
+// Partials per partition (Args::ksub): 1 for the BF16 / FP8 formats and when each warp is to
+// own whole partitions (partition_schedule 2); else the smallest power of two (<= 8) that
+// gives the batch at least kTargetItems items, at least 2 when the partitions are to be
+// shared (partition_schedule 1), within kMaxPartitions partials per row. Depends on the
+// parameters only, so the workspace size does too.
+constexpr long long kTargetItems = 8192;
+constexpr int kMaxKsub = 8;
+inline int sub_items(const da_params& p) {
+  if (p.kv_format == DA_KV_BF16 || p.kv_format == DA_KV_FP8_E4M3 || p.partition_schedule == 2) return 1;
+  const int P = host_max_partitions(p);
+  const long long units = (long long)p.batch * p.num_kv_heads * P *
+                          column_groups(query_len(p), p.num_q_heads / p.num_kv_heads);
+  int k = 1;
+  while (k < kMaxKsub && units * k < kTargetItems) k *= 2;
+  if (p.partition_schedule == 1 && k < 2) k = 2;
+  while (k > 1 && (long long)P * k > kMaxPartitions) k /= 2;
+  return k;
+}
+
 inline Layout workspace_layout(const da_params& p) {
   Layout l{};
   const size_t BH = (size_t)p.batch * query_len(p) * p.num_q_heads;
-  const size_t P = (size_t)host_max_partitions(p);
+  const size_t P = (size_t)host_max_partitions(p) * sub_items(p);
   size_t off = 0;
   l.err = off;
   off = align256(off + sizeof(uint32_t));
@@ -201,7 +235,7 @@ inline int partitions_per_cta(const Args& a, int per_sm, int* cached_sms) {
     cached_sms[dev] = sms;
   }
   if (a.ppc_req > 0) return a.ppc_req;
-  const long long units = (long long)a.P * a.Hkv * a.B;
+  const long long units = (long long)a.P * a.Hkv * a.B * a.ncg;
   const long long waves = units / (8ll * cached_sms[dev] * (per_sm > 0 ? per_sm : 1));
   return waves < 1 ? 1 : (waves > 8 ? 8 : (int)waves);
 }
@@ -220,7 +254,7 @@ inline bool warps_own_partitions(const Args& a, int per_sm, int warps_per_cta, i
   if (a.schedule == 2) return true;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || cached_sms[dev] <= 0) return false;
-  const long long units = (long long)a.P * a.Hkv * a.B;
+  const long long units = (long long)a.P * a.Hkv * a.B * a.ncg;
   return 2ll * units >= (long long)min_fill_x2 * cached_sms[dev] * (per_sm > 0 ? per_sm : 1) * warps_per_cta;
 }
 

@@ -32,13 +32,17 @@ int check_params(const da_params* p) {
   if (p->kv_format < DA_KV_BF16 || p->kv_format > DA_KV_CB3K_CB4V) return DA_ERR_INVALID_ARG;
   const int G = p->num_q_heads / p->num_kv_heads;
   if (G != 1 && G != 2 && G != 4 && G != 8) return DA_ERR_UNSUPPORTED;
-  if ((long long)query_len(*p) * G > 8) return DA_ERR_UNSUPPORTED;  // query tokens x group heads per tile
+  if ((long long)query_len(*p) * G > kMaxColumns) return DA_ERR_UNSUPPORTED;  // (query token, head) pairs
   if (p->head_dim != 128 && p->head_dim != 256) return DA_ERR_UNSUPPORTED;
   if (p->block_size != kBlockSize) return DA_ERR_UNSUPPORTED;
   if ((long long)p->batch * query_len(*p) > 65535 || p->num_kv_heads > 65535 || p->num_q_heads > 65535)
     return DA_ERR_UNSUPPORTED;
   if (host_max_partitions(*p) > kMaxPartitions) return DA_ERR_UNSUPPORTED;
   if ((long long)p->num_blocks * p->num_kv_heads * p->block_size >= (1ll << 31)) return DA_ERR_UNSUPPORTED;
+  // the partition kernels index their work items with 32-bit integers
+  if ((long long)p->batch * p->num_kv_heads * host_max_partitions(*p) * column_groups(query_len(*p), G) *
+          kMaxKsub >= (1ll << 31))
+    return DA_ERR_UNSUPPORTED;
   return DA_OK;
 }
 
@@ -97,6 +101,8 @@ Args make_args(const void* q, const void* k, const void* v, const float* ks, con
   a.thresh = p->split_threshold;
   a.P = host_max_partitions(*p);
   a.ppc = 1;
+  a.ncg = column_groups(a.T, a.Hq / a.Hkv);
+  a.ksub = sub_items(*p);
   a.lut_stride = 128;
   a.alibi = p->alibi_slopes;
   a.schedule = p->partition_schedule;

@@ -7,6 +7,12 @@
 // ahead of the compute side with IssueCursor, across partition boundaries, so the next
 // partition's pages are already in flight while a partition is finished; the compute side
 // walks the same list with the same counts (warp_pages).
+//
+// When warps own partitions, odd partitions are walked from their last page down. A partition
+// that does not start on a page boundary (a window start) shares its first page with the end
+// of the partition before it; with alternating directions the two warps that need such a page
+// reach it at about the same time (both at the start, or both at the end, of their partitions),
+// so the second read is served by L2 instead of a second read from DRAM.
 #pragma once
 
 #include "da_internal.cuh"
@@ -17,6 +23,15 @@ constexpr int kPageTokens = 16;
 
 // Pages of a partition that warp w of W handles.
 __device__ __forceinline__ int warp_pages(int npages, int w, int W) { return npages > w ? (npages - w + W - 1) / W : 0; }
+
+// Index, within a partition's pages, of the k-th page of the warp's walk (n: the warp's page
+// count there): pages page_off, page_off + page_step, ..., in reverse order when `rev`.
+__device__ __forceinline__ int walk_page(int k, int n, int page_off, int page_step, bool rev) {
+  return page_off + page_step * (rev ? n - 1 - k : k);
+}
+
+// Whether a warp walks partition p from its last page down (odd partitions, owned schedule).
+__device__ __forceinline__ bool walk_reversed(bool owner, int p) { return owner && (p & 1); }
 
 // First page and page count of a non-empty token range.
 __device__ __forceinline__ void range_pages(const Range& r, int& first, int& npages) {
@@ -35,10 +50,11 @@ struct IssueCursor {
   int first;              // first page of partition p
   int bid;                // lane l: physical block of the warp's page (i & ~31) + l of partition p (-1 if none)
   bool more;              // a page is left at the cursor
+  bool owner, rev;        // warps own partitions; partition p is walked in reverse
 
   __device__ __forceinline__ void load_bids(const Args& a) {
     const int k = (i & ~31) + lane;
-    bid = k < n ? load_block(a, b, first + page_off + page_step * k) : -1;
+    bid = k < n ? load_block(a, b, first + walk_page(k, n, page_off, page_step, rev)) : -1;
   }
   // Moves to the next of the warp's partitions that has pages for it (the first one when
   // p < p0 on entry).
@@ -49,6 +65,7 @@ struct IssueCursor {
       range_pages(partition_range(L, a.T, p, a.window, a.psize, a.thresh), first, npages);
       n = warp_pages(npages, page_off, page_step);
       i = 0;
+      rev = walk_reversed(owner, p);
       if (n > 0) {
         more = true;
         load_bids(a);
@@ -66,6 +83,7 @@ struct IssueCursor {
     p_end = p_end_;
     page_off = page_off_;
     page_step = page_step_;
+    owner = page_step_ == 1;  // a warp that takes every page of its partitions owns them
     next_partition(a);
   }
   // Physical block (-1: bad block id, nothing to load) of the page at the cursor, the same

@@ -3,33 +3,38 @@
 // 4-bit V, 3-bit K + 4-bit V. Tensor-core MMAs on operands dequantised through a shared-
 // memory lookup table.
 //
-// A CTA of four or eight warps takes consecutive partitions of one (sequence, kv head). With
-// the owned schedule (chosen when there are partitions enough) each warp owns whole
-// partitions (p_begin + w, p_begin + w + W, ...), so it writes its partition's partial itself
-// and no warp waits for another after the tables are built; with the shared schedule the
-// warps deal each partition's pages round-robin and merge at its end. Each warp runs its own
-// pipeline of shared-memory stages filled by TMA / bulk copies (a page's K codes, V codes and
-// their per-token norms) and signalled on an mbarrier, continuing across its partitions. Per page a warp computes, in the rotated basis (the keys' and values' own
-// basis, no dequantisation to the original one):
+// A persistent kernel: one CTA per SM (16 warps at D = 128 with up to four columns, else 8)
+// builds the lookup tables once, then every warp walks its share of the call's flattened item
+// list (item_walk.cuh: one item per (sequence, kv head, partition, column group, sub-item);
+// warp gw takes items gw, gw + N, ...), so the load is balanced whatever the context lengths
+// and no warp ever waits for another. Each warp runs its own pipeline of shared-memory stages
+// filled by TMA / bulk copies (a page's K codes, V codes and their per-token norms) and
+// signalled on an mbarrier; it continues across its items, and a stage is refilled as soon as
+// the page in it has been read into registers. Per page a warp computes, in the rotated basis
+// (the keys' and values' own basis, no dequantisation to the original one):
 //   S^T[16 tokens x 8 cols] = K_rot[16 x D] . Q_rot^T     then  s_t *= ||k_t||
 //   O^T[D x 8 cols]        += V_rot^T[D x 16] . (P ||v||)^T
-// with mma.m16n8k16 on f16 operands and fp32 accumulators. A codebook operand is built
-// from its codes with one shared-memory load per byte: a 256-entry table maps a byte (two
-// 4-bit codes) to the f16 pair (cb[lo], cb[hi]) -- for 3-bit keys a 64-entry table maps a
-// 6-bit pair of codes. Each table is replicated 32 times, copy l in bank l, so the lanes of
-// a warp never conflict whatever codes they look up.
+// with mma.m16n8k16 on f16 operands and fp32 accumulators, and at the end of an item writes
+// its partial (output, max, sum) straight from registers; the reduce kernel combines the
+// partials and un-rotates the output.
 //
-// The dot product's coordinate order is free, so each thread takes the coordinates that
-// sit in a contiguous run of its key rows: thread (gid, tig) reads D/8 bytes of K rows gid
-// and gid + 8, which hold the k-columns its A fragments need; Q^T's B fragments use the
-// same coordinate order. For V^T (coordinates as the MMA's M) an m-tile's rows gid and
-// gid + 8 are the two coordinates of one byte, and prmt pairs the bytes of two tokens.
+// A codebook operand is built from its codes with one byte permute and one shared-memory load
+// per byte: a 256-entry table maps a byte (two 4-bit codes) to the f16 pair (cb[lo], cb[hi]) --
+// for 3-bit keys a 64-entry table maps a 6-bit pair of codes. Entry e sits at byte 256 e and is
+// replicated 32 times there, copy l in bank l, so the lanes of a warp never conflict whatever
+// codes they look up, and the permute that extracts a byte also places it at bits 8..15 next to
+// the lane's copy offset (4 l), giving the load address in one instruction.
 //
-// Precision: the rotated query is split q = q_hi + q_lo (both f16, after scaling by a power
-// of two), the lo half riding in the spare columns of S^T (G <= 4) or in a second MMA, so
-// the scores carry only the rounding of the codebook values to f16 (2^-12 relative); P is
-// split hi + lo as in the BF16 kernel. Partials are always written: the reduce kernel
-// un-rotates the combined output.
+// The dot product's coordinate order is free, so each thread takes the coordinates that sit in
+// a contiguous run of its key rows: thread (gid, tig) reads D/8 bytes of K rows gid and gid + 8,
+// which hold the k-columns its A fragments need; Q^T's B fragments use the same coordinate
+// order. For V^T (coordinates as the MMA's M) an m-tile's rows gid and gid + 8 are the two
+// coordinates of one byte, and byte-wise logic pairs the codes of two tokens into one index.
+//
+// Precision: the rotated query is split q = q_hi + q_lo (both f16, after scaling by a power of
+// two), the lo half riding in the spare columns of S^T (up to four columns) or in a second MMA,
+// so the scores carry only the rounding of the codebook values to f16 (2^-12 relative); P is
+// split hi + lo as in the BF16 kernel.
 //
 // (attention.rs README, KV Cache Formats table: the 4-bit Walsh-Hadamard codebook format and
 // split-K decode for it; turboquant-rs 0.4.1, src/cache/cuda/attention.rs: the fused kernel
@@ -45,6 +50,7 @@
 #include <mutex>
 
 #include "da_internal.cuh"
+#include "item_walk.cuh"
 #include "kv_formats.cuh"
 #include "page_softmax.cuh"
 #include "page_walk.cuh"
@@ -56,17 +62,17 @@ namespace {
 constexpr int kPage = 16;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr unsigned kFull = 0xffffffffu;
+constexpr int kSmemLimit = 227 * 1024;  // dynamic shared memory a CTA may use
 
 constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
 
-// KS: the key side (kSideCB4, kSideFP8, kSideCB3); values are 4-bit codes. NV: the group's
-// (query token, head) pairs ("virtual heads" v = jq * G + h) padded to a power of two <= 8.
+// KS: the key side (kSideCB4, kSideFP8, kSideCB3); values are 4-bit codes. NV: the CTA's
+// columns, i.e. the group's (query token, head) pairs ("virtual heads" v = jq * G + h) padded
+// to a power of two <= 8 (8 when more than 8 pairs are split into column groups).
 template <int KS, int D, int NV>
 struct Cb {
-  // eight warps share one CTA's lookup tables where their registers and two stages of 4 KB
-  // or less per warp allow two such CTAs per SM (D = 128, up to four columns of virtual
-  // heads, codebook keys), else four
-  static constexpr int kWarps = (D == 128 && NV <= 4 && KS != kSideFP8) ? 8 : 4;
+  // 16 warps where 128 registers per thread suffice (D = 128, up to four columns), else 8
+  static constexpr int kWarps = (D == 128 && NV <= 4) ? 16 : 8;
   static constexpr int kThreads = 32 * kWarps;
   static constexpr int kKRow = row_bytes(KS, D);  // bytes of one key row
   static constexpr int kVRow = D / 2;             // bytes of one value row
@@ -79,31 +85,28 @@ struct Cb {
   // behind the keys); 3-bit keys by a plain bulk copy (rows read unswizzled)
   static constexpr int kVAlign = D == 256 ? 1024 : 512;
   static constexpr int kKAlign = KS == kSideFP8 ? 1024 : KS == kSideCB4 ? kVAlign : 128;
-  static constexpr int kOffV = align_up(kKBytes, kVAlign);
-  static constexpr int kOffKN = kOffV + kVBytes;
-  static constexpr int kOffVN = kOffKN + (kKNorms ? 64 : 0);
   static constexpr int kAlign = kKAlign > kVAlign ? kKAlign : kVAlign;
-  static constexpr int kStageBytes = align_up(kOffVN + 64, kAlign);
+  static constexpr int kOffV = align_up(kKBytes, kVAlign);          // V codes within a code stage
+  static constexpr int kCodeBytes = align_up(kOffV + kVBytes, kAlign);
+  static constexpr int kNormBytes = 128;                            // per stage: K norms, V norms
   static constexpr int kTxBytes = kKBytes + kVBytes + (kKNorms ? 64 : 0) + 64;
-  static constexpr int kLutV = 256 * 32 * 4;  // 4-bit pair table, 32 copies
-  static constexpr int kLutK = KS == kSideCB3 ? 64 * 32 * 4 : 0;
-  static constexpr int kDP = D + 4;  // padded row of the merge buffer
-  // each warp's output staging (a warp owns the partition), or the cross-warp merge buffer
-  static constexpr int kMergeSmem = (kWarps * NV * kDP + 2 * kWarps * 8) * 4;
-  // stages: what two CTAs per SM leave after the tables and the merge buffer (228 KB per SM,
-  // 1 KB reserved and ~2 KB of alignment slack and barriers per CTA), 2 to 6 per warp
-  static constexpr int kStageBudget = (233472 / 2 - 3072 - kLutV - kLutK - kMergeSmem) / kWarps;
-  static constexpr int kFit = kStageBudget / kStageBytes;
-  static constexpr int kStages = kFit < 2 ? 2 : (kFit > 6 ? 6 : kFit);
+  // lookup tables: entry e at byte 256 e, the copy of lane l at + 4 l
+  static constexpr int kLutV = 256 * 256;
+  static constexpr int kLutK = KS == kSideCB3 ? 64 * 256 : 0;
+  static constexpr int kOffCodes = kLutV + kLutK;
+  // per warp: ring of item descriptors and walk state; per stage: mbarrier
+  static constexpr int kFixed = kOffCodes + kWarps * ItemIssue::kStateBytes + 1024;  // + alignment slack
+  static constexpr int kFit = (kSmemLimit - kFixed - kWarps * 8 * 8) / (kWarps * (kCodeBytes + kNormBytes));
+  static constexpr int kStages = kFit > 6 ? 6 : kFit;
+  static_assert(kStages >= 2, "shared memory holds fewer than two stages per warp");
+  static constexpr int kOffNorms = kOffCodes + kWarps * kStages * kCodeBytes;
+  static constexpr int kOffRing = kOffNorms + kWarps * kStages * kNormBytes;
+  static constexpr int kOffBars = kOffRing + kWarps * ItemIssue::kStateBytes;
+  static constexpr int kSmem = kOffBars + kWarps * kStages * 8 + 1024;
+  static_assert(kSmem <= kSmemLimit, "shared memory budget exceeded");
   static constexpr int kNT = NV <= 4 ? 1 : 2;           // P.V column tiles
   static constexpr int kMT = D / 16;                    // O^T row tiles
   static constexpr int kKS = D / 16;                    // k-steps of S^T
-  static constexpr int kOffStages = kLutV + kLutK;
-  static constexpr int kStageSmem = kWarps * kStages * kStageBytes;
-  static constexpr int kOffMerge = kOffStages + kStageSmem;
-  static constexpr int kSmem = kOffMerge + kMergeSmem + 1024;
-  // two CTAs per SM (228 KB, 1 KB reserved per CTA, barriers) wherever the stage budget allowed
-  static_assert(kFit < 2 || 2 * (kSmem + 1024 + 8 * kWarps * kStages) <= 233472, "two CTAs per SM do not fit");
 };
 
 __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
@@ -132,58 +135,66 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
 }
 __device__ __forceinline__ float ldsf(uint32_t addr) { return __uint_as_float(lds32(addr)); }
 
-// A lookup table as seen by one lane: its copy's first word, and the entry stride (128 bytes,
-// given at run time so the address is one multiply-add on the FMA pipe rather than a shift
-// and an add on the busier integer ALU pipe).
-struct LutRef {
-  uint32_t base, stride;  // shared-memory address of the lane's copy; entry stride in bytes (128)
+// A lookup table as seen by one lane: the table's address and the lane's copy offset.
+struct Lut {
+  uint32_t base;   // shared address of entry 0 (entries 256 bytes apart)
+  uint32_t lane4;  // 4 * lane
 };
-// Entry e of the lane's copy of a table.
-__device__ __forceinline__ uint32_t lut(const LutRef& t, uint32_t e) { return lds32(t.base + e * t.stride); }
-// byte j of a little-endian word array
+// Entry (byte J of w) of the lane's copy: the permute puts the byte at bits 8..15 and the
+// lane's offset at bits 0..7.
 template <int J>
-__device__ __forceinline__ uint32_t byte_of(const uint32_t* w) {
-  return __byte_perm(w[J >> 2], 0, 0x4440 | (J & 3));
+__device__ __forceinline__ uint32_t lut_byte(const Lut& t, uint32_t w) {
+  return lds32(t.base + __byte_perm(w, t.lane4, 0x5504 | (J << 4)));
 }
-// 6-bit field j (bits 6j .. 6j + 5) of a little-endian word array
+// byte J of a little-endian word array
 template <int J>
-__device__ __forceinline__ uint32_t field6(const uint32_t* w) {
+__device__ __forceinline__ uint32_t lut_byte_of(const Lut& t, const uint32_t* w) {
+  return lut_byte<J & 3>(t, w[J >> 2]);
+}
+// Entry (6-bit field J, bits 6J .. 6J + 5 of a little-endian word array) of the lane's copy:
+// the field is moved to bits 8..13 by one shift, then masked and joined with the lane's offset.
+template <int J>
+__device__ __forceinline__ uint32_t lut_field6(const Lut& t, const uint32_t* w) {
   constexpr int bit = 6 * J, wi = bit >> 5, sh = bit & 31;
-  if constexpr (sh <= 26)
-    return (w[wi] >> sh) & 63u;
+  uint32_t x;
+  if constexpr (sh < 8)
+    x = w[wi] << (8 - sh);
+  else if constexpr (sh <= 26)
+    x = w[wi] >> (sh - 8);
   else
-    return __funnelshift_r(w[wi], w[wi + 1], sh) & 63u;
+    x = __funnelshift_r(w[wi], w[wi + 1], sh - 8);  // the field crosses into the next word
+  return lds32(t.base + ((x & 0x3f00u) | t.lane4));
 }
 
-// A fragments of S^T for k-step KS_ from the thread's key bytes (rows gid: k0, gid + 8: k1).
-template <int KS, int D, int S>
-__device__ __forceinline__ void key_frag(uint32_t (&af)[4], const uint32_t* k0, const uint32_t* k1, const LutRef& lutk) {
+// A fragments of S^T for k-step S from the thread's key bytes (rows gid: k0, gid + 8: k1).
+template <int KS, int S>
+__device__ __forceinline__ void key_frag(uint32_t (&af)[4], const uint32_t* k0, const uint32_t* k1, const Lut& lutk) {
   if constexpr (KS == kSideCB4) {
-    af[0] = lut(lutk, byte_of<2 * S>(k0));
-    af[1] = lut(lutk, byte_of<2 * S>(k1));
-    af[2] = lut(lutk, byte_of<2 * S + 1>(k0));
-    af[3] = lut(lutk, byte_of<2 * S + 1>(k1));
+    af[0] = lut_byte_of<2 * S>(lutk, k0);
+    af[1] = lut_byte_of<2 * S>(lutk, k1);
+    af[2] = lut_byte_of<2 * S + 1>(lutk, k0);
+    af[3] = lut_byte_of<2 * S + 1>(lutk, k1);
   } else {
-    af[0] = lut(lutk, field6<2 * S>(k0));
-    af[1] = lut(lutk, field6<2 * S>(k1));
-    af[2] = lut(lutk, field6<2 * S + 1>(k0));
-    af[3] = lut(lutk, field6<2 * S + 1>(k1));
+    af[0] = lut_field6<2 * S>(lutk, k0);
+    af[1] = lut_field6<2 * S>(lutk, k1);
+    af[2] = lut_field6<2 * S + 1>(lutk, k0);
+    af[3] = lut_field6<2 * S + 1>(lutk, k1);
   }
 }
 
-template <int S, int N, int KS, int D, int NV>
+template <int S, int N, int KS, int NV>
 struct KeySteps {
   // S^T += A(k-step S) . Q^T for S = S .. N-1 (compile-time unrolled so byte offsets are
   // constants), odd k-steps into sc1 so that the two dependent MMA chains are half as long
   __device__ static __forceinline__ void run(float (&sc0)[4], float (&sc1)[4], const uint32_t* k0, const uint32_t* k1,
-                                             const LutRef& lutk, const uint32_t (*qf)[2], const uint32_t (*ql)[2]) {
+                                             const Lut& lutk, const uint32_t (*qf)[2], const uint32_t (*ql)[2]) {
     if constexpr (S < N) {
       uint32_t af[4];
-      key_frag<KS, D, S>(af, k0, k1, lutk);
+      key_frag<KS, S>(af, k0, k1, lutk);
       float(&sc)[4] = (S & 1) ? sc1 : sc0;
       ptx::mma_f16(sc, af, qf[S][0], qf[S][1]);
       if constexpr (NV == 8) ptx::mma_f16(sc, af, ql[S][0], ql[S][1]);
-      KeySteps<S + 1, N, KS, D, NV>::run(sc0, sc1, k0, k1, lutk, qf, ql);
+      KeySteps<S + 1, N, KS, NV>::run(sc0, sc1, k0, k1, lutk, qf, ql);
     }
   }
 };
@@ -193,11 +204,11 @@ struct ValueTiles {
   // O^T[m-tile M] += V^T(m-tile M) . P^T for M = M .. N-1. vx[r]: table indices, byte M of
   // word array r: r = 0 / 1: the low / high nibbles of tokens (2 tig, 2 tig + 1) paired, r =
   // 2 / 3 the same for tokens (2 tig + 8, 2 tig + 9); one lookup gives an A register.
-  __device__ static __forceinline__ void run(float (&o)[NT][D / 16][4], const uint32_t (*vx)[D / 64], const LutRef& lutv,
+  __device__ static __forceinline__ void run(float (&o)[NT][D / 16][4], const uint32_t (*vx)[D / 64], const Lut& lutv,
                                              const uint32_t (&pb)[NT][2]) {
     if constexpr (M < N) {
-      const uint32_t af[4] = {lut(lutv, byte_of<M>(vx[0])), lut(lutv, byte_of<M>(vx[1])),
-                              lut(lutv, byte_of<M>(vx[2])), lut(lutv, byte_of<M>(vx[3]))};
+      const uint32_t af[4] = {lut_byte_of<M>(lutv, vx[0]), lut_byte_of<M>(lutv, vx[1]), lut_byte_of<M>(lutv, vx[2]),
+                              lut_byte_of<M>(lutv, vx[3])};
 #pragma unroll
       for (int t = 0; t < NT; ++t) ptx::mma_f16(o[t][M], af, pb[t][0], pb[t][1]);
       ValueTiles<M + 1, N, D, NT>::run(o, vx, lutv, pb);
@@ -205,32 +216,45 @@ struct ValueTiles {
   }
 };
 
+// The thread's two columns of an item: the query position of each, and the positions it
+// attends within the partition, [lo, hi) (causal limit and window).
+struct Cols {
+  int lo[2], hi[2], pos[2], vh[2];
+};
+template <int NV>
+__device__ __forceinline__ Cols item_cols(const Args& a, const Item& it, const Range& r, int tig, int G) {
+  const int vbase = 8 * it.cg, V = min(NV, a.T * G - vbase);
+  Cols c;
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    c.vh[j] = vbase + ((2 * tig + j) % NV) % V;
+    c.pos[j] = it.L - a.T + c.vh[j] / G;
+    c.lo[j] = max(window_start(c.pos[j], a.window), r.start);
+    c.hi[j] = min(c.pos[j] + 1, r.end);
+  }
+  return c;
+}
+
 // CAP: softcap on (a separate instantiation, so the plain kernel carries no tanh)
 template <int KS, int D, int NV, bool CAP>
-__global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 2)
+__global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 1)
     partition_cb_kernel(const Args a, const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap nmap) {
   using C = Cb<KS, D, NV>;
-  constexpr int kWarps = C::kWarps, kThreads = C::kThreads, DP = C::kDP;
-  const int g = blockIdx.y, b = blockIdx.z;
+  constexpr int kWarps = C::kWarps, kThreads = C::kThreads;
   // the warp index through a shuffle from lane 0, which the compiler then treats as uniform
   const int tid = threadIdx.x, lane = tid & 31, w = __shfl_sync(kFull, tid >> 5, 0);
   const int gid = lane >> 2, tig = lane & 3;
-  const int G = a.Hq / a.Hkv, V = a.T * G;
-  ptx::grid_dependency_wait();   // what the kernel before this one writes (q, the rotated q, ...)
+  const int G = a.Hq / a.Hkv;
+  ptx::grid_dependency_wait();    // what the kernel before this one writes (q, the rotated q, ...)
   ptx::grid_dependents_launch();  // the reduce may be scheduled once every CTA has started
-  const int L = load_len(a, b, blockIdx.x == 0 && g == 0 && tid == 0);
-  const int np = seq_partitions(L, a.T, a.window, a.psize, a.thresh);
-  // this CTA's partitions of (b, g)
-  const int p_begin = blockIdx.x * a.ppc, p_end = min(p_begin + a.ppc, np);
-  if (p_begin >= p_end) return;
 
   extern __shared__ unsigned char smem_raw[];
-  __shared__ __align__(8) uint64_t bars[kWarps * C::kStages];
   const uint32_t smem = (ptx::smem_u32(smem_raw) + 1023u) & ~1023u;
-  unsigned char* smem_gen = smem_raw + (smem - ptx::smem_u32(smem_raw));
-  const uint32_t bar0 = ptx::smem_u32(bars) + w * C::kStages * 8;
-  const uint32_t stage0 = smem + C::kOffStages + w * C::kStages * C::kStageBytes;
+  const uint32_t bar0 = smem + C::kOffBars + w * C::kStages * 8;
+  const uint32_t code0 = smem + C::kOffCodes + w * C::kStages * C::kCodeBytes;
+  const uint32_t norm0 = smem + C::kOffNorms + w * C::kStages * C::kNormBytes;
+  const uint32_t ring = smem + C::kOffRing + w * ItemIssue::kStateBytes;
 
   if (lane == 0) {
     ptx::prefetch_tensor_map(&kmap);
@@ -241,37 +265,35 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 2)
   }
   __syncwarp();
 
-  // offsets within a stage of the 4-bit K and V codes and of the two norm vectors (the side with
-  // the lower address first when one map spans both)
+  // offsets within a code stage of the 4-bit K and V codes, and within a norm slot of the two
+  // norm vectors (the side with the lower address first when one map spans both)
   const uint32_t koff = (KS == kSideCB4 && a.kv_zk) ? C::kOffV : 0;
   const uint32_t voff = KS == kSideCB4 ? C::kOffV - koff : C::kOffV;
   const uint32_t knoff = a.kn_zk ? 64 : 0;
   const uint32_t vnoff = C::kKNorms ? 64 - knoff : 0;
-  // ---- the warp's partitions and pages, copied kStages ahead of the compute: with
-  //      a.owner, partitions p_begin + w, p_begin + w + kWarps, ... and all their pages; else
-  //      every partition of the CTA and pages w, w + kWarps, ... of each
-  const bool owner = a.owner != 0;
-  const int p_first = owner ? p_begin + w : p_begin, p_step = owner ? kWarps : 1;
-  const int pg_off = owner ? 0 : w, pg_step = owner ? 1 : kWarps;
-  IssueCursor cur;
-  cur.init(a, b, L, p_first, p_step, p_end, pg_off, pg_step, lane);
+
+  // ---- the warp's items and their pages, copied kStages pages ahead of the compute
+  const int stride = gridDim.x * kWarps;  // warps in the grid
+  ItemIssue cur;
+  cur.init(a, blockIdx.x * kWarps + w, ring, stride, lane);
   uint32_t valid_mask = 0;  // bit s: the page in stage s has a valid block (warp-uniform)
   unsigned issued = 0;
   int is = 0;  // stage of the next copy (issued % kStages)
   auto issue_next = [&]() {  // all lanes; lane 0 issues the copies of the page at the cursor
-    const int phys = cur.take(a);
+    const int gk = cur.g;
+    const int phys = cur.take(a, ring, stride, lane);
     const int s = is;
     is = is + 1 == C::kStages ? 0 : is + 1;
     ++issued;
     valid_mask = phys >= 0 ? (valid_mask | (1u << s)) : (valid_mask & ~(1u << s));
     if (lane == 0) {
-      const uint32_t bar = bar0 + 8 * s, dst = stage0 + s * C::kStageBytes;
+      const uint32_t bar = bar0 + 8 * s, dst = code0 + s * C::kCodeBytes, ndst = norm0 + s * C::kNormBytes;
       if (phys < 0) {
         ptx::mbar_arrive(bar);  // completes the phase with nothing loaded
       } else {
         ptx::fence_proxy_async();
         ptx::mbar_arrive_expect_tx(bar, C::kTxBytes);
-        const size_t unit = (size_t)phys * a.Hkv + g;  // (block, kv head): 16 consecutive rows
+        const size_t unit = (size_t)phys * a.Hkv + gk;  // (block, kv head): 16 consecutive rows
         const int y = (int)unit * kPage;
         if constexpr (KS == kSideCB4) {  // codes of K and V: one copy when one map spans both
           if (a.kv_pair) {
@@ -291,13 +313,13 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 2)
         }
         if constexpr (C::kKNorms) {  // per-token norms of K and V: one copy when one map spans both
           if (a.kn_pair) {
-            ptx::tma_load_3d(dst + C::kOffKN, &nmap, 0, (int)unit, 0, bar);
+            ptx::tma_load_3d(ndst, &nmap, 0, (int)unit, 0, bar);
           } else {
-            ptx::bulk_load(dst + C::kOffKN + knoff, a.k_scales + unit * kPage, 64, bar);
-            ptx::bulk_load(dst + C::kOffKN + vnoff, a.v_scales + unit * kPage, 64, bar);
+            ptx::bulk_load(ndst + knoff, a.k_scales + unit * kPage, 64, bar);
+            ptx::bulk_load(ndst + vnoff, a.v_scales + unit * kPage, 64, bar);
           }
         } else {
-          ptx::bulk_load(dst + C::kOffVN, a.v_scales + unit * kPage, 64, bar);
+          ptx::bulk_load(ndst, a.v_scales + unit * kPage, 64, bar);
         }
       }
     }
@@ -305,298 +327,200 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 2)
   for (int k = 0; k < C::kStages && cur.more; ++k) issue_next();
 
   // ---- lookup tables: byte -> (cb[lo], cb[hi]) for values (and 4-bit keys), 6-bit pair ->
-  //      (cbk[lo], cbk[hi]) for 3-bit keys; 32 copies, entry e of copy l at word 32 e + l
+  //      (cbk[lo], cbk[hi]) for 3-bit keys; entry e at word 64 e, 32 copies (word 64 e + l)
   {
     const float* cbv = a.codebook + (KS == kSideCB3 ? 8 : 0);
-    uint32_t* lv = reinterpret_cast<uint32_t*>(smem_gen);
+    uint32_t* lv = reinterpret_cast<uint32_t*>(smem_raw + (smem - ptx::smem_u32(smem_raw)));
     for (int i = tid; i < 256 * 8; i += kThreads) {
       const int e = i >> 3;
       const uint32_t x = pack_f16(__ldg(cbv + (e & 15)), __ldg(cbv + (e >> 4)));
-      *reinterpret_cast<uint4*>(lv + e * 32 + (i & 7) * 4) = make_uint4(x, x, x, x);
+      *reinterpret_cast<uint4*>(lv + e * 64 + (i & 7) * 4) = make_uint4(x, x, x, x);
     }
     if constexpr (KS == kSideCB3) {
-      uint32_t* lk = lv + 256 * 32;
+      uint32_t* lk = lv + C::kLutV / 4;
       for (int i = tid; i < 64 * 8; i += kThreads) {
         const int e = i >> 3;
         const uint32_t x = pack_f16(__ldg(a.codebook + (e & 7)), __ldg(a.codebook + (e >> 3)));
-        *reinterpret_cast<uint4*>(lk + e * 32 + (i & 7) * 4) = make_uint4(x, x, x, x);
+        *reinterpret_cast<uint4*>(lk + e * 64 + (i & 7) * 4) = make_uint4(x, x, x, x);
       }
     }
   }
-  const LutRef lutv{smem + lane * 4u, a.lut_stride};
-  const LutRef lutk{KS == kSideCB3 ? lutv.base + C::kLutV : lutv.base, a.lut_stride};
+  const Lut lutv{smem, 4u * lane};
+  const Lut lutk{KS == kSideCB3 ? smem + C::kLutV : smem, 4u * lane};
+  __syncthreads();  // lookup tables written; from here on no warp waits for another
 
-  // ---- query fragments (B operand of S^T). Column n scores virtual head (n % NV) % V.
-  const int qv = (gid % NV) % V;
-  const size_t qrow = (((size_t)b * a.T + qv / G) * a.Hq + g * G + qv % G) * D;
-  uint32_t qf[C::kKS][2], ql[NV == 8 ? C::kKS : 1][2];
-  float score_scale;
-  if constexpr (KS == kSideFP8) {
-    // unrotated bf16 query, scaled by a power of two into the f16 range (exact)
-    const uint16_t* qp = a.q + qrow;
-    float x[C::kKS][4];
-    float mx = 0.0f;
-#pragma unroll
-    for (int ks = 0; ks < C::kKS; ++ks)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        x[ks][e] = bf16_to_f32(qp[16 * ks + 4 * tig + e]);
-        mx = fmaxf(mx, fabsf(x[ks][e]));
-      }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
-    int ex = 0;
-    frexpf(mx, &ex);
-    const int e2 = ex > 14 ? 14 - ex : 0;
-    const float qs = ldexpf(1.0f, e2);
-#pragma unroll
-    for (int ks = 0; ks < C::kKS; ++ks) {
-      qf[ks][0] = pack_f16(x[ks][0] * qs, x[ks][1] * qs);
-      qf[ks][1] = pack_f16(x[ks][2] * qs, x[ks][3] * qs);
-    }
-    score_scale = a.scale * __ldg(a.k_scales) * ldexpf(1.0f, -e2) * kLog2e;
-  } else {
-    // rotated fp32 query: coordinates (D/4) tig + 4 ks + {0, 1} (b0) and + {2, 3} (b1),
-    // scaled by 2^e2 (max below 2^15) and split into f16 hi + lo; for NV <= 4 the columns
-    // n >= 4 carry the lo half (same heads as n - 4)
-    const float4* qp = reinterpret_cast<const float4*>(a.q_rot + qrow + (D / 4) * tig);
-    float4 x[C::kKS];
-    float mx = 0.0f;
-#pragma unroll
-    for (int ks = 0; ks < C::kKS; ++ks) {
-      x[ks] = qp[ks];
-      mx = fmaxf(fmaxf(mx, fmaxf(fabsf(x[ks].x), fabsf(x[ks].y))), fmaxf(fabsf(x[ks].z), fabsf(x[ks].w)));
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
-    int ex = 0;
-    frexpf(mx, &ex);
-    const int e2 = 15 - ex;
-    const float qs = ldexpf(1.0f, e2);
-    const bool lo_col = NV <= 4 && gid >= 4;
-#pragma unroll
-    for (int ks = 0; ks < C::kKS; ++ks) {
-      const float y0 = x[ks].x * qs, y1 = x[ks].y * qs, y2 = x[ks].z * qs, y3 = x[ks].w * qs;
-      const float h0 = hi_f16(y0), h1 = hi_f16(y1), h2 = hi_f16(y2), h3 = hi_f16(y3);
-      if constexpr (NV == 8) {
-        qf[ks][0] = pack_f16(h0, h1);
-        qf[ks][1] = pack_f16(h2, h3);
-        ql[ks][0] = pack_f16(y0 - h0, y1 - h1);
-        ql[ks][1] = pack_f16(y2 - h2, y3 - h3);
-      } else {
-        qf[ks][0] = lo_col ? pack_f16(y0 - h0, y1 - h1) : pack_f16(h0, h1);
-        qf[ks][1] = lo_col ? pack_f16(y2 - h2, y3 - h3) : pack_f16(h2, h3);
-      }
-    }
-    score_scale = a.scale * ldexpf(1.0f, -e2) * kLog2e;
-  }
   const float cap = a.softcap;
   const float cap_pre = CAP ? 1.0f / (cap * kLog2e) : 0.0f;  // log2-domain score -> s_nat / cap
   const float cap_post = cap * kLog2e;
-
-  // hi/lo role of this thread's two P columns (NV <= 4: column c carries part c / NV), and
-  // the positions its columns' query tokens attend: [lo_w, pos] (causal limit and window)
-  int part[2], lo_w[2], pos_c[2];
-#pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    part[j] = NV <= 4 ? (2 * tig + j) / NV : 0;
-    pos_c[j] = L - a.T + (((2 * tig + j) % NV) % V) / G;
-    lo_w[j] = window_start(pos_c[j], a.window);
-  }
-  // ALiBi: the slope of each column's query head, in the log2 domain of the scores
   const bool alibi = a.alibi != nullptr;
-  float slope_c[2] = {0.0f, 0.0f};
-  if (alibi) {
-#pragma unroll
-    for (int j = 0; j < 2; ++j) slope_c[j] = __ldg(a.alibi + g * G + (((2 * tig + j) % NV) % V) % G) * kLog2e;
-  }
-  float* ep_o = reinterpret_cast<float*>(smem_gen + C::kOffMerge);  // [kWarps][NV][DP]
-  float* ep_m = ep_o + kWarps * NV * DP;                             // [kWarps][8]
-  float* ep_l = ep_m + kWarps * 8;                                   // [kWarps][8]
-
-  __syncthreads();  // lookup tables written
-
+  const int PK = a.P * a.ksub;  // partial slots per output row
   const int mi = lane >> 3, ri = lane & 7;  // ldmatrix (FP8 keys): matrix index and row of this lane's address
-  unsigned consumed = 0, stall_from = 0;
+  unsigned consumed = 0, stall_from = 0, popped = 0;
   int cs = 0;            // stage of the next page to compute (consumed % kStages)
   uint32_t cphase = 0;   // its mbarrier phase parity ((consumed / kStages) & 1)
   bool stalled = false;  // a copy never arrived: no more waits, copies or compute
-
-  for (int p = p_first; p < p_end; p += p_step) {
-  const Range r = partition_range(L, a.T, p, a.window, a.psize, a.thresh);
-  int first_page, npages;
-  range_pages(r, first_page, npages);
-  const int nw = warp_pages(npages, pg_off, pg_step);
-  // tokens each column attends in this partition, and the pages that need no mask in any
-  // column: [lo_all, hi_all) (warp-uniform)
-  int lo_c[2], hi_c[2];
+  int q_b = -1, q_g = -1, q_cg = -1;  // (sequence, kv head, column group) of the loaded query fragments
+  // P column roles (NV <= 4: column c carries the hi part when c / NV == 0, the lo part when
+  // c / NV == 1, nothing beyond) as multipliers: x = p cl + h (ch - cl)
+  float p_lo[2], p_hl[2];
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
-    lo_c[j] = max(lo_w[j], r.start);
-    hi_c[j] = min(pos_c[j] + 1, r.end);
+    const int part = NV <= 4 ? (2 * tig + j) / NV : 0;
+    p_lo[j] = part == 1 ? 1.0f : 0.0f;
+    p_hl[j] = part == 0 ? 1.0f : (part == 1 ? -1.0f : 0.0f);
   }
-  int lo_all = max(lo_c[0], lo_c[1]), hi_all = min(hi_c[0], hi_c[1]);
-  lo_all = max(lo_all, __shfl_xor_sync(kFull, lo_all, 1));
-  lo_all = max(lo_all, __shfl_xor_sync(kFull, lo_all, 2));
-  hi_all = min(hi_all, __shfl_xor_sync(kFull, hi_all, 1));
-  hi_all = min(hi_all, __shfl_xor_sync(kFull, hi_all, 2));
-  // ---- running state: column c = 2*tig + j of S^T and of every O^T column tile. O^T is kept
-  //      in units of 2^(ev_run - 127): ev_run is the largest biased binary32 exponent of the
-  //      value norms seen so far, so P * ||v|| * 2^(127 - ev_run) < 2^(kLazyLog2 + 1) fits f16
-  float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.0f, 0.0f};
-  float o[C::kNT][C::kMT][4];
-#pragma unroll
-  for (int t = 0; t < C::kNT; ++t)
-#pragma unroll
-    for (int mt = 0; mt < C::kMT; ++mt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) o[t][mt][e] = 0.0f;
-  int ev_run = 0;
-  float v_unit = 1.0f;  // 2^(127 - ev_run)
+  uint32_t qf[C::kKS][2], ql[NV == 8 ? C::kKS : 1][2];
+  float score_scale = 0.0f;
 
-  for (int i = 0; i < nw; ++i, ++consumed) {
-    const int s = cs;
-    if (!stalled && !ptx::mbar_wait(bar0 + 8 * s, cphase)) {
-      stalled = true;
-      stall_from = consumed;
-    }
-    if (++cs == C::kStages) {
-      cs = 0;
-      cphase ^= 1u;
-    }
-    if (!stalled && (valid_mask & (1u << s))) {
-      const uint32_t sb = stage0 + s * C::kStageBytes, kb = sb + koff, vb = sb + voff;
-      const int tok0 = (first_page + pg_off + pg_step * i) * kPage;
-      // -- S^T = K . Q^T, the k-steps alternating between two accumulators (two dependent MMA
-      //    chains of half the length), added at the end
-      float sc[4] = {0.0f, 0.0f, 0.0f, 0.0f}, sc2[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  while (!stalled) {
+    __syncwarp();  // the ring entry written by lane 0 is visible to the warp
+    if (popped == cur.pushed) break;  // no item left for this warp
+    const Item it = ring_item(ring, popped++);
+    const ItemPages ip = item_pages(a, it);
+    const int b = it.b, g = it.g;
+    // the item's columns: virtual heads vbase .. vbase + V - 1
+    const int vbase = 8 * it.cg, V = min(NV, a.T * G - vbase);
+
+    // ---- query fragments (B operand of S^T). Column n scores virtual head vbase + (n % NV) % V.
+    if (b != q_b || g != q_g || it.cg != q_cg) {
+      q_b = b, q_g = g, q_cg = it.cg;
+      const int qv = vbase + (gid % NV) % V;
+      const size_t qrow = query_row(a, b, g, G, qv) * D;
       if constexpr (KS == kSideFP8) {
+        // unrotated bf16 query, scaled by a power of two into the f16 range (exact)
+        const uint16_t* qp = a.q + qrow;
+        float x[C::kKS][4];
+        float mx = 0.0f;
 #pragma unroll
-        for (int j2 = 0; j2 < C::kKS / 2; ++j2) {
-          const int row = ri + 8 * (mi & 1), chunk = 2 * j2 + (mi >> 1);
-          uint32_t rr[4];
-          ptx::ldmatrix_x4(rr, kb + (chunk >> 3) * 2048 + row * 128 + (((chunk & 7) ^ (row & 7)) << 4));
-          const uint32_t a0[4] = {e4m3x2_to_f16x2(rr[0]), e4m3x2_to_f16x2(rr[1]), e4m3x2_to_f16x2(rr[0] >> 16),
-                                  e4m3x2_to_f16x2(rr[1] >> 16)};
-          ptx::mma_f16(sc, a0, qf[2 * j2][0], qf[2 * j2][1]);
-          const uint32_t a1[4] = {e4m3x2_to_f16x2(rr[2]), e4m3x2_to_f16x2(rr[3]), e4m3x2_to_f16x2(rr[2] >> 16),
-                                  e4m3x2_to_f16x2(rr[3] >> 16)};
-          ptx::mma_f16(sc2, a1, qf[2 * j2 + 1][0], qf[2 * j2 + 1][1]);
+        for (int ks = 0; ks < C::kKS; ++ks)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            x[ks][e] = bf16_to_f32(qp[16 * ks + 4 * tig + e]);
+            mx = fmaxf(mx, fabsf(x[ks][e]));
+          }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+        int ex = 0;
+        frexpf(mx, &ex);
+        const int e2 = ex > 14 ? 14 - ex : 0;
+        const float qs = ldexpf(1.0f, e2);
+#pragma unroll
+        for (int ks = 0; ks < C::kKS; ++ks) {
+          qf[ks][0] = pack_f16(x[ks][0] * qs, x[ks][1] * qs);
+          qf[ks][1] = pack_f16(x[ks][2] * qs, x[ks][3] * qs);
         }
-#pragma unroll
-        for (int e = 0; e < 4; ++e) sc[e] += sc2[e];
+        score_scale = a.scale * __ldg(a.k_scales) * ldexpf(1.0f, -e2) * kLog2e;
       } else {
-        // the thread's key bytes: D/8 per row (4-bit) or 3D/32 (3-bit), rows gid and gid + 8
-        constexpr int kWords = KS == kSideCB4 ? D / 32 : 3 * D / 128;
-        uint32_t k0[kWords + 1], k1[kWords + 1];
-        k0[kWords] = k1[kWords] = 0u;
-        if constexpr (KS == kSideCB4 && D == 128) {
-          // 64-byte rows, 64-byte swizzle: 16-byte chunk c of row r at c ^ ((r >> 1) & 3)
-          const uint32_t ch = (tig ^ ((gid >> 1) & 3)) << 4;  // the same for rows gid and gid + 8
-          const uint4 x0 = lds128(kb + gid * 64 + ch), x1 = lds128(kb + (gid + 8) * 64 + ch);
-          k0[0] = x0.x, k0[1] = x0.y, k0[2] = x0.z, k0[3] = x0.w;
-          k1[0] = x1.x, k1[1] = x1.y, k1[2] = x1.z, k1[3] = x1.w;
-        } else if constexpr (KS == kSideCB4) {  // D = 256, 128-byte swizzle: chunks 2 tig, 2 tig + 1
+        // rotated fp32 query: coordinates (D/4) tig + 4 ks + {0, 1} (b0) and + {2, 3} (b1),
+        // scaled by 2^e2 (max below 2^15) and split into f16 hi + lo; for NV <= 4 the columns
+        // n >= 4 carry the lo half (same heads as n - 4)
+        const float4* qp = reinterpret_cast<const float4*>(a.q_rot + qrow + (D / 4) * tig);
+        float4 x[C::kKS];
+        float mx = 0.0f;
 #pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            const int ch = 2 * tig + c;
-            const uint4 x0 = lds128(kb + gid * 128 + ((ch ^ gid) << 4));
-            const uint4 x1 = lds128(kb + (gid + 8) * 128 + ((ch ^ gid) << 4));  // (gid + 8) & 7 == gid
-            k0[4 * c] = x0.x, k0[4 * c + 1] = x0.y, k0[4 * c + 2] = x0.z, k0[4 * c + 3] = x0.w;
-            k1[4 * c] = x1.x, k1[4 * c + 1] = x1.y, k1[4 * c + 2] = x1.z, k1[4 * c + 3] = x1.w;
+        for (int ks = 0; ks < C::kKS; ++ks) {
+          x[ks] = qp[ks];
+          mx = fmaxf(fmaxf(mx, fmaxf(fabsf(x[ks].x), fabsf(x[ks].y))), fmaxf(fabsf(x[ks].z), fabsf(x[ks].w)));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+        int ex = 0;
+        frexpf(mx, &ex);
+        const int e2 = 15 - ex;
+        const float qs = ldexpf(1.0f, e2);
+        const bool lo_col = NV <= 4 && gid >= 4;
+#pragma unroll
+        for (int ks = 0; ks < C::kKS; ++ks) {
+          const float y0 = x[ks].x * qs, y1 = x[ks].y * qs, y2 = x[ks].z * qs, y3 = x[ks].w * qs;
+          const float h0 = hi_f16(y0), h1 = hi_f16(y1), h2 = hi_f16(y2), h3 = hi_f16(y3);
+          if constexpr (NV == 8) {
+            qf[ks][0] = pack_f16(h0, h1);
+            qf[ks][1] = pack_f16(h2, h3);
+            ql[ks][0] = pack_f16(y0 - h0, y1 - h1);
+            ql[ks][1] = pack_f16(y2 - h2, y3 - h3);
+          } else {
+            qf[ks][0] = lo_col ? pack_f16(y0 - h0, y1 - h1) : pack_f16(h0, h1);
+            qf[ks][1] = lo_col ? pack_f16(y2 - h2, y3 - h3) : pack_f16(h2, h3);
           }
-        } else {  // 3-bit: 12 (D = 128) or 24 (D = 256) bytes per row at (3D/32) tig
-#pragma unroll
-          for (int c = 0; c < kWords; ++c) {
-            k0[c] = lds32(kb + gid * C::kKRow + (3 * D / 32) * tig + 4 * c);
-            k1[c] = lds32(kb + (gid + 8) * C::kKRow + (3 * D / 32) * tig + 4 * c);
-          }
         }
-        KeySteps<0, C::kKS, KS, D, NV>::run(sc, sc2, k0, k1, lutk, qf, ql);
+        score_scale = a.scale * ldexpf(1.0f, -e2) * kLog2e;
+      }
+    }
+
+    // the pages no column masks: tokens [lo_all, hi_all) (warp-uniform); first token of the
+    // k-th page of the item's walk: tk0 + k * tkstep
+    int lo_all, hi_all;
+    {
+      const Cols c = item_cols<NV>(a, it, ip.r, tig, G);
+      lo_all = max(c.lo[0], c.lo[1]);
+      hi_all = min(c.hi[0], c.hi[1]);
+      lo_all = max(lo_all, __shfl_xor_sync(kFull, lo_all, 1));
+      lo_all = max(lo_all, __shfl_xor_sync(kFull, lo_all, 2));
+      hi_all = min(hi_all, __shfl_xor_sync(kFull, hi_all, 1));
+      hi_all = min(hi_all, __shfl_xor_sync(kFull, hi_all, 2));
+    }
+    const int tk0 = (ip.first + it.sub + (ip.rev ? a.ksub * (ip.n - 1) : 0)) * kPage;
+    const int tkstep = (ip.rev ? -a.ksub : a.ksub) * kPage;
+    const int n_pages = ip.n;
+
+    // ---- running state: column c = 2*tig + j of S^T and of every O^T column tile. O^T is kept
+    //      in units of 2^(ev_run - 127): ev_run is the largest biased binary32 exponent of the
+    //      value norms seen so far, so P * ||v|| * 2^(127 - ev_run) < 2^(kLazyLog2 + 1) fits f16
+    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.0f, 0.0f};
+    float o[C::kNT][C::kMT][4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) sc[e] += sc2[e];
-        if constexpr (NV <= 4) {
+    for (int t = 0; t < C::kNT; ++t)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) sc[e] += __shfl_xor_sync(kFull, sc[e], 2);  // hi + lo columns
+      for (int mt = 0; mt < C::kMT; ++mt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[t][mt][e] = 0.0f;
+    int ev_run = 0;
+    float v_unit = 1.0f;  // 2^(127 - ev_run)
+
+    for (int i = 0; i < n_pages; ++i, ++consumed) {
+      const int s = cs;
+      if (!ptx::mbar_wait(bar0 + 8 * s, cphase)) {
+        stalled = true;
+        stall_from = consumed;
+        break;
+      }
+      if (++cs == C::kStages) {
+        cs = 0;
+        cphase ^= 1u;
+      }
+      const bool valid = valid_mask & (1u << s);
+      const uint32_t cb0 = code0 + s * C::kCodeBytes, kb = cb0 + koff, vb = cb0 + voff;
+      const uint32_t nb = norm0 + s * C::kNormBytes;
+      const int tok0 = tk0 + i * tkstep;
+
+      // -- the page into registers: key bytes (codebook keys), value bytes, norms
+      constexpr int kWords = KS == kSideCB4 ? D / 32 : KS == kSideCB3 ? 3 * D / 128 : 1;
+      uint32_t k0[kWords + 1], k1[kWords + 1];
+      k0[kWords] = k1[kWords] = 0u;
+      if constexpr (KS == kSideCB4 && D == 128) {
+        // 64-byte rows, 64-byte swizzle: 16-byte chunk c of row r at c ^ ((r >> 1) & 3)
+        const uint32_t ch = (tig ^ ((gid >> 1) & 3)) << 4;  // the same for rows gid and gid + 8
+        const uint4 x0 = lds128(kb + gid * 64 + ch), x1 = lds128(kb + (gid + 8) * 64 + ch);
+        k0[0] = x0.x, k0[1] = x0.y, k0[2] = x0.z, k0[3] = x0.w;
+        k1[0] = x1.x, k1[1] = x1.y, k1[2] = x1.z, k1[3] = x1.w;
+      } else if constexpr (KS == kSideCB4) {  // D = 256, 128-byte swizzle: chunks 2 tig, 2 tig + 1
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const int ch = 2 * tig + c;
+          const uint4 x0 = lds128(kb + gid * 128 + ((ch ^ gid) << 4));
+          const uint4 x1 = lds128(kb + (gid + 8) * 128 + ((ch ^ gid) << 4));  // (gid + 8) & 7 == gid
+          k0[4 * c] = x0.x, k0[4 * c + 1] = x0.y, k0[4 * c + 2] = x0.z, k0[4 * c + 3] = x0.w;
+          k1[4 * c] = x1.x, k1[4 * c + 1] = x1.y, k1[4 * c + 2] = x1.z, k1[4 * c + 3] = x1.w;
+        }
+      } else if constexpr (KS == kSideCB3) {  // 12 (D = 128) or 24 (D = 256) bytes per row at (3D/32) tig
+#pragma unroll
+        for (int c = 0; c < kWords; ++c) {
+          k0[c] = lds32(kb + gid * C::kKRow + (3 * D / 32) * tig + 4 * c);
+          k1[c] = lds32(kb + (gid + 8) * C::kKRow + (3 * D / 32) * tig + 4 * c);
         }
       }
-      // -- scale (and key norms), softcap, mask; sc[0], sc[1]: token gid; sc[2], sc[3]: gid + 8
-      float kn0 = 1.0f, kn1 = 1.0f;
-      if constexpr (C::kKNorms) {
-        kn0 = ldsf(sb + C::kOffKN + knoff + 4 * gid);
-        kn1 = ldsf(sb + C::kOffKN + knoff + 4 * (gid + 8));
-      }
-      const float ss0 = score_scale * kn0, ss1 = score_scale * kn1;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float y = sc[e] * ((e >> 1) ? ss1 : ss0);
-        sc[e] = CAP ? cap_post * tanhf(y * cap_pre) : y;
-      }
-      if (alibi) {  // + slope * (t - pos) for token t of each element
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          sc[e] += slope_c[e & 1] * (float)(tok0 + gid + (e >> 1) * 8 - pos_c[e & 1]);
-      }
-      if (tok0 < lo_all || tok0 + kPage > hi_all) mask_page(sc, tok0, gid, lo_c, hi_c);
-      // -- online softmax per column (lazily moved reference max); a larger value-norm
-      //    exponent on this page rescales O^T by the same exact power of two
-      float alpha[2], pr[4];
-      bool rescale = page_softmax(sc, m_run, l_run, alpha, pr);
-      const uint32_t vnb = sb + C::kOffKN + vnoff;  // = kOffVN with separate norm copies
-      const float vn0 = ldsf(vnb + 4 * gid), vn1 = ldsf(vnb + 4 * (gid + 8));
-      int ev = (int)(__float_as_uint(fmaxf(fabsf(vn0), fabsf(vn1))) >> 23);
-      if (__any_sync(kFull, ev > ev_run)) {  // a larger exponent on this page: the warp's max
-        ev = max(ev, __shfl_xor_sync(kFull, ev, 4));
-        ev = max(ev, __shfl_xor_sync(kFull, ev, 8));
-        ev = max(ev, __shfl_xor_sync(kFull, ev, 16));
-        const float f = ldexpf(1.0f, ev_run - ev);
-        alpha[0] *= f;
-        alpha[1] *= f;
-        ev_run = ev;
-        v_unit = ldexpf(1.0f, 127 - ev);
-        rescale = true;
-      }
-      if (rescale) {
-#pragma unroll
-        for (int t = 0; t < C::kNT; ++t)
-#pragma unroll
-          for (int mt = 0; mt < C::kMT; ++mt) {
-            o[t][mt][0] *= alpha[0];
-            o[t][mt][1] *= alpha[1];
-            o[t][mt][2] *= alpha[0];
-            o[t][mt][3] *= alpha[1];
-          }
-      }
-      // -- (P * value norms)^T as the B operand: hi/lo parts in C layout, transposed with movmatrix
-      const float vu0 = vn0 * v_unit, vu1 = vn1 * v_unit;
-      float pv[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) pv[e] = pr[e] * ((e >> 1) ? vu1 : vu0);
-      uint32_t pb[C::kNT][2];
-      if constexpr (NV <= 4) {
-        float x[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int pt = part[e & 1];
-          const float h = hi_f16(pv[e]);
-          x[e] = pt == 0 ? h : (pt == 1 ? pv[e] - h : 0.0f);
-        }
-        pb[0][0] = ptx::movmatrix_trans(pack_f16(x[0], x[1]));
-        pb[0][1] = ptx::movmatrix_trans(pack_f16(x[2], x[3]));
-      } else {
-        float hi[4], lo[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          hi[e] = hi_f16(pv[e]);
-          lo[e] = pv[e] - hi[e];
-        }
-        pb[0][0] = ptx::movmatrix_trans(pack_f16(hi[0], hi[1]));
-        pb[0][1] = ptx::movmatrix_trans(pack_f16(hi[2], hi[3]));
-        pb[C::kNT - 1][0] = ptx::movmatrix_trans(pack_f16(lo[0], lo[1]));
-        pb[C::kNT - 1][1] = ptx::movmatrix_trans(pack_f16(lo[2], lo[3]));
-      }
-      // -- O^T += V^T . P^T: the thread's value bytes of tokens 2 tig, 2 tig + 1, 2 tig + 8,
-      //    2 tig + 9, D/16 bytes each at byte (D/16) gid
+      // the thread's value bytes of tokens 2 tig, 2 tig + 1, 2 tig + 8, 2 tig + 9, D/16 bytes
+      // each at byte (D/16) gid
       uint32_t vw[4][D / 64];
 #pragma unroll
       for (int i4 = 0; i4 < 4; ++i4) {
@@ -609,100 +533,178 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 2)
           vw[i4][0] = x.x, vw[i4][1] = x.y, vw[i4][2] = x.z, vw[i4][3] = x.w;
         }
       }
-      // byte b of token t holds coordinates 2b (low nibble) and 2b + 1 (high nibble); pair
-      // tokens t, t + 1 into the index (code_t | code_t+1 << 4) of the table, whose entry is
-      // then the A register (v_t, v_t+1) of one coordinate
-      uint32_t vx[4][D / 64];
-#pragma unroll
-      for (int k = 0; k < D / 64; ++k) {
-        vx[0][k] = (vw[0][k] & 0x0f0f0f0fu) | ((vw[1][k] << 4) & 0xf0f0f0f0u);
-        vx[1][k] = ((vw[0][k] >> 4) & 0x0f0f0f0fu) | (vw[1][k] & 0xf0f0f0f0u);
-        vx[2][k] = (vw[2][k] & 0x0f0f0f0fu) | ((vw[3][k] << 4) & 0xf0f0f0f0u);
-        vx[3][k] = ((vw[2][k] >> 4) & 0x0f0f0f0fu) | (vw[3][k] & 0xf0f0f0f0u);
+      float kn0 = 1.0f, kn1 = 1.0f;
+      if constexpr (C::kKNorms) {
+        kn0 = ldsf(nb + knoff + 4 * gid);
+        kn1 = ldsf(nb + knoff + 4 * (gid + 8));
       }
-      ValueTiles<0, C::kMT, D, C::kNT>::run(o, vx, lutv, pb);
-    }
-    __syncwarp();
-    if (!stalled && cur.more) issue_next();
-  }
+      const float vn0 = ldsf(nb + vnoff + 4 * gid), vn1 = ldsf(nb + vnoff + 4 * (gid + 8));
+      // FP8 keys are read with ldmatrix during the MMAs below, so their stage is refilled after
+      if constexpr (KS != kSideFP8) {
+        __syncwarp();  // every lane has read the stage
+        if (cur.more) issue_next();
+      }
 
-  // ---- partition epilogue (O^T: hi and lo columns added, back to absolute units)
-  const float o_unit = ldexpf(1.0f, ev_run - 127);
+      if (valid) {
+        // -- S^T = K . Q^T, the k-steps alternating between two accumulators (two dependent MMA
+        //    chains of half the length), added at the end
+        float sc[4] = {0.0f, 0.0f, 0.0f, 0.0f}, sc2[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        if constexpr (KS == kSideFP8) {
 #pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    l_run[j] += __shfl_xor_sync(kFull, l_run[j], 4);
-    l_run[j] += __shfl_xor_sync(kFull, l_run[j], 8);
-    l_run[j] += __shfl_xor_sync(kFull, l_run[j], 16);
-  }
-  float* ep_w = ep_o + w * NV * DP;
+          for (int j2 = 0; j2 < C::kKS / 2; ++j2) {
+            const int row = ri + 8 * (mi & 1), chunk = 2 * j2 + (mi >> 1);
+            uint32_t rr[4];
+            ptx::ldmatrix_x4(rr, kb + (chunk >> 3) * 2048 + row * 128 + (((chunk & 7) ^ (row & 7)) << 4));
+            const uint32_t a0[4] = {e4m3x2_to_f16x2(rr[0]), e4m3x2_to_f16x2(rr[1]), e4m3x2_to_f16x2(rr[0] >> 16),
+                                    e4m3x2_to_f16x2(rr[1] >> 16)};
+            ptx::mma_f16(sc, a0, qf[2 * j2][0], qf[2 * j2][1]);
+            const uint32_t a1[4] = {e4m3x2_to_f16x2(rr[2]), e4m3x2_to_f16x2(rr[3]), e4m3x2_to_f16x2(rr[2] >> 16),
+                                    e4m3x2_to_f16x2(rr[3] >> 16)};
+            ptx::mma_f16(sc2, a1, qf[2 * j2 + 1][0], qf[2 * j2 + 1][1]);
+          }
 #pragma unroll
-  for (int mt = 0; mt < C::kMT; ++mt)
+          for (int e = 0; e < 4; ++e) sc[e] += sc2[e];
+        } else {
+          KeySteps<0, C::kKS, KS, NV>::run(sc, sc2, k0, k1, lutk, qf, ql);
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      float v = o[0][mt][e];
-      if constexpr (NV == 8) v += o[C::kNT - 1][mt][e];
-      if constexpr (NV == 4) v += __shfl_xor_sync(kFull, v, 2);  // columns c, c + 4
-      if constexpr (NV == 2) v += __shfl_xor_sync(kFull, v, 1);  // columns c, c + 2
-      if constexpr (NV == 1) v += (e & 1) ? 0.0f : o[0][mt][e + 1];  // columns 0, 1
-      const int col = 2 * tig + (e & 1);
-      // O^T rows gid and gid + 8 of m-tile mt: the two coordinates of byte (D/16) gid + mt
-      const int rowd = 2 * ((D / 16) * gid + mt) + (e >> 1);
-      if (col < V) ep_w[col * DP + rowd] = v * o_unit;
+          for (int e = 0; e < 4; ++e) sc[e] += sc2[e];
+          if constexpr (NV <= 4) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sc[e] += __shfl_xor_sync(kFull, sc[e], 2);  // hi + lo columns
+          }
+        }
+        // -- scale (and key norms), softcap, mask; sc[0], sc[1]: token gid; sc[2], sc[3]: gid + 8
+        const float ss0 = score_scale * kn0, ss1 = score_scale * kn1;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float y = sc[e] * ((e >> 1) ? ss1 : ss0);
+          sc[e] = CAP ? cap_post * tanhf(y * cap_pre) : y;
+        }
+        if (alibi || tok0 < lo_all || tok0 + kPage > hi_all) {
+          // the columns' limits and positions again, from the item's ring entry (rare pages)
+          const Item it2 = ring_item(ring, popped - 1);
+          const Cols c = item_cols<NV>(a, it2, partition_range(it2.L, a.T, it2.p, a.window, a.psize, a.thresh), tig,
+                                       G);
+          if (alibi) {  // + slope * (t - pos) for token t of each element
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              sc[e] += __ldg(a.alibi + it2.g * G + c.vh[e & 1] % G) * kLog2e *
+                       (float)(tok0 + gid + (e >> 1) * 8 - c.pos[e & 1]);
+          }
+          if (tok0 < lo_all || tok0 + kPage > hi_all) mask_page(sc, tok0, gid, c.lo, c.hi);
+        }
+        // -- online softmax per column (lazily moved reference max); a larger value-norm
+        //    exponent on this page rescales O^T by the same exact power of two
+        float alpha[2], pr[4];
+        bool rescale = page_softmax(sc, m_run, l_run, alpha, pr);
+        int ev = (int)(__float_as_uint(fmaxf(fabsf(vn0), fabsf(vn1))) >> 23);
+        if (__any_sync(kFull, ev > ev_run)) {  // a larger exponent on this page: the warp's max
+          ev = max(ev, __shfl_xor_sync(kFull, ev, 4));
+          ev = max(ev, __shfl_xor_sync(kFull, ev, 8));
+          ev = max(ev, __shfl_xor_sync(kFull, ev, 16));
+          const float f = ldexpf(1.0f, ev_run - ev);
+          alpha[0] *= f;
+          alpha[1] *= f;
+          ev_run = ev;
+          v_unit = ldexpf(1.0f, 127 - ev);
+          rescale = true;
+        }
+        if (rescale) {
+#pragma unroll
+          for (int t = 0; t < C::kNT; ++t)
+#pragma unroll
+            for (int mt = 0; mt < C::kMT; ++mt) {
+              o[t][mt][0] *= alpha[0];
+              o[t][mt][1] *= alpha[1];
+              o[t][mt][2] *= alpha[0];
+              o[t][mt][3] *= alpha[1];
+            }
+        }
+        // -- (P * value norms)^T as the B operand: hi/lo parts in C layout, transposed with movmatrix
+        const float vu0 = vn0 * v_unit, vu1 = vn1 * v_unit;
+        float pv[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) pv[e] = pr[e] * ((e >> 1) ? vu1 : vu0);
+        uint32_t pb[C::kNT][2];
+        if constexpr (NV <= 4) {
+          float x[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) x[e] = fmaf(pv[e], p_lo[e & 1], hi_f16(pv[e]) * p_hl[e & 1]);
+          pb[0][0] = ptx::movmatrix_trans(pack_f16(x[0], x[1]));
+          pb[0][1] = ptx::movmatrix_trans(pack_f16(x[2], x[3]));
+        } else {
+          float hi[4], lo[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            hi[e] = hi_f16(pv[e]);
+            lo[e] = pv[e] - hi[e];
+          }
+          pb[0][0] = ptx::movmatrix_trans(pack_f16(hi[0], hi[1]));
+          pb[0][1] = ptx::movmatrix_trans(pack_f16(hi[2], hi[3]));
+          pb[C::kNT - 1][0] = ptx::movmatrix_trans(pack_f16(lo[0], lo[1]));
+          pb[C::kNT - 1][1] = ptx::movmatrix_trans(pack_f16(lo[2], lo[3]));
+        }
+        // -- O^T += V^T . P^T: byte b of token t holds coordinates 2b (low nibble) and 2b + 1
+        //    (high nibble); pair tokens t, t + 1 into the index (code_t | code_t+1 << 4) of the
+        //    table, whose entry is then the A register (v_t, v_t+1) of one coordinate
+        uint32_t vx[4][D / 64];
+#pragma unroll
+        for (int k = 0; k < D / 64; ++k) {
+          vx[0][k] = (vw[0][k] & 0x0f0f0f0fu) | ((vw[1][k] << 4) & 0xf0f0f0f0u);
+          vx[1][k] = ((vw[0][k] >> 4) & 0x0f0f0f0fu) | (vw[1][k] & 0xf0f0f0f0u);
+          vx[2][k] = (vw[2][k] & 0x0f0f0f0fu) | ((vw[3][k] << 4) & 0xf0f0f0f0u);
+          vx[3][k] = ((vw[2][k] >> 4) & 0x0f0f0f0fu) | (vw[3][k] & 0xf0f0f0f0u);
+        }
+        ValueTiles<0, C::kMT, D, C::kNT>::run(o, vx, lutv, pb);
+      }
+      if constexpr (KS == kSideFP8) {
+        __syncwarp();  // every lane has read the stage
+        if (cur.more) issue_next();
+      }
     }
-  if (owner) {
-    // the warp's (o, m, l) is the partition's partial: m and l from the column owners, O^T
-    // from the staging buffer in 16-byte stores
-    if (gid == 0) {
+    if (stalled) break;
+
+    // ---- item epilogue: the partial (O^T with hi and lo columns added, back to absolute
+    //      units; running max and sum) straight from registers. Thread (gid, tig) holds, for
+    //      columns 2 tig + j, the D/8 consecutive coordinates (D/8) gid .. (D/8) gid + D/8 - 1:
+    //      O^T rows gid and gid + 8 of m-tile mt are coordinates 2 ((D/16) gid + mt) + {0, 1}.
+    const float o_unit = ldexpf(1.0f, ev_run - 127);
 #pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const int col = 2 * tig + j;
-        if (col < V) {
-          const size_t pi = (((size_t)b * a.T + col / G) * a.Hq + g * G + col % G) * a.P + p;
-          a.part_m[pi] = m_run[j];
-          a.part_l[pi] = l_run[j];
+    for (int j = 0; j < 2; ++j) {
+      l_run[j] += __shfl_xor_sync(kFull, l_run[j], 4);
+      l_run[j] += __shfl_xor_sync(kFull, l_run[j], 8);
+      l_run[j] += __shfl_xor_sync(kFull, l_run[j], 16);
+    }
+    float ov[C::kMT][4];
+#pragma unroll
+    for (int mt = 0; mt < C::kMT; ++mt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float v = o[0][mt][e];
+        if constexpr (NV == 8) v += o[C::kNT - 1][mt][e];
+        if constexpr (NV == 4) v += __shfl_xor_sync(kFull, v, 2);  // columns c, c + 4
+        if constexpr (NV == 2) v += __shfl_xor_sync(kFull, v, 1);  // columns c, c + 2
+        if constexpr (NV == 1) v += (e & 1) ? 0.0f : o[0][mt][e + 1];  // columns 0, 1
+        ov[mt][e] = v * o_unit;
+      }
+    const Item it3 = ring_item(ring, popped - 1);
+    const int slot = it3.p * a.ksub + it3.sub, vbase3 = 8 * it3.cg, V3 = min(NV, a.T * G - vbase3);
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int col = 2 * tig + j;
+      if (col < V3) {
+        const size_t row = query_row(a, it3.b, it3.g, G, vbase3 + col);
+        float4* dst = reinterpret_cast<float4*>(a.part_o + (row * PK + slot) * D + (D / 8) * gid);
+#pragma unroll
+        for (int q4 = 0; q4 < C::kMT / 2; ++q4)
+          dst[q4] = make_float4(ov[2 * q4][j], ov[2 * q4][j + 2], ov[2 * q4 + 1][j], ov[2 * q4 + 1][j + 2]);
+        if (gid == 0) {
+          a.part_m[row * PK + slot] = m_run[j];
+          a.part_l[row * PK + slot] = l_run[j];
         }
       }
     }
-    __syncwarp();
-    for (int idx = lane; idx < V * D / 4; idx += 32) {
-      const int v = idx / (D / 4), d = 4 * (idx % (D / 4));
-      const size_t pi = (((size_t)b * a.T + v / G) * a.Hq + g * G + v % G) * a.P + p;
-      *reinterpret_cast<float4*>(a.part_o + pi * D + d) = *reinterpret_cast<const float4*>(ep_w + v * DP + d);
-    }
-    __syncwarp();  // the staging buffer is rewritten by the warp's next partition
-    continue;
-  }
-  // shared partition: the warps' (o, m, l) merged into the partition's partial
-  if (gid == 0) {
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      ep_m[w * 8 + 2 * tig + j] = m_run[j];
-      ep_l[w * 8 + 2 * tig + j] = l_run[j];
-    }
-  }
-  __syncthreads();
-  for (int idx = tid; idx < V * D; idx += kThreads) {
-    const int v = idx / D, d = idx % D;
-    float M = -INFINITY;
-#pragma unroll
-    for (int ww = 0; ww < kWarps; ++ww) M = fmaxf(M, ep_m[ww * 8 + v]);
-    float acc = 0.0f, l = 0.0f;
-#pragma unroll
-    for (int ww = 0; ww < kWarps; ++ww) {
-      const float mw = ep_m[ww * 8 + v];
-      const float wt = mw == -INFINITY ? 0.0f : exp2f(mw - M);
-      acc += wt * ep_o[(ww * NV + v) * DP + d];
-      l += wt * ep_l[ww * 8 + v];
-    }
-    const size_t pi = (((size_t)b * a.T + v / G) * a.Hq + g * G + v % G) * a.P + p;
-    a.part_o[pi * D + d] = acc;
-    if (d == 0) {
-      a.part_m[pi] = M;
-      a.part_l[pi] = l;
-    }
-  }
-  __syncthreads();  // the merge buffer is rewritten by the next partition
-  }  // partitions
+  }  // items
 
   if (stalled) {
     if (lane == 0) atomicOr(a.err, DA_DEVERR_TIMEOUT);
@@ -790,18 +792,19 @@ cudaError_t launch_fixed(const Args& a, cudaStream_t s) {
   static DeviceFlags attr;
   cudaError_t e = ensure_dynamic_smem(kern, C::kSmem, attr);
   if (e != cudaSuccess) return e;
-  static int per_sm = 0, sms[64] = {};
-  if (per_sm == 0 &&
-      (e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, C::kThreads, C::kSmem)) != cudaSuccess)
+  static int sms[64] = {};
+  int dev = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (sms[dev] == 0 && (e = cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
     return e;
-  // where there are partitions enough, each warp owns whole partitions and a CTA takes kWarps
-  // (or a multiple) consecutive ones
-  b.ppc = partitions_per_cta(a, per_sm, sms);
-  b.owner = warps_own_partitions(a, per_sm, C::kWarps, 1, sms);  // from half a partition per resident warp
-  if (b.owner) b.ppc = C::kWarps * ((b.ppc + C::kWarps - 1) / C::kWarps);
+  // one CTA per SM, fewer when the call has fewer items than the grid has warps
+  const long long items = (long long)a.B * a.Hkv * a.P * a.ncg * a.ksub;
+  const long long ctas = (items + C::kWarps - 1) / C::kWarps;
+  const int grid = (int)(ctas < sms[dev] ? (ctas > 0 ? ctas : 1) : sms[dev]);
   // scheduled during the previous kernel's last CTAs (the query rotation, for codebook keys);
   // waits in-kernel before its first read
-  return launch_pdl(kern, dim3((a.P + b.ppc - 1) / b.ppc, a.Hkv, a.B), dim3(C::kThreads), C::kSmem, s, b, km, vm, nm);
+  return launch_pdl(kern, dim3(grid), dim3(C::kThreads), C::kSmem, s, b, km, vm, nm);
 }
 
 template <int KS, int D, bool CAP>
@@ -810,7 +813,7 @@ cudaError_t launch_nv(const Args& a, cudaStream_t s) {
   if (v <= 1) return launch_fixed<KS, D, 1, CAP>(a, s);
   if (v <= 2) return launch_fixed<KS, D, 2, CAP>(a, s);
   if (v <= 4) return launch_fixed<KS, D, 4, CAP>(a, s);
-  if (v <= 8) return launch_fixed<KS, D, 8, CAP>(a, s);
+  if (v <= kMaxColumns) return launch_fixed<KS, D, 8, CAP>(a, s);  // 8 columns per item, a.ncg column groups
   return cudaErrorInvalidValue;
 }
 

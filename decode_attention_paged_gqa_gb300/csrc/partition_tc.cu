@@ -19,8 +19,10 @@
 //
 // Multi-token decode (T query tokens per sequence at positions L-T .. L-1): the columns are
 // the group's (query token, head) pairs, each masked at its own token's causal (and window)
-// limit; T * G <= 8. ALiBi slopes, when given, add slope_h * (t - pos) to each column's
-// scores.
+// limit. Up to 8 pairs share one CTA's columns; more (T * G <= 32) are split into column
+// groups of 8, one CTA each, adjacent in the grid so that the pages they all read are
+// fetched from DRAM once and from L2 by the others. ALiBi slopes, when given, add
+// slope_h * (t - pos) to each column's scores.
 //
 // (attention.rs README: split-K decode kernels per KV format and m16n8k16 tensor-core MMA
 // with async copies on SM100-class GPUs; turboquant-rs 0.4.1, src/cache/cuda/attention.rs:
@@ -49,8 +51,9 @@ constexpr int kPage = 16;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr unsigned kFull = 0xffffffffu;
 
-// NV: the group's (query token, head) pairs ("virtual heads" v = jq * G + h) padded to a
-// power of two <= 8; with one query token NV = G.
+// NV: the CTA's columns: the group's (query token, head) pairs ("virtual heads" v = jq * G + h)
+// padded to a power of two <= 8 (8 when there are several column groups); with one query
+// token NV = G.
 template <int FMT, int D, int NV>
 struct Tc {
   static constexpr int kElemBytes = FMT == DA_KV_BF16 ? 2 : 1;
@@ -114,13 +117,14 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 3 : 2)
   // the warp index through a shuffle from lane 0, which the compiler then treats as uniform
   const int tid = threadIdx.x, lane = tid & 31, w = __shfl_sync(kFull, tid >> 5, 0);
   const int gid = lane >> 2, tig = lane & 3;
-  const int G = a.Hq / a.Hkv, V = a.T * G;  // group size; virtual heads in use (<= NV)
+  // the CTA's columns: virtual heads (query token, head of the group) vbase .. vbase + V - 1
+  const int G = a.Hq / a.Hkv, vbase = 8 * (blockIdx.x % a.ncg), V = min(NV, a.T * G - vbase);
   ptx::grid_dependency_wait();   // what the kernel before this one writes (q, the rotated q, ...)
   ptx::grid_dependents_launch();  // the reduce may be scheduled once every CTA has started
   const int L = load_len(a, b, blockIdx.x == 0 && g == 0 && tid == 0);
   const int np = seq_partitions(L, a.T, a.window, a.psize, a.thresh);
   // this CTA's partitions of (b, g)
-  const int p_begin = blockIdx.x * a.ppc, p_end = min(p_begin + a.ppc, np);
+  const int p_begin = (blockIdx.x / a.ncg) * a.ppc, p_end = min(p_begin + a.ppc, np);
   if (p_begin >= p_end) return;
 
   extern __shared__ unsigned char smem_raw[];
@@ -183,7 +187,7 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 3 : 2)
   for (int k = 0; k < T::kStages && cur.more; ++k) issue_next();
 
   // ---- query fragments (B operand of S^T): column n holds virtual head (n % NV) % V
-  const int qv = (gid % NV) % V;
+  const int qv = vbase + (gid % NV) % V;
   const uint16_t* qrow = a.q + (((size_t)b * a.T + qv / G) * a.Hq + g * G + qv % G) * D;
   uint32_t qf[T::kKS][2];
   float score_scale = a.scale * kLog2e;  // applied to the MMA result (log2 domain)
@@ -227,7 +231,7 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 3 : 2)
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
     part[j] = NV <= 4 ? (2 * tig + j) / NV : 0;
-    pos_c[j] = L - a.T + (((2 * tig + j) % NV) % V) / G;
+    pos_c[j] = L - a.T + (vbase + ((2 * tig + j) % NV) % V) / G;
     lo_w[j] = window_start(pos_c[j], a.window);
   }
   // ALiBi: the slope of each column's query head, in the log2 domain of the scores
@@ -235,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 3 : 2)
   float slope_c[2] = {0.0f, 0.0f};
   if (alibi) {
 #pragma unroll
-    for (int j = 0; j < 2; ++j) slope_c[j] = __ldg(a.alibi + g * G + (((2 * tig + j) % NV) % V) % G) * kLog2e;
+    for (int j = 0; j < 2; ++j) slope_c[j] = __ldg(a.alibi + g * G + (vbase + ((2 * tig + j) % NV) % V) % G) * kLog2e;
   }
   float* ep_o = reinterpret_cast<float*>(smem_gen + T::kStageSmem);  // [kWarps][NV][DP]
   float* ep_m = ep_o + kWarps * NV * DP;                              // [kWarps][8]
@@ -252,6 +256,7 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 3 : 2)
   int first_page, npages;
   range_pages(r, first_page, npages);
   const int nw = warp_pages(npages, pg_off, pg_step);
+  const bool rev = walk_reversed(owner, p);  // odd owned partitions: last page first
   // tokens each column attends in this partition, and the pages that need no mask in any
   // column: [lo_all, hi_all) (warp-uniform)
   int lo_c[2], hi_c[2];
@@ -287,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 3 : 2)
     }
     if (!stalled && (valid_mask & (1u << s))) {
       const uint32_t kb = stage0 + s * T::kStageBytes + koff, vb = stage0 + s * T::kStageBytes + voff;
-      const int tok0 = (first_page + pg_off + pg_step * i) * kPage;
+      const int tok0 = (first_page + walk_page(i, nw, pg_off, pg_step, rev)) * kPage;
       // -- S^T = K . Q^T, the k-steps alternating between two accumulators (two dependent MMA
       //    chains of half the length), added at the end
       float sc[4] = {0.0f, 0.0f, 0.0f, 0.0f}, sc2[4] = {0.0f, 0.0f, 0.0f, 0.0f};
@@ -427,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 3 : 2)
       for (int j = 0; j < 2; ++j) {
         const int col = 2 * tig + j;
         if (col < V) {
-          const size_t pi = (((size_t)b * a.T + col / G) * a.Hq + g * G + col % G) * a.P + p;
+          const size_t pi = query_row(a, b, g, G, vbase + col) * a.P + p;
           a.part_m[pi] = m_run[j];
           a.part_l[pi] = l_run[j];
         }
@@ -436,7 +441,7 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 3 : 2)
     __syncwarp();
     for (int idx = lane; idx < V * D / 4; idx += 32) {
       const int v = idx / (D / 4), d = 4 * (idx % (D / 4));
-      const size_t bh = ((size_t)b * a.T + v / G) * a.Hq + g * G + v % G;
+      const size_t bh = query_row(a, b, g, G, vbase + v);
       const float4 x = *reinterpret_cast<const float4*>(ep_w + v * DP + d);
       if (direct) {  // the caller's output is only 4-byte aligned
         float* dst = a.out + bh * D + d;
@@ -485,7 +490,7 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 3 : 2)
       acc += wt * ep_o[(ww * NV + v) * DP + d];
       l += wt * ep_l[ww * 8 + v];
     }
-    const size_t bh = ((size_t)b * a.T + v / G) * a.Hq + g * G + v % G;
+    const size_t bh = query_row(a, b, g, G, vbase + v);
     if (direct) {
       a.out[bh * D + d] = l > 0.0f ? acc * out_scale / l : 0.0f;
     } else {
@@ -586,7 +591,7 @@ cudaError_t launch_fixed(const Args& a, cudaStream_t s) {
   if (b.owner) b.ppc = kWarps * ((b.ppc + kWarps - 1) / kWarps);
   // scheduled during the previous kernel's last CTAs (the query rotation, for codebook keys);
   // waits in-kernel before its first read
-  return launch_pdl(kern, dim3((a.P + b.ppc - 1) / b.ppc, a.Hkv, a.B), dim3(kThreads), T::kSmem, s, b, km, vm);
+  return launch_pdl(kern, dim3((a.P + b.ppc - 1) / b.ppc * a.ncg, a.Hkv, a.B), dim3(kThreads), T::kSmem, s, b, km, vm);
 }
 
 template <int FMT, int D, bool CAP>
@@ -595,7 +600,7 @@ cudaError_t launch_nv(const Args& a, cudaStream_t s) {
   if (v <= 1) return launch_fixed<FMT, D, 1, CAP>(a, s);
   if (v <= 2) return launch_fixed<FMT, D, 2, CAP>(a, s);
   if (v <= 4) return launch_fixed<FMT, D, 4, CAP>(a, s);
-  if (v <= 8) return launch_fixed<FMT, D, 8, CAP>(a, s);
+  if (v <= kMaxColumns) return launch_fixed<FMT, D, 8, CAP>(a, s);  // 8 columns per CTA, a.ncg CTAs
   return cudaErrorInvalidValue;
 }
 

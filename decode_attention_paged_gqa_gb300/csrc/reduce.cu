@@ -5,6 +5,9 @@
 //
 // For sequence b, head h with partials (o_p, m_p, l_p), p < P_b (m in log2 units):
 //   M = max_p m_p,  w_p = 2^(m_p - M),  out = sum_p w_p o_p / sum_p w_p l_p.
+// When the partition kernel dealt each partition's pages to ksub sub-items, every sub-item
+// that had pages wrote a partial of its own, and all of them are combined the same way
+// (sub-item s of partition p has pages when s < the partition's page count).
 // One CTA per (row, head); the partials' loads are issued together: m_p and l_p in one round,
 // the float4 columns of o_p in one or two more, with the partitions spread over thread groups
 // (128 threads: 4 groups at D = 128, 2 at D = 256; 256 threads, for 32 or more partitions: 8 / 4).
@@ -51,15 +54,21 @@ __global__ void __launch_bounds__(kThreads) reduce_kernel(const Args a) {
     for (int d = tid; d < D; d += kThreads) out[d] = 0.0f;
     return;
   }
-  if (np == 1 && !kUnrotate) return;
-  const size_t base = ((size_t)row * a.Hq + h) * a.P;
+  if (np == 1 && a.ksub == 1 && !kUnrotate) return;
+  const int PK = a.P * a.ksub, nk = np * a.ksub;  // partial slots per row; those of this row
+  const size_t base = ((size_t)row * a.Hq + h) * PK;
 
-  // M = max_p m_p and s = sum_p 2^(m_p - M) l_p, each thread folding its partitions
-  // p = tid, tid + kThreads, ... (m_p and l_p loaded together), then across the block
+  // M = max_p m_p and s = sum_p 2^(m_p - M) l_p, each thread folding its partials
+  // j = tid, tid + kThreads, ... (m_p and l_p loaded together), then across the block
   float M = -INFINITY, s = 0.0f;
-  for (int p = tid; p < np; p += kThreads) {
-    const float m = a.part_m[base + p], l = a.part_l[base + p];
-    w_s[p] = m;
+  for (int j = tid; j < nk; j += kThreads) {
+    bool valid = true;
+    if (a.ksub > 1) {  // sub-item j % ksub of partition j / ksub: written iff it had pages
+      const Range r = partition_range(L, a.T, j / a.ksub, a.window, a.psize, a.thresh);
+      valid = j % a.ksub < (r.end - 1) / kBlockSize - r.start / kBlockSize + 1;
+    }
+    const float m = valid ? a.part_m[base + j] : -INFINITY, l = valid ? a.part_l[base + j] : 0.0f;
+    w_s[j] = m;
     fold(M, s, m, l);
   }
 #pragma unroll
@@ -76,7 +85,7 @@ __global__ void __launch_bounds__(kThreads) reduce_kernel(const Args a) {
   s = red_s[0];
 #pragma unroll
   for (int i = 1; i < kThreads / 32; ++i) fold(M, s, red_m[i], red_s[i]);
-  for (int p = tid; p < np; p += kThreads) w_s[p] = M == -INFINITY ? 0.0f : exp2f(w_s[p] - M);
+  for (int j = tid; j < nk; j += kThreads) w_s[j] = M == -INFINITY ? 0.0f : exp2f(w_s[j] - M);
   __syncthreads();
 
   // sum_p w_p o_p: thread (group, column) takes float4 column `col` of partitions
@@ -85,9 +94,10 @@ __global__ void __launch_bounds__(kThreads) reduce_kernel(const Args a) {
   const float4* src = reinterpret_cast<const float4*>(a.part_o + base * D) + col;
   float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
 #pragma unroll 8
-  for (int p = group; p < np; p += kGroups) {
-    const float wp = w_s[p];
-    const float4 o = src[(size_t)p * kCols];
+  for (int j = group; j < nk; j += kGroups) {
+    const float wp = w_s[j];
+    if (wp == 0.0f) continue;  // an empty partial, or a sub-item slot that was never written
+    const float4 o = src[(size_t)j * kCols];
     acc.x = fmaf(wp, o.x, acc.x);
     acc.y = fmaf(wp, o.y, acc.y);
     acc.z = fmaf(wp, o.z, acc.z);
@@ -116,12 +126,12 @@ __global__ void __launch_bounds__(kThreads) reduce_kernel(const Args a) {
 template <int D>
 cudaError_t launch_d(const Args& a, cudaStream_t s) {
   dim3 grid(a.Hq, a.B * a.T);
-  const size_t smem = sizeof(float) * (size_t)a.P;  // P <= kMaxPartitions: within the default 48 KB
+  const size_t smem = sizeof(float) * (size_t)a.P * a.ksub;  // <= kMaxPartitions: within the default 48 KB
   // scheduled during the partition kernel's last CTAs; waits for its partials in-kernel. Many
   // partitions per row: 256 threads, so each thread's loads are one round; few: 128, so that a
   // large batch's rows stay within one wave of CTAs.
   const bool rot = is_codebook(v_side(a.fmt));
-  if (a.P >= 32)
+  if (a.P * a.ksub >= 32)
     return rot ? launch_pdl(reduce_kernel<D, true, 256>, grid, dim3(256), smem, s, a)
                : launch_pdl(reduce_kernel<D, false, 256>, grid, dim3(256), smem, s, a);
   return rot ? launch_pdl(reduce_kernel<D, true, 128>, grid, dim3(128), smem, s, a)

@@ -96,7 +96,7 @@ typedef struct da_params {
   int32_t query_len;          /* T >= 1 query tokens per sequence (0 counts as 1). T = 1 is ordinary
                                  decode; T > 1 is multi-token decode with a causal mask: query token j
                                  sits at position L_b - T + j and attends positions up to its own (the
-                                 last `window` of them when a window is set). T * G <= 8. */
+                                 last `window` of them when a window is set). T * G <= 32. */
   int32_t num_q_heads;        /* Hq >= 1 */
   int32_t num_kv_heads;       /* Hkv >= 1, Hq % Hkv == 0; group size G = Hq / Hkv in {1, 2, 4, 8} */
   int32_t head_dim;           /* D in {128, 256} */

@@ -62,7 +62,8 @@ def test_window_and_softcap(fmt, window, softcap):
 
 @pytest.mark.parametrize("fmt", ["bf16", "fp8", "cb4", "fp8k_cb4v", "cb3k_cb4v"])
 @pytest.mark.parametrize("schedule", [1, 2])
-@pytest.mark.parametrize("D,G,T,window", [(128, 4, 1, 0), (256, 2, 1, 700), (128, 2, 3, 0), (128, 8, 1, 0)])
+@pytest.mark.parametrize("D,G,T,window", [(128, 4, 1, 0), (256, 2, 1, 700), (128, 2, 3, 0), (128, 8, 1, 0),
+                                          (128, 4, 4, 300)])
 def test_partition_schedules(fmt, schedule, D, G, T, window):
     """Both ways of dealing a CTA's partitions to its warps (shared by the warps, or each warp
     owning whole partitions), with the automatic and with three partitions per CTA (rounded up
@@ -287,11 +288,13 @@ def test_rising_scores(fmt):
     assert_close(run_gpu(c), run_oracle(c), f"{fmt} rising scores")
 
 
-@pytest.mark.parametrize("fmt", ["bf16", "fp8", "cb4", "fp8k_cb4v"])
-@pytest.mark.parametrize("T,G,window", [(2, 4, 0), (4, 2, 0), (3, 2, 700), (8, 1, 0), (2, 1, 1000), (5, 1, 64)])
+@pytest.mark.parametrize("fmt", ["bf16", "fp8", "cb4", "fp8k_cb4v", "cb3k_cb4v"])
+@pytest.mark.parametrize("T,G,window", [(2, 4, 0), (4, 2, 0), (3, 2, 700), (8, 1, 0), (2, 1, 1000), (5, 1, 64),
+                                        (4, 4, 0), (8, 4, 0), (4, 8, 0), (3, 4, 900), (5, 4, 0), (32, 1, 0)])
 def test_multi_token_causal(fmt, T, G, window):
     """T query tokens per sequence at positions L-T .. L-1, each attending positions up to its
-    own (multi-token / speculative decode)."""
+    own (multi-token / speculative decode). More than 8 (query token, head) pairs are split
+    into column groups of 8, one CTA each (T * G up to 32)."""
     lens = [3, 17, 600, 1024, 1030, 2500]  # includes fewer tokens than queries
     spec = wl.WorkloadSpec(f"mt_{fmt}", len(lens), 2 * G, 2, 128, fmt, 0, max(lens), seed=T * 10 + G, window=window,
                            query_len=T)
@@ -304,7 +307,7 @@ def test_multi_token_causal(fmt, T, G, window):
 def test_multi_token_group_too_wide_is_rejected():
     import decode_attention_paged_gqa_gb300 as da
 
-    spec = wl.WorkloadSpec("wide", 2, 8, 2, 128, "bf16", 10, 40, seed=1, query_len=3)  # 3 x 4 > 8
+    spec = wl.WorkloadSpec("wide", 2, 8, 2, 128, "bf16", 10, 40, seed=1, query_len=9)  # 9 x 4 > 32
     c = make_case(spec)
     with pytest.raises(da.DecodeAttnError) as e:
         run_gpu(c)

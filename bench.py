@@ -159,10 +159,12 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------- inputs
-def build_inputs(spec, encode_on_gpu=True):
+def build_inputs(spec, encode_on_gpu=True, writer_times=None):
     """Seeded inputs on the host for the chosen workload. BF16 caches come straight from the
     generator; FP8 and codebook caches are written on the GPU by the library's own encoders
     from the seeded fp32 source (and copied back to the host for the end-to-end leg).
+    writer_times: a dict that receives, per cache side, the cache writer's device time
+    (CUDA events around its launches) and the vectors (rows of D) it wrote.
     Returns (layout, host tensors, fp32 sources or None)."""
     import math
 
@@ -194,16 +196,29 @@ def build_inputs(spec, encode_on_gpu=True):
         sg_d = host["sign"].cuda()
     for w, side in zip(("k", "v"), sides):
         x = src[w].cuda()
+        ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
         if side == "fp8":
             codes = torch.empty(x.shape, dtype=torch.uint8, device="cuda")
             sc = torch.empty(1, dtype=torch.float32, device="cuda")
+            torch.cuda.synchronize()
+            ev[0].record()
             da.decode_attn_encode_fp8(x, x.numel(), codes, sc)
+            ev[1].record()
         else:
             bits = 3 if side == "cb3" else 4
             codes = torch.empty(x.shape[:-1] + (D * bits // 8,), dtype=torch.uint8, device="cuda")
             sc = torch.empty(x.shape[:-1], dtype=torch.float32, device="cuda")
-            da.decode_attn_encode_codebook(x, x.numel() // D, D, bits, sg_d, cbs[bits].cuda(), codes, sc)
+            cb_d = cbs[bits].cuda()
+            torch.cuda.synchronize()
+            ev[0].record()
+            da.decode_attn_encode_codebook(x, x.numel() // D, D, bits, sg_d, cb_d, codes, sc)
+            ev[1].record()
         torch.cuda.synchronize()
+        if writer_times is not None:
+            ms = ev[0].elapsed_time(ev[1])
+            nvec = x.numel() // D
+            writer_times[w] = {"format": side, "vectors": nvec, "ms": ms, "ns_per_vector": ms * 1e6 / nvec,
+                               "input_gbs": x.numel() * 4 / (ms * 1e-3) / 1e9}
         host[w], host[w + "_scales"] = codes.cpu(), sc.cpu()
         del x
     return lay, host, src
@@ -363,7 +378,8 @@ class Prepared:
         from decode_attention_paged_gqa_gb300.metrics import algorithmic_kv_bytes
 
         self.spec = spec
-        self.lay, self.host, self.src = build_inputs(spec)
+        self.writer_times = {}
+        self.lay, self.host, self.src = build_inputs(spec, writer_times=self.writer_times)
         self.dev = {k: (None if t is None else t.cuda()) for k, t in self.host.items()}
         self.kv_bytes = algorithmic_kv_bytes(self.lay.context_lens, spec.window, spec.num_kv_heads, spec.kv_format,
                                              spec.head_dim)
@@ -487,6 +503,8 @@ def per_workload_entries(names, K, warmup, peak, local, with_cpu, cpu_seconds):
              "gpu_launches": K * KERNELS_PER_CALL[spec.kv_format]}
         if prep.cache_bytes <= L2_BYTES:
             e["note"] = "L2-resident and latency-bound: not compared with the HBM peak"
+        if prep.writer_times:  # the cache writers that filled this workload's quantised caches
+            e["cache_writers"] = prep.writer_times
         if with_cpu and spec.name == "tiny_bf16":
             oracle.build()
             e["cpu_baseline"] = {"all_cores": cpu_baseline_entry(spec, prep, cpu_seconds),

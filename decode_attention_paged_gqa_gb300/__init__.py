@@ -7,6 +7,7 @@ ctypes binding (``_binding``) plus the seeded synthetic input generators (``work
 from ._binding import (  # noqa: F401
     DA_DEVERR_BLOCK_ID,
     DA_DEVERR_CONTEXT_LEN,
+    DA_DEVERR_SMEM_LAYOUT,
     DA_DEVERR_TIMEOUT,
     DA_KV_BF16,
     DA_KV_CB3K_CB4V,

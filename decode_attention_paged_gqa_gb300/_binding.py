@@ -20,7 +20,7 @@ KV_FORMATS = {"bf16": DA_KV_BF16, "fp8": DA_KV_FP8_E4M3, "cb4": DA_KV_CB4, "fp8k
               "cb3k_cb4v": DA_KV_CB3K_CB4V}
 DA_OK, DA_ERR_INVALID_ARG, DA_ERR_UNSUPPORTED, DA_ERR_WORKSPACE, DA_ERR_LAUNCH, DA_ERR_CUDA = 0, -1, -2, -3, -4, -5
 DA_ERR_STATIC_WORKSPACE = -6
-DA_DEVERR_BLOCK_ID, DA_DEVERR_CONTEXT_LEN, DA_DEVERR_TIMEOUT = 0x1, 0x2, 0x4
+DA_DEVERR_BLOCK_ID, DA_DEVERR_CONTEXT_LEN, DA_DEVERR_TIMEOUT, DA_DEVERR_SMEM_LAYOUT = 0x1, 0x2, 0x4, 0x8
 
 
 class DecodeAttnError(RuntimeError):

@@ -74,4 +74,45 @@ __device__ __forceinline__ bool page_softmax(const float (&sc)[4], float (&m)[2]
   return moved_any;
 }
 
+// ---- one column per thread: the thread holds the scores of tokens gid (s[0]) and gid + 8
+//      (s[1]) of a single column (the layout in which a column pair carries one head's hi and
+//      lo parts). The running max starts at kNoMax, a finite stand-in for "nothing seen yet":
+//      the first finite score always moves it, masked (-inf) scores give 2^-inf = 0, and an
+//      all-masked column keeps (kNoMax, 0), which a combine weighs with 2^(kNoMax - M) = 0.
+constexpr float kNoMax = -3.4028234663852886e38f;  // -FLT_MAX
+
+// Tokens outside [lo, hi) get -inf (no weight).
+__device__ __forceinline__ void mask_page_col(float (&s)[2], int tok0, int gid, int lo, int hi) {
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    const int t = tok0 + gid + 8 * e;
+    if (t < lo || t >= hi) s[e] = -INFINITY;
+  }
+}
+
+// One page of one column: updates (m, l), returns the probabilities relative to the new
+// reference and the factor alpha the column's running output must be multiplied by; true if
+// any column of the warp moved its reference.
+__device__ __forceinline__ bool page_softmax_col(const float (&s)[2], float& m, float& l, float& alpha,
+                                                 float (&pr)[2]) {
+  alpha = 1.0f;
+  bool moved_any = false;
+  if (__any_sync(0xffffffffu, fmaxf(s[0], s[1]) > m + kLazyLog2)) {
+    float mx = fmaxf(s[0], s[1]);
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+    const bool move = mx > m + kLazyLog2;
+    if (move) {
+      alpha = exp2_fast(m - mx);  // 2^(kNoMax - mx) = 0 clears the (zero) state
+      m = mx;
+    }
+    moved_any = __any_sync(0xffffffffu, move);
+  }
+  pr[0] = exp2_fast(s[0] - m);
+  pr[1] = exp2_fast(s[1] - m);
+  l = fmaf(l, alpha, pr[0] + pr[1]);
+  return moved_any;
+}
+
 }  // namespace da

@@ -22,8 +22,15 @@
 // per byte: a 256-entry table maps a byte (two 4-bit codes) to the f16 pair (cb[lo], cb[hi]) --
 // for 3-bit keys a 64-entry table maps a 6-bit pair of codes. Entry e sits at byte 256 e and is
 // replicated 32 times there, copy l in bank l, so the lanes of a warp never conflict whatever
-// codes they look up, and the permute that extracts a byte also places it at bits 8..15 next to
-// the lane's copy offset (4 l), giving the load address in one instruction.
+// codes they look up. The table starts on a 64 KB boundary of the shared window, so the permute
+// that extracts a byte (bits 8..15) and joins it with the lane's copy offset (4 l, bits 0..7)
+// and the table's base (bits 16..31) gives the whole load address in one instruction.
+//
+// Columns: with up to four (query token, head) pairs the 8 MMA columns are pairs: column 2h
+// carries pair h with the query's (and the probabilities') hi part, column 2h + 1 the lo part,
+// so the thread that owns a pair's scores owns both halves (adding them is one register add)
+// and each thread runs the online softmax of one pair over two tokens. With more pairs (8 per
+// item) the lo parts take a second MMA / second column tile.
 //
 // The dot product's coordinate order is free, so each thread takes the coordinates that sit in
 // a contiguous run of its key rows: thread (gid, tig) reads D/8 bytes of K rows gid and gid + 8,
@@ -32,9 +39,8 @@
 // coordinates of one byte, and byte-wise logic pairs the codes of two tokens into one index.
 //
 // Precision: the rotated query is split q = q_hi + q_lo (both f16, after scaling by a power of
-// two), the lo half riding in the spare columns of S^T (up to four columns) or in a second MMA,
-// so the scores carry only the rounding of the codebook values to f16 (2^-12 relative); P is
-// split hi + lo as in the BF16 kernel.
+// two), so the scores carry only the rounding of the codebook values to f16 (2^-12 relative);
+// P * ||v|| is split hi + lo the same way.
 //
 // (attention.rs README, KV Cache Formats table: the 4-bit Walsh-Hadamard codebook format and
 // split-K decode for it; turboquant-rs 0.4.1, src/cache/cuda/attention.rs: the fused kernel
@@ -63,6 +69,11 @@ constexpr int kPage = 16;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kSmemLimit = 227 * 1024;  // dynamic shared memory a CTA may use
+// Shared address at which the dynamic shared memory of a kernel without static shared memory
+// starts: the part of the CTA's window the system reserves (cudaDevAttrReservedSharedMemoryPerBlock,
+// checked by the launcher).
+constexpr int kDynStart = 1024;
+constexpr int kLutAlign = 65536;  // the lookup tables start on a 64 KB boundary
 
 constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
 
@@ -71,7 +82,8 @@ constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
 // to a power of two <= 8 (8 when more than 8 pairs are split into column groups).
 template <int KS, int D, int NV>
 struct Cb {
-  // 16 warps where 128 registers per thread suffice (D = 128, up to four columns), else 8
+  static constexpr bool kPaired = NV <= 4;  // column 2h / 2h + 1: hi / lo part of pair h
+  // 16 warps where 128 registers per thread suffice (D = 128, up to four pairs), else 8
   static constexpr int kWarps = (D == 128 && NV <= 4) ? 16 : 8;
   static constexpr int kThreads = 32 * kWarps;
   static constexpr int kKRow = row_bytes(KS, D);  // bytes of one key row
@@ -90,23 +102,28 @@ struct Cb {
   static constexpr int kCodeBytes = align_up(kOffV + kVBytes, kAlign);
   static constexpr int kNormBytes = 128;                            // per stage: K norms, V norms
   static constexpr int kTxBytes = kKBytes + kVBytes + (kKNorms ? 64 : 0) + 64;
-  // lookup tables: entry e at byte 256 e, the copy of lane l at + 4 l
+  // lookup tables: entry e at byte 256 e, the copy of lane l at + 4 l; the value table at the
+  // first 64 KB boundary of the window, the 3-bit key table right behind it
   static constexpr int kLutV = 256 * 256;
   static constexpr int kLutK = KS == kSideCB3 ? 64 * 256 : 0;
-  static constexpr int kOffCodes = kLutV + kLutK;
-  // per warp: ring of item descriptors and walk state; per stage: mbarrier
-  static constexpr int kFixed = kOffCodes + kWarps * ItemIssue::kStateBytes + 1024;  // + alignment slack
-  static constexpr int kFit = (kSmemLimit - kFixed - kWarps * 8 * 8) / (kWarps * (kCodeBytes + kNormBytes));
-  static constexpr int kStages = kFit > 6 ? 6 : kFit;
-  static_assert(kStages >= 2, "shared memory holds fewer than two stages per warp");
-  static constexpr int kOffNorms = kOffCodes + kWarps * kStages * kCodeBytes;
-  static constexpr int kOffRing = kOffNorms + kWarps * kStages * kNormBytes;
-  static constexpr int kOffBars = kOffRing + kWarps * ItemIssue::kStateBytes;
-  static constexpr int kSmem = kOffBars + kWarps * kStages * 8 + 1024;
-  static_assert(kSmem <= kSmemLimit, "shared memory budget exceeded");
-  static constexpr int kNT = NV <= 4 ? 1 : 2;           // P.V column tiles
-  static constexpr int kMT = D / 16;                    // O^T row tiles
-  static constexpr int kKS = D / 16;                    // k-steps of S^T
+  // Each warp's block: its code stages, norm slots, walk state (ring) and mbarriers. The blocks
+  // fill the space before the tables (region A) and after them (region B).
+  static constexpr int block_bytes(int s) {
+    return align_up(s * (kCodeBytes + kNormBytes) + ItemIssue::kStateBytes + 8 * s, kAlign);
+  }
+  static constexpr int kRegionA = kLutAlign - align_up(kDynStart, kAlign);
+  static constexpr int kRegionB = kDynStart + kSmemLimit - kLutAlign - kLutV - kLutK;
+  static constexpr bool fits(int s) { return kRegionA / block_bytes(s) + kRegionB / block_bytes(s) >= kWarps; }
+  static constexpr int kStages = fits(6) ? 6 : fits(5) ? 5 : fits(4) ? 4 : fits(3) ? 3 : 2;
+  static_assert(fits(kStages), "shared memory holds fewer than two stages per warp");
+  static constexpr int kBlock = block_bytes(kStages);
+  static constexpr int kOffNorms = kStages * kCodeBytes;  // within a block
+  static constexpr int kOffRing = kOffNorms + kStages * kNormBytes;
+  static constexpr int kOffBars = kOffRing + ItemIssue::kStateBytes;
+  static constexpr int kSmem = kSmemLimit;
+  static constexpr int kNT = kPaired ? 1 : 2;  // P.V column tiles (the second: lo parts)
+  static constexpr int kMT = D / 16;           // O^T row tiles
+  static constexpr int kKS = D / 16;           // k-steps of S^T
 };
 
 __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
@@ -135,16 +152,16 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
 }
 __device__ __forceinline__ float ldsf(uint32_t addr) { return __uint_as_float(lds32(addr)); }
 
-// A lookup table as seen by one lane: the table's address and the lane's copy offset.
+// A lookup table as seen by one lane: the table's base (a multiple of 64 KB) joined with the
+// lane's copy offset 4 * lane.
 struct Lut {
-  uint32_t base;   // shared address of entry 0 (entries 256 bytes apart)
-  uint32_t lane4;  // 4 * lane
+  uint32_t lanebase;
 };
-// Entry (byte J of w) of the lane's copy: the permute puts the byte at bits 8..15 and the
-// lane's offset at bits 0..7.
+// Entry (byte J of w) of the lane's copy: the permute takes bits 0..7 (lane offset) and 16..31
+// (table base) from lanebase and puts the byte at bits 8..15.
 template <int J>
 __device__ __forceinline__ uint32_t lut_byte(const Lut& t, uint32_t w) {
-  return lds32(t.base + __byte_perm(w, t.lane4, 0x5504 | (J << 4)));
+  return lds32(__byte_perm(w, t.lanebase, 0x7604 | (J << 4)));
 }
 // byte J of a little-endian word array
 template <int J>
@@ -152,7 +169,7 @@ __device__ __forceinline__ uint32_t lut_byte_of(const Lut& t, const uint32_t* w)
   return lut_byte<J & 3>(t, w[J >> 2]);
 }
 // Entry (6-bit field J, bits 6J .. 6J + 5 of a little-endian word array) of the lane's copy:
-// the field is moved to bits 8..13 by one shift, then masked and joined with the lane's offset.
+// the field is moved to bits 8..13 by one shift, then masked and joined with lanebase.
 template <int J>
 __device__ __forceinline__ uint32_t lut_field6(const Lut& t, const uint32_t* w) {
   constexpr int bit = 6 * J, wi = bit >> 5, sh = bit & 31;
@@ -163,7 +180,7 @@ __device__ __forceinline__ uint32_t lut_field6(const Lut& t, const uint32_t* w) 
     x = w[wi] >> (sh - 8);
   else
     x = __funnelshift_r(w[wi], w[wi + 1], sh - 8);  // the field crosses into the next word
-  return lds32(t.base + ((x & 0x3f00u) | t.lane4));
+  return lds32((x & 0x3f00u) | t.lanebase);
 }
 
 // A fragments of S^T for k-step S from the thread's key bytes (rows gid: k0, gid + 8: k1).
@@ -216,8 +233,9 @@ struct ValueTiles {
   }
 };
 
-// The thread's two columns of an item: the query position of each, and the positions it
-// attends within the partition, [lo, hi) (causal limit and window).
+// The thread's score columns of an item: the (query token, head) pair of each, its query
+// position, and the positions it attends within the partition, [lo, hi) (causal limit and
+// window). Paired layout: one pair (columns 2 tig, 2 tig + 1); else two (2 tig + j).
 struct Cols {
   int lo[2], hi[2], pos[2], vh[2];
 };
@@ -227,7 +245,7 @@ __device__ __forceinline__ Cols item_cols(const Args& a, const Item& it, const R
   Cols c;
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
-    c.vh[j] = vbase + ((2 * tig + j) % NV) % V;
+    c.vh[j] = vbase + (NV <= 4 ? tig % V : (2 * tig + j) % V);
     c.pos[j] = it.L - a.T + c.vh[j] / G;
     c.lo[j] = max(window_start(c.pos[j], a.window), r.start);
     c.hi[j] = min(c.pos[j] + 1, r.end);
@@ -242,6 +260,7 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 1)
                         const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap nmap) {
   using C = Cb<KS, D, NV>;
   constexpr int kWarps = C::kWarps, kThreads = C::kThreads;
+  constexpr bool kPaired = C::kPaired;
   // the warp index through a shuffle from lane 0, which the compiler then treats as uniform
   const int tid = threadIdx.x, lane = tid & 31, w = __shfl_sync(kFull, tid >> 5, 0);
   const int gid = lane >> 2, tig = lane & 3;
@@ -249,12 +268,19 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 1)
   ptx::grid_dependency_wait();    // what the kernel before this one writes (q, the rotated q, ...)
   ptx::grid_dependents_launch();  // the reduce may be scheduled once every CTA has started
 
-  extern __shared__ unsigned char smem_raw[];
-  const uint32_t smem = (ptx::smem_u32(smem_raw) + 1023u) & ~1023u;
-  const uint32_t bar0 = smem + C::kOffBars + w * C::kStages * 8;
-  const uint32_t code0 = smem + C::kOffCodes + w * C::kStages * C::kCodeBytes;
-  const uint32_t norm0 = smem + C::kOffNorms + w * C::kStages * C::kNormBytes;
-  const uint32_t ring = smem + C::kOffRing + w * ItemIssue::kStateBytes;
+  // ---- shared memory: the lookup tables at the first 64 KB boundary of the window, the warps'
+  //      blocks before them (region A) and after them (region B)
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  const uint32_t start = ptx::smem_u32(smem_raw);
+  const uint32_t tbl = (start + (kLutAlign - 1)) & ~uint32_t(kLutAlign - 1);
+  const uint32_t a0 = (start + (C::kAlign - 1)) & ~uint32_t(C::kAlign - 1);
+  const int in_a = tbl > a0 ? (int)((tbl - a0) / C::kBlock) : 0;
+  const uint32_t blk = w < in_a ? a0 + w * C::kBlock : tbl + C::kLutV + C::kLutK + (w - in_a) * C::kBlock;
+  if (blk + C::kBlock > start + C::kSmem || tbl + C::kLutV + C::kLutK > start + C::kSmem) {
+    if (tid == 0) atomicOr(a.err, DA_DEVERR_SMEM_LAYOUT);  // the launcher checks this never happens
+    return;
+  }
+  const uint32_t code0 = blk, norm0 = blk + C::kOffNorms, ring = blk + C::kOffRing, bar0 = blk + C::kOffBars;
 
   if (lane == 0) {
     ptx::prefetch_tensor_map(&kmap);
@@ -330,7 +356,7 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 1)
   //      (cbk[lo], cbk[hi]) for 3-bit keys; entry e at word 64 e, 32 copies (word 64 e + l)
   {
     const float* cbv = a.codebook + (KS == kSideCB3 ? 8 : 0);
-    uint32_t* lv = reinterpret_cast<uint32_t*>(smem_raw + (smem - ptx::smem_u32(smem_raw)));
+    uint32_t* lv = reinterpret_cast<uint32_t*>(smem_raw + (tbl - start));
     for (int i = tid; i < 256 * 8; i += kThreads) {
       const int e = i >> 3;
       const uint32_t x = pack_f16(__ldg(cbv + (e & 15)), __ldg(cbv + (e >> 4)));
@@ -345,8 +371,8 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 1)
       }
     }
   }
-  const Lut lutv{smem, 4u * lane};
-  const Lut lutk{KS == kSideCB3 ? smem + C::kLutV : smem, 4u * lane};
+  const Lut lutv{tbl | (4u * lane)};
+  const Lut lutk{(KS == kSideCB3 ? tbl + C::kLutV : tbl) | (4u * lane)};
   __syncthreads();  // lookup tables written; from here on no warp waits for another
 
   const float cap = a.softcap;
@@ -360,16 +386,7 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 1)
   uint32_t cphase = 0;   // its mbarrier phase parity ((consumed / kStages) & 1)
   bool stalled = false;  // a copy never arrived: no more waits, copies or compute
   int q_b = -1, q_g = -1, q_cg = -1;  // (sequence, kv head, column group) of the loaded query fragments
-  // P column roles (NV <= 4: column c carries the hi part when c / NV == 0, the lo part when
-  // c / NV == 1, nothing beyond) as multipliers: x = p cl + h (ch - cl)
-  float p_lo[2], p_hl[2];
-#pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    const int part = NV <= 4 ? (2 * tig + j) / NV : 0;
-    p_lo[j] = part == 1 ? 1.0f : 0.0f;
-    p_hl[j] = part == 0 ? 1.0f : (part == 1 ? -1.0f : 0.0f);
-  }
-  uint32_t qf[C::kKS][2], ql[NV == 8 ? C::kKS : 1][2];
+  uint32_t qf[C::kKS][2], ql[kPaired ? 1 : C::kKS][2];
   float score_scale = 0.0f;
 
   while (!stalled) {
@@ -381,10 +398,12 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 1)
     // the item's columns: virtual heads vbase .. vbase + V - 1
     const int vbase = 8 * it.cg, V = min(NV, a.T * G - vbase);
 
-    // ---- query fragments (B operand of S^T). Column n scores virtual head vbase + (n % NV) % V.
+    // ---- query fragments (B operand of S^T). Paired: column n holds pair (n / 2) % V, its hi
+    //      part for even n, its lo part for odd n; else column n holds pair n % V (hi part) and
+    //      a second set of fragments the lo parts.
     if (b != q_b || g != q_g || it.cg != q_cg) {
       q_b = b, q_g = g, q_cg = it.cg;
-      const int qv = vbase + (gid % NV) % V;
+      const int qv = vbase + (kPaired ? (gid >> 1) % V : gid % V);
       const size_t qrow = query_row(a, b, g, G, qv) * D;
       if constexpr (KS == kSideFP8) {
         // unrotated bf16 query, scaled by a power of two into the f16 range (exact)
@@ -404,16 +423,18 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 1)
         frexpf(mx, &ex);
         const int e2 = ex > 14 ? 14 - ex : 0;
         const float qs = ldexpf(1.0f, e2);
+        // bf16 values fit f16 exactly after the scaling: the lo parts are zero
+        const bool lo_col = kPaired && (gid & 1);
 #pragma unroll
         for (int ks = 0; ks < C::kKS; ++ks) {
-          qf[ks][0] = pack_f16(x[ks][0] * qs, x[ks][1] * qs);
-          qf[ks][1] = pack_f16(x[ks][2] * qs, x[ks][3] * qs);
+          qf[ks][0] = lo_col ? 0u : pack_f16(x[ks][0] * qs, x[ks][1] * qs);
+          qf[ks][1] = lo_col ? 0u : pack_f16(x[ks][2] * qs, x[ks][3] * qs);
+          if constexpr (!kPaired) ql[ks][0] = ql[ks][1] = 0u;
         }
         score_scale = a.scale * __ldg(a.k_scales) * ldexpf(1.0f, -e2) * kLog2e;
       } else {
         // rotated fp32 query: coordinates (D/4) tig + 4 ks + {0, 1} (b0) and + {2, 3} (b1),
-        // scaled by 2^e2 (max below 2^15) and split into f16 hi + lo; for NV <= 4 the columns
-        // n >= 4 carry the lo half (same heads as n - 4)
+        // scaled by 2^e2 (max below 2^15) and split into f16 hi + lo
         const float4* qp = reinterpret_cast<const float4*>(a.q_rot + qrow + (D / 4) * tig);
         float4 x[C::kKS];
         float mx = 0.0f;
@@ -428,19 +449,19 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 1)
         frexpf(mx, &ex);
         const int e2 = 15 - ex;
         const float qs = ldexpf(1.0f, e2);
-        const bool lo_col = NV <= 4 && gid >= 4;
+        const bool lo_col = kPaired && (gid & 1);
 #pragma unroll
         for (int ks = 0; ks < C::kKS; ++ks) {
           const float y0 = x[ks].x * qs, y1 = x[ks].y * qs, y2 = x[ks].z * qs, y3 = x[ks].w * qs;
           const float h0 = hi_f16(y0), h1 = hi_f16(y1), h2 = hi_f16(y2), h3 = hi_f16(y3);
-          if constexpr (NV == 8) {
+          if constexpr (kPaired) {
+            qf[ks][0] = lo_col ? pack_f16(y0 - h0, y1 - h1) : pack_f16(h0, h1);
+            qf[ks][1] = lo_col ? pack_f16(y2 - h2, y3 - h3) : pack_f16(h2, h3);
+          } else {
             qf[ks][0] = pack_f16(h0, h1);
             qf[ks][1] = pack_f16(h2, h3);
             ql[ks][0] = pack_f16(y0 - h0, y1 - h1);
             ql[ks][1] = pack_f16(y2 - h2, y3 - h3);
-          } else {
-            qf[ks][0] = lo_col ? pack_f16(y0 - h0, y1 - h1) : pack_f16(h0, h1);
-            qf[ks][1] = lo_col ? pack_f16(y2 - h2, y3 - h3) : pack_f16(h2, h3);
           }
         }
         score_scale = a.scale * ldexpf(1.0f, -e2) * kLog2e;
@@ -463,10 +484,12 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 1)
     const int tkstep = (ip.rev ? -a.ksub : a.ksub) * kPage;
     const int n_pages = ip.n;
 
-    // ---- running state: column c = 2*tig + j of S^T and of every O^T column tile. O^T is kept
-    //      in units of 2^(ev_run - 127): ev_run is the largest biased binary32 exponent of the
-    //      value norms seen so far, so P * ||v|| * 2^(127 - ev_run) < 2^(kLazyLog2 + 1) fits f16
-    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.0f, 0.0f};
+    // ---- running state. Paired: one (m, l) per thread (its pair); else one per column j.
+    //      O^T is kept in units of 2^(ev_run - 127): ev_run is the largest biased binary32
+    //      exponent of the value norms seen so far, so P * ||v|| * 2^(127 - ev_run) <
+    //      2^(kLazyLog2 + 1) fits f16.
+    float m_run[2] = {kNoMax, kNoMax}, l_run[2] = {0.0f, 0.0f};
+    if constexpr (!kPaired) m_run[0] = m_run[1] = -INFINITY;
     float o[C::kNT][C::kMT][4];
 #pragma unroll
     for (int t = 0; t < C::kNT; ++t)
@@ -562,43 +585,67 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 1)
                                     e4m3x2_to_f16x2(rr[3] >> 16)};
             ptx::mma_f16(sc2, a1, qf[2 * j2 + 1][0], qf[2 * j2 + 1][1]);
           }
-#pragma unroll
-          for (int e = 0; e < 4; ++e) sc[e] += sc2[e];
         } else {
-          KeySteps<0, C::kKS, KS, NV>::run(sc, sc2, k0, k1, lutk, qf, ql);
+          KeySteps<0, C::kKS, KS, kPaired ? 1 : 8>::run(sc, sc2, k0, k1, lutk, qf, ql);
+        }
+        const float ss0 = score_scale * kn0, ss1 = score_scale * kn1;
+        float alpha[2], pv[4];
+        bool rescale;
+        if constexpr (kPaired) {
+          // -- the pair's scores of tokens gid and gid + 8: hi + lo columns, scale (and key
+          //    norm), softcap, ALiBi, mask
+          float sp[2] = {((sc[0] + sc2[0]) + (sc[1] + sc2[1])) * ss0, ((sc[2] + sc2[2]) + (sc[3] + sc2[3])) * ss1};
+          if constexpr (CAP) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) sp[e] = cap_post * tanhf(sp[e] * cap_pre);
+          }
+          if (alibi || tok0 < lo_all || tok0 + kPage > hi_all) {
+            // the column's limits and position again, from the item's ring entry (rare pages)
+            const Item it2 = ring_item(ring, popped - 1);
+            const Cols c = item_cols<NV>(a, it2, partition_range(it2.L, a.T, it2.p, a.window, a.psize, a.thresh),
+                                         tig, G);
+            if (alibi) {  // + slope * (t - pos) for token t
+              const float slope = __ldg(a.alibi + it2.g * G + c.vh[0] % G) * kLog2e;
+#pragma unroll
+              for (int e = 0; e < 2; ++e) sp[e] += slope * (float)(tok0 + gid + 8 * e - c.pos[0]);
+            }
+            if (tok0 < lo_all || tok0 + kPage > hi_all) mask_page_col(sp, tok0, gid, c.lo[0], c.hi[0]);
+          }
+          // -- online softmax of the pair (lazily moved reference max)
+          float pr[2];
+          rescale = page_softmax_col(sp, m_run[0], l_run[0], alpha[0], pr);
+          alpha[1] = alpha[0];
+          pv[0] = pr[0] * vn0;
+          pv[1] = pr[1] * vn1;
+        } else {
+          // -- two columns per thread: hi + lo fragments were added by the MMAs
 #pragma unroll
           for (int e = 0; e < 4; ++e) sc[e] += sc2[e];
-          if constexpr (NV <= 4) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) sc[e] += __shfl_xor_sync(kFull, sc[e], 2);  // hi + lo columns
+          for (int e = 0; e < 4; ++e) {
+            const float y = sc[e] * ((e >> 1) ? ss1 : ss0);
+            sc[e] = CAP ? cap_post * tanhf(y * cap_pre) : y;
           }
-        }
-        // -- scale (and key norms), softcap, mask; sc[0], sc[1]: token gid; sc[2], sc[3]: gid + 8
-        const float ss0 = score_scale * kn0, ss1 = score_scale * kn1;
+          if (alibi || tok0 < lo_all || tok0 + kPage > hi_all) {
+            const Item it2 = ring_item(ring, popped - 1);
+            const Cols c = item_cols<NV>(a, it2, partition_range(it2.L, a.T, it2.p, a.window, a.psize, a.thresh),
+                                         tig, G);
+            if (alibi) {  // + slope * (t - pos) for token t of each element
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float y = sc[e] * ((e >> 1) ? ss1 : ss0);
-          sc[e] = CAP ? cap_post * tanhf(y * cap_pre) : y;
-        }
-        if (alibi || tok0 < lo_all || tok0 + kPage > hi_all) {
-          // the columns' limits and positions again, from the item's ring entry (rare pages)
-          const Item it2 = ring_item(ring, popped - 1);
-          const Cols c = item_cols<NV>(a, it2, partition_range(it2.L, a.T, it2.p, a.window, a.psize, a.thresh), tig,
-                                       G);
-          if (alibi) {  // + slope * (t - pos) for token t of each element
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              sc[e] += __ldg(a.alibi + it2.g * G + c.vh[e & 1] % G) * kLog2e *
-                       (float)(tok0 + gid + (e >> 1) * 8 - c.pos[e & 1]);
+              for (int e = 0; e < 4; ++e)
+                sc[e] += __ldg(a.alibi + it2.g * G + c.vh[e & 1] % G) * kLog2e *
+                         (float)(tok0 + gid + (e >> 1) * 8 - c.pos[e & 1]);
+            }
+            if (tok0 < lo_all || tok0 + kPage > hi_all) mask_page(sc, tok0, gid, c.lo, c.hi);
           }
-          if (tok0 < lo_all || tok0 + kPage > hi_all) mask_page(sc, tok0, gid, c.lo, c.hi);
+          float pr[4];
+          rescale = page_softmax(sc, m_run, l_run, alpha, pr);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) pv[e] = pr[e] * ((e >> 1) ? vn1 : vn0);
         }
-        // -- online softmax per column (lazily moved reference max); a larger value-norm
-        //    exponent on this page rescales O^T by the same exact power of two
-        float alpha[2], pr[4];
-        bool rescale = page_softmax(sc, m_run, l_run, alpha, pr);
+        // -- a larger value-norm exponent on this page rescales O^T by the same exact power of two
         int ev = (int)(__float_as_uint(fmaxf(fabsf(vn0), fabsf(vn1))) >> 23);
-        if (__any_sync(kFull, ev > ev_run)) {  // a larger exponent on this page: the warp's max
+        if (__any_sync(kFull, ev > ev_run)) {  // the warp's max
           ev = max(ev, __shfl_xor_sync(kFull, ev, 4));
           ev = max(ev, __shfl_xor_sync(kFull, ev, 8));
           ev = max(ev, __shfl_xor_sync(kFull, ev, 16));
@@ -620,24 +667,21 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 1)
               o[t][mt][3] *= alpha[1];
             }
         }
-        // -- (P * value norms)^T as the B operand: hi/lo parts in C layout, transposed with movmatrix
-        const float vu0 = vn0 * v_unit, vu1 = vn1 * v_unit;
-        float pv[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) pv[e] = pr[e] * ((e >> 1) ? vu1 : vu0);
+        // -- (P * value norms)^T as the B operand, split hi + lo, transposed with movmatrix
         uint32_t pb[C::kNT][2];
-        if constexpr (NV <= 4) {
-          float x[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) x[e] = fmaf(pv[e], p_lo[e & 1], hi_f16(pv[e]) * p_hl[e & 1]);
-          pb[0][0] = ptx::movmatrix_trans(pack_f16(x[0], x[1]));
-          pb[0][1] = ptx::movmatrix_trans(pack_f16(x[2], x[3]));
+        if constexpr (kPaired) {
+          // C layout (token gid: columns 2 tig, 2 tig + 1) = (hi, lo) of the pair's value
+          const float x0 = pv[0] * v_unit, x1 = pv[1] * v_unit;
+          const float h0 = hi_f16(x0), h1 = hi_f16(x1);
+          pb[0][0] = ptx::movmatrix_trans(pack_f16(h0, x0 - h0));
+          pb[0][1] = ptx::movmatrix_trans(pack_f16(h1, x1 - h1));
         } else {
           float hi[4], lo[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            hi[e] = hi_f16(pv[e]);
-            lo[e] = pv[e] - hi[e];
+            const float x = pv[e] * v_unit;
+            hi[e] = hi_f16(x);
+            lo[e] = x - hi[e];
           }
           pb[0][0] = ptx::movmatrix_trans(pack_f16(hi[0], hi[1]));
           pb[0][1] = ptx::movmatrix_trans(pack_f16(hi[2], hi[3]));
@@ -664,10 +708,10 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 1)
     }
     if (stalled) break;
 
-    // ---- item epilogue: the partial (O^T with hi and lo columns added, back to absolute
-    //      units; running max and sum) straight from registers. Thread (gid, tig) holds, for
-    //      columns 2 tig + j, the D/8 consecutive coordinates (D/8) gid .. (D/8) gid + D/8 - 1:
-    //      O^T rows gid and gid + 8 of m-tile mt are coordinates 2 ((D/16) gid + mt) + {0, 1}.
+    // ---- item epilogue: the partial (output back to absolute units, running max and sum)
+    //      straight from registers. Thread (gid, tig) holds, per column, the D/8 consecutive
+    //      coordinates (D/8) gid .. (D/8) gid + D/8 - 1: O^T rows gid and gid + 8 of m-tile mt
+    //      are coordinates 2 ((D/16) gid + mt) + {0, 1}.
     const float o_unit = ldexpf(1.0f, ev_run - 127);
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
@@ -675,29 +719,25 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 1)
       l_run[j] += __shfl_xor_sync(kFull, l_run[j], 8);
       l_run[j] += __shfl_xor_sync(kFull, l_run[j], 16);
     }
-    float ov[C::kMT][4];
-#pragma unroll
-    for (int mt = 0; mt < C::kMT; ++mt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        float v = o[0][mt][e];
-        if constexpr (NV == 8) v += o[C::kNT - 1][mt][e];
-        if constexpr (NV == 4) v += __shfl_xor_sync(kFull, v, 2);  // columns c, c + 4
-        if constexpr (NV == 2) v += __shfl_xor_sync(kFull, v, 1);  // columns c, c + 2
-        if constexpr (NV == 1) v += (e & 1) ? 0.0f : o[0][mt][e + 1];  // columns 0, 1
-        ov[mt][e] = v * o_unit;
-      }
     const Item it3 = ring_item(ring, popped - 1);
     const int slot = it3.p * a.ksub + it3.sub, vbase3 = 8 * it3.cg, V3 = min(NV, a.T * G - vbase3);
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      const int col = 2 * tig + j;
+    for (int j = 0; j < (kPaired ? 1 : 2); ++j) {
+      // paired: the thread's pair is tig (hi + lo columns added); else column 2 tig + j
+      const int col = kPaired ? tig : 2 * tig + j;
       if (col < V3) {
+        float ov[C::kMT][2];
+#pragma unroll
+        for (int mt = 0; mt < C::kMT; ++mt)
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+            ov[mt][h] = (kPaired ? o[0][mt][2 * h] + o[0][mt][2 * h + 1] : o[0][mt][2 * h + j] + o[1][mt][2 * h + j]) *
+                        o_unit;
         const size_t row = query_row(a, it3.b, it3.g, G, vbase3 + col);
         float4* dst = reinterpret_cast<float4*>(a.part_o + (row * PK + slot) * D + (D / 8) * gid);
 #pragma unroll
         for (int q4 = 0; q4 < C::kMT / 2; ++q4)
-          dst[q4] = make_float4(ov[2 * q4][j], ov[2 * q4][j + 2], ov[2 * q4 + 1][j], ov[2 * q4 + 1][j + 2]);
+          dst[q4] = make_float4(ov[2 * q4][0], ov[2 * q4][1], ov[2 * q4 + 1][0], ov[2 * q4 + 1][1]);
         if (gid == 0) {
           a.part_m[row * PK + slot] = m_run[j];
           a.part_l[row * PK + slot] = l_run[j];
@@ -792,12 +832,18 @@ cudaError_t launch_fixed(const Args& a, cudaStream_t s) {
   static DeviceFlags attr;
   cudaError_t e = ensure_dynamic_smem(kern, C::kSmem, attr);
   if (e != cudaSuccess) return e;
-  static int sms[64] = {};
+  static int sms[64] = {}, reserved[64] = {};
   int dev = 0;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (sms[dev] == 0 && (e = cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
-    return e;
+  if (sms[dev] == 0) {
+    if ((e = cudaDeviceGetAttribute(&reserved[dev], cudaDevAttrReservedSharedMemoryPerBlock, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return e;
+  }
+  // the shared-memory layout (tables on a 64 KB boundary, warps' blocks around them) is laid out
+  // for dynamic shared memory starting kDynStart bytes into the CTA's window
+  if (reserved[dev] != kDynStart) return cudaErrorNotSupported;
   // one CTA per SM, fewer when the call has fewer items than the grid has warps
   const long long items = (long long)a.B * a.Hkv * a.P * a.ncg * a.ksub;
   const long long ctas = (items + C::kWarps - 1) / C::kWarps;

@@ -90,6 +90,8 @@ enum da_status {
 #define DA_DEVERR_BLOCK_ID 0x1u    /* a block-table entry used by the call was outside [0, num_blocks) */
 #define DA_DEVERR_CONTEXT_LEN 0x2u /* a context length was < 0 or above the limits in the header comment */
 #define DA_DEVERR_TIMEOUT 0x4u     /* a wait for a page copy gave up after 200 ms (never expected) */
+#define DA_DEVERR_SMEM_LAYOUT 0x8u /* a partition kernel's shared-memory layout did not fit the CTA's
+                                      window, so it computed nothing (never expected) */
 
 typedef struct da_params {
   int32_t batch;              /* B >= 0 sequences (B == 0: nothing to do) */

@@ -151,6 +151,13 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
   return v;
 }
 __device__ __forceinline__ float ldsf(uint32_t addr) { return __uint_as_float(lds32(addr)); }
+// A load from the lookup tables, which no thread writes after the CTA's first barrier: not
+// volatile, so the compiler may interleave the lookups with the work around them.
+__device__ __forceinline__ uint32_t lds32_table(uint32_t addr) {
+  uint32_t v;
+  asm("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
 
 // A lookup table as seen by one lane: the table's base (a multiple of 64 KB) joined with the
 // lane's copy offset 4 * lane.
@@ -161,7 +168,7 @@ struct Lut {
 // (table base) from lanebase and puts the byte at bits 8..15.
 template <int J>
 __device__ __forceinline__ uint32_t lut_byte(const Lut& t, uint32_t w) {
-  return lds32(__byte_perm(w, t.lanebase, 0x7604 | (J << 4)));
+  return lds32_table(__byte_perm(w, t.lanebase, 0x7604 | (J << 4)));
 }
 // byte J of a little-endian word array
 template <int J>
@@ -180,7 +187,7 @@ __device__ __forceinline__ uint32_t lut_field6(const Lut& t, const uint32_t* w) 
     x = w[wi] >> (sh - 8);
   else
     x = __funnelshift_r(w[wi], w[wi + 1], sh - 8);  // the field crosses into the next word
-  return lds32((x & 0x3f00u) | t.lanebase);
+  return lds32_table((x & 0x3f00u) | t.lanebase);
 }
 
 // A fragments of S^T for k-step S from the thread's key bytes (rows gid: k0, gid + 8: k1).
@@ -302,7 +309,6 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 1)
   const int stride = gridDim.x * kWarps;  // warps in the grid
   ItemIssue cur;
   cur.init(a, blockIdx.x * kWarps + w, ring, stride, lane);
-  uint32_t valid_mask = 0;  // bit s: the page in stage s has a valid block (warp-uniform)
   unsigned issued = 0;
   int is = 0;  // stage of the next copy (issued % kStages)
   auto issue_next = [&]() {  // all lanes; lane 0 issues the copies of the page at the cursor
@@ -311,15 +317,14 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 1)
     const int s = is;
     is = is + 1 == C::kStages ? 0 : is + 1;
     ++issued;
-    valid_mask = phys >= 0 ? (valid_mask | (1u << s)) : (valid_mask & ~(1u << s));
     if (lane == 0) {
       const uint32_t bar = bar0 + 8 * s, dst = code0 + s * C::kCodeBytes, ndst = norm0 + s * C::kNormBytes;
-      if (phys < 0) {
-        ptx::mbar_arrive(bar);  // completes the phase with nothing loaded
-      } else {
+      {
         ptx::fence_proxy_async();
         ptx::mbar_arrive_expect_tx(bar, C::kTxBytes);
-        const size_t unit = (size_t)phys * a.Hkv + gk;  // (block, kv head): 16 consecutive rows
+        // a bad block id (flagged by the walk) reads block 0 in its place: the affected outputs
+        // are unspecified, as the interface states
+        const size_t unit = (size_t)(phys < 0 ? 0 : phys) * a.Hkv + gk;  // (block, kv head): 16 rows
         const int y = (int)unit * kPage;
         if constexpr (KS == kSideCB4) {  // codes of K and V: one copy when one map spans both
           if (a.kv_pair) {
@@ -511,7 +516,6 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 1)
         cs = 0;
         cphase ^= 1u;
       }
-      const bool valid = valid_mask & (1u << s);
       const uint32_t cb0 = code0 + s * C::kCodeBytes, kb = cb0 + koff, vb = cb0 + voff;
       const uint32_t nb = norm0 + s * C::kNormBytes;
       const int tok0 = tk0 + i * tkstep;
@@ -568,7 +572,7 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 1)
         if (cur.more) issue_next();
       }
 
-      if (valid) {
+      {
         // -- S^T = K . Q^T, the k-steps alternating between two accumulators (two dependent MMA
         //    chains of half the length), added at the end
         float sc[4] = {0.0f, 0.0f, 0.0f, 0.0f}, sc2[4] = {0.0f, 0.0f, 0.0f, 0.0f};

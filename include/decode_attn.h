@@ -35,8 +35,9 @@
  *     DA_ERR_UNSUPPORTED or DA_ERR_WORKSPACE has enqueued nothing.
  *   - Bad DATA found by a kernel (a block id outside [0, num_blocks), a context length
  *     outside [0, min(max_context_len, max_blocks_per_seq * block_size)]) does not fault:
- *     the kernel skips the bad page or clamps the length, sets a bit in the workspace's
- *     error word, and carries on. The affected outputs are then unspecified.
+ *     the kernel skips the bad page (or reads block 0 in its place) or clamps the length,
+ *     sets a bit in the workspace's error word, and carries on. The affected outputs are
+ *     then unspecified.
  *     decode_attn_get_device_error reports the bits.
  */
 #ifndef DECODE_ATTN_H_

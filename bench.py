@@ -228,7 +228,7 @@ def build_inputs(spec, encode_on_gpu=True, writer_times=None):
 # reported while the kernel's sources still hash to the profiled build)
 PARTITION_SOURCES = {
     "partition_tc_kernel": ("partition_tc.cu", "page_softmax.cuh", "page_walk.cuh", "ptx.cuh", "da_internal.cuh"),
-    "partition_cb_kernel": ("partition_cb.cu", "item_walk.cuh", "page_softmax.cuh", "page_walk.cuh", "ptx.cuh",
+    "partition_cb_kernel": ("partition_cb.cuh", "item_walk.cuh", "page_softmax.cuh", "page_walk.cuh", "ptx.cuh",
                             "da_internal.cuh", "kv_formats.cuh"),
 }
 

@@ -108,16 +108,23 @@ struct Cb {
   // first 64 KB boundary of the window, the 3-bit key table right behind it
   static constexpr int kLutV = 256 * 256;
   static constexpr int kLutK = KS == kSideCB3 ? 64 * 256 : 0;
-  // Each warp's block: its code stages, norm slots, walk state (ring) and mbarriers. The blocks
-  // fill the space before the tables (region A) and after them (region B).
+  // Pages per stage (one mbarrier, one wait, one copy issue): two consecutive pages of the warp's
+  // stream for codebook keys, which are read into registers before the stage is refilled; one
+  // for FP8 keys, which the MMAs read from the stage.
+  static constexpr int kSlots = KS != kSideFP8 ? 2 : 1;
+  // Each warp's block: its pages' code and norm slots, walk state (ring) and mbarriers. The
+  // blocks fill the space before the tables (region A) and after them (region B).
   static constexpr int block_bytes(int s) {
-    return align_up(s * (kCodeBytes + kNormBytes) + ItemIssue::kStateBytes + 8 * s, kAlign);
+    return align_up(s * (kCodeBytes + kNormBytes) + ItemIssue::kStateBytes + 8 * (s / kSlots), kAlign);
   }
   static constexpr int kRegionA = kLutAlign - align_up(kDynStart, kAlign);
   static constexpr int kRegionB = kDynStart + kSmemLimit - kLutAlign - kLutV - kLutK;
-  static constexpr bool fits(int s) { return kRegionA / block_bytes(s) + kRegionB / block_bytes(s) >= kWarps; }
-  static constexpr int kStages = fits(6) ? 6 : fits(5) ? 5 : fits(4) ? 4 : fits(3) ? 3 : 2;
-  static_assert(fits(kStages), "shared memory holds fewer than two stages per warp");
+  static constexpr bool fits(int s) {
+    return s % kSlots == 0 && kRegionA / block_bytes(s) + kRegionB / block_bytes(s) >= kWarps;
+  }
+  static constexpr int kStages = fits(6) ? 6 : fits(5) ? 5 : fits(4) ? 4 : fits(3) ? 3 : 2;  // pages per warp
+  static_assert(fits(kStages), "shared memory holds fewer than two pages per warp");
+  static constexpr int kNStages = kStages / kSlots;  // stages (mbarriers) per warp
   static constexpr int kBlock = block_bytes(kStages);
   static constexpr int kOffNorms = kStages * kCodeBytes;  // within a block
   static constexpr int kOffRing = kOffNorms + kStages * kNormBytes;
@@ -297,7 +304,7 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 1)
     ptx::prefetch_tensor_map(&kmap);
     if (!(PAIR || a.kv_pair)) ptx::prefetch_tensor_map(&vmap);
     if (PAIR || a.kn_pair) ptx::prefetch_tensor_map(&nmap);
-    for (int s = 0; s < C::kStages; ++s) ptx::mbar_init(bar0 + 8 * s, 1);
+    for (int s = 0; s < C::kNStages; ++s) ptx::mbar_init(bar0 + 8 * s, 1);
     ptx::fence_mbar_init();
   }
   __syncwarp();
@@ -313,22 +320,32 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 1)
   const int stride = gridDim.x * kWarps;  // warps in the grid
   ItemIssue cur;
   cur.init(a, blockIdx.x * kWarps + w, ring, stride, lane);
-  unsigned issued = 0;
-  int is = 0;  // stage of the next copy (issued % kStages)
-  auto issue_next = [&]() {  // all lanes; lane 0 issues the copies of the page at the cursor
-    const int gk = cur.g;
-    const int phys = cur.take(a, ring, stride, lane);
+  unsigned issued = 0;  // stages issued
+  int is = 0;           // stage of the next copies (issued % kNStages)
+  auto issue_next = [&]() {  // all lanes; lane 0 issues the copies of the next kSlots pages
+    int gk[C::kSlots], phys[C::kSlots], n = 0;
+#pragma unroll
+    for (int j = 0; j < C::kSlots; ++j)
+      if (j == 0 || cur.more) {
+        gk[j] = cur.g;
+        phys[j] = cur.take(a, ring, stride, lane);
+        n = j + 1;
+      }
     const int s = is;
-    is = is + 1 == C::kStages ? 0 : is + 1;
+    is = is + 1 == C::kNStages ? 0 : is + 1;
     ++issued;
     if (lane == 0) {
-      const uint32_t bar = bar0 + 8 * s, dst = code0 + s * C::kCodeBytes, ndst = norm0 + s * C::kNormBytes;
-      {
-        ptx::fence_proxy_async();
-        ptx::mbar_arrive_expect_tx(bar, C::kTxBytes);
+      const uint32_t bar = bar0 + 8 * s;
+      ptx::fence_proxy_async();
+      ptx::mbar_arrive_expect_tx(bar, n * C::kTxBytes);
+#pragma unroll
+      for (int j = 0; j < C::kSlots; ++j) {
+        if (j >= n) break;
+        const uint32_t dst = code0 + (s * C::kSlots + j) * C::kCodeBytes;
+        const uint32_t ndst = norm0 + (s * C::kSlots + j) * C::kNormBytes;
         // a bad block id (flagged by the walk) reads block 0 in its place: the affected outputs
         // are unspecified, as the interface states
-        const size_t unit = (size_t)(phys < 0 ? 0 : phys) * a.Hkv + gk;  // (block, kv head): 16 rows
+        const size_t unit = (size_t)(phys[j] < 0 ? 0 : phys[j]) * a.Hkv + gk[j];  // (block, kv head): 16 rows
         const int y = (int)unit * kPage;
         if constexpr (KS == kSideCB4) {  // codes of K and V: one copy when one map spans both
           if (PAIR || a.kv_pair) {
@@ -359,7 +376,7 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 1)
       }
     }
   };
-  for (int k = 0; k < C::kStages && cur.more; ++k) issue_next();
+  for (int k = 0; k < C::kNStages && cur.more; ++k) issue_next();
 
   // ---- lookup tables: byte -> (cb[lo], cb[hi]) for values (and 4-bit keys), 6-bit pair ->
   //      (cbk[lo], cbk[hi]) for 3-bit keys; entry e at word 64 e, 32 copies (word 64 e + l)
@@ -390,9 +407,7 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 1)
   const bool alibi = a.alibi != nullptr;
   const int PK = a.P * a.ksub;  // partial slots per output row
   const int mi = lane >> 3, ri = lane & 7;  // ldmatrix (FP8 keys): matrix index and row of this lane's address
-  unsigned consumed = 0, stall_from = 0, popped = 0;
-  int cs = 0;            // stage of the next page to compute (consumed % kStages)
-  uint32_t cphase = 0;   // its mbarrier phase parity ((consumed / kStages) & 1)
+  unsigned consumed = 0, stall_from = 0, popped = 0;  // pages computed; stage of a stall
   bool stalled = false;  // a copy never arrived: no more waits, copies or compute
   int q_b = -1, q_g = -1, q_cg = -1;  // (sequence, kv head, column group) of the loaded query fragments
   uint32_t qf[C::kKS][2], ql[kPaired ? 1 : C::kKS][2];
@@ -510,18 +525,16 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 1)
     float v_unit = 1.0f;  // 2^(127 - ev_run)
 
     for (int i = 0; i < n_pages; ++i, ++consumed) {
-      const int s = cs;
-      if (!ptx::mbar_wait(bar0 + 8 * s, cphase)) {
+      // page `consumed` of the warp's stream: slot `slot` of stage use `use`
+      const unsigned use = consumed / C::kSlots, slot = consumed % C::kSlots;
+      const int s = use % C::kNStages;
+      if (slot == 0 && !ptx::mbar_wait(bar0 + 8 * s, (use / C::kNStages) & 1)) {
         stalled = true;
-        stall_from = consumed;
+        stall_from = use;
         break;
       }
-      if (++cs == C::kStages) {
-        cs = 0;
-        cphase ^= 1u;
-      }
-      const uint32_t cb0 = code0 + s * C::kCodeBytes, kb = cb0 + koff, vb = cb0 + voff;
-      const uint32_t nb = norm0 + s * C::kNormBytes;
+      const uint32_t cb0 = code0 + (s * C::kSlots + slot) * C::kCodeBytes, kb = cb0 + koff, vb = cb0 + voff;
+      const uint32_t nb = norm0 + (s * C::kSlots + slot) * C::kNormBytes;
       const int tok0 = tk0 + i * tkstep;
 
       // -- the page into registers: key bytes (codebook keys), value bytes, norms
@@ -572,8 +585,10 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 1)
       const float vn0 = ldsf(nb + vnoff + 4 * gid), vn1 = ldsf(nb + vnoff + 4 * (gid + 8));
       // FP8 keys are read with ldmatrix during the MMAs below, so their stage is refilled after
       if constexpr (KS != kSideFP8) {
-        __syncwarp();  // every lane has read the stage
-        if (cur.more) issue_next();
+        if (slot == C::kSlots - 1) {  // the stage's last page is in registers
+          __syncwarp();                // every lane has read the stage
+          if (cur.more) issue_next();
+        }
       }
 
       {
@@ -760,7 +775,7 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 1)
     // time limit shared by all of them)
     uint64_t deadline = 0;
     for (unsigned k = stall_from; k < issued; ++k)
-      ptx::mbar_wait_until(bar0 + 8 * (k % C::kStages), (k / C::kStages) & 1, deadline);
+      ptx::mbar_wait_until(bar0 + 8 * (k % C::kNStages), (k / C::kNStages) & 1, deadline);
   }
 }
 

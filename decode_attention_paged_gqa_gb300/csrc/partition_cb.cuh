@@ -109,9 +109,9 @@ struct Cb {
   static constexpr int kLutV = 256 * 256;
   static constexpr int kLutK = KS == kSideCB3 ? 64 * 256 : 0;
   // Pages per stage (one mbarrier, one wait, one copy issue): two consecutive pages of the warp's
-  // stream for codebook keys, which are read into registers before the stage is refilled; one
-  // for FP8 keys, which the MMAs read from the stage.
-  static constexpr int kSlots = KS != kSideFP8 ? 2 : 1;
+  // stream for 4-bit keys (measured faster), one for the other key sides (3-bit keys: measured
+  // faster with one; FP8 keys, which the MMAs read from the stage, refill it after the MMAs).
+  static constexpr int kSlots = KS == kSideCB4 ? 2 : 1;
   // Each warp's block: its pages' code and norm slots, walk state (ring) and mbarriers. The
   // blocks fill the space before the tables (region A) and after them (region B).
   static constexpr int block_bytes(int s) {

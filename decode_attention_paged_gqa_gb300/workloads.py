@@ -70,6 +70,10 @@ WORKLOADS = {
     # the same batch with FP8 keys + 4-bit values, and with 3-bit keys + 4-bit values
     "fp8k_cb4v_long_32k": WorkloadSpec("fp8k_cb4v_long_32k", 32, 32, 8, 128, "fp8k_cb4v", 32768, 32768, seed=1006),
     "cb3k_cb4v_long_32k": WorkloadSpec("cb3k_cb4v_long_32k", 32, 32, 8, 128, "cb3k_cb4v", 32768, 32768, seed=1007),
+    # smaller batches of spread lengths (how well the work is spread over the SMs): 16 Llama-shaped
+    # BF16 sequences of U[512, 8192] tokens, and 32 4-bit sequences of U[1, 32768] tokens
+    "llama3_8b_bf16_b16": WorkloadSpec("llama3_8b_bf16_b16", 16, 32, 8, 128, "bf16", 512, 8192, seed=1008),
+    "cb4_spread_32k": WorkloadSpec("cb4_spread_32k", 32, 32, 8, 128, "cb4", 1, 32768, seed=1009),
 }
 
 

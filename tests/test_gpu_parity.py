@@ -239,6 +239,17 @@ def test_full_size_workloads_whole_output(name):
     print(f"{name}: whole output, max_abs={max_abs:.3e} rel_l2={rel:.3e}")
 
 
+@pytest.mark.parametrize("fmt", ["bf16", "fp8", "cb4", "fp8k_cb4v", "cb3k_cb4v"])
+def test_spread_context_lengths(fmt):
+    """A batch whose context lengths spread from 1 to 32768 tokens (unsplit and split sequences,
+    1 to 64 partitions each) in the automatic launch configuration: the codebook-value kernel
+    deals this uneven work to its warps from one flattened list of items."""
+    lens = [1, 32768, 17, 300, 20000, 1023, 1024, 7000, 2500, 12345, 512, 4097, 31999, 64]
+    spec = wl.WorkloadSpec(f"spread_{fmt}", len(lens), 32, 8, 128, fmt, 0, max(lens), seed=404)
+    c = make_case(spec, wl.make_layout(spec, lens=lens))
+    assert_close(run_gpu(c), run_oracle(c), f"{fmt} spread lengths")
+
+
 @pytest.mark.parametrize("fmt", ["bf16", "fp8"])
 @pytest.mark.parametrize("qscale", [1e-3, 3e2, 1e5])
 def test_query_magnitudes(fmt, qscale):

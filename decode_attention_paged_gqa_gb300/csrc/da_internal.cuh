@@ -54,6 +54,8 @@ struct Args {
                               // warps of a CTA share each partition (set by its launcher)
   // workspace pieces
   uint32_t* err;              // device error word (DA_DEVERR_* bits)
+  uint32_t* claim;            // [2] next to it: the codebook-value kernel's item counter and count of
+                              // warps done (zero between calls; zeroed with the workspace)
   float* q_rot;               // [B][T][Hq][D] (formats whose keys are on the rotated basis)
   float* part_o;              // [B][T][Hq][P * ksub][D], unnormalised partial outputs
   float* part_m;              // [B][T][Hq][P * ksub], running max in log2 units
@@ -177,8 +179,8 @@ inline Layout workspace_layout(const da_params& p) {
   const size_t BH = (size_t)p.batch * query_len(p) * p.num_q_heads;
   const size_t P = (size_t)host_max_partitions(p) * sub_items(p);
   size_t off = 0;
-  l.err = off;
-  off = align256(off + sizeof(uint32_t));
+  l.err = off;  // the error word, then the item counter and the count of warps done
+  off = align256(off + 3 * sizeof(uint32_t));
   l.q_rot = off;
   const bool rotated_keys = p.kv_format == DA_KV_CB4 || p.kv_format == DA_KV_CB3K_CB4V;
   off = align256(off + (rotated_keys ? BH * p.head_dim * sizeof(float) : 0));

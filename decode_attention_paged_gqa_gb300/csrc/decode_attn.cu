@@ -112,6 +112,7 @@ Args make_args(const void* q, const void* k, const void* v, const float* ks, con
   const Layout l = workspace_layout(*p);
   char* ws = static_cast<char*>(p->workspace);
   a.err = reinterpret_cast<uint32_t*>(ws + l.err);
+  a.claim = a.err + 1;
   a.q_rot = reinterpret_cast<float*>(ws + l.q_rot);
   a.part_o = reinterpret_cast<float*>(ws + l.part_o);
   a.part_m = reinterpret_cast<float*>(ws + l.part_m);

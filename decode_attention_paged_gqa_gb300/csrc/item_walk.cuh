@@ -5,9 +5,11 @@
 // pairs each) and every sub-item s < ksub, one item. With ksub > 1 (batches with few
 // partitions) the pages of a partition are dealt round-robin to its ksub sub-items, each of
 // which writes a partial of its own; the reduce combines them with the partition's others.
-// Warp gw of the grid takes items gw, gw + N, gw + 2N, ... (N = the grid's warps), so the warps
-// get equal shares of the work whatever the spread of the context lengths, and consecutive
-// warps of a CTA take consecutive partitions of one (sequence, kv head).
+// The warps claim items from a counter in the workspace (one atomic add per item, issued one
+// item ahead so its latency is hidden), so a warp that finishes early takes more: the work is
+// spread evenly whatever the spread of the context lengths, and warps that are free at the same
+// time take consecutive partitions of one (sequence, kv head). The last warp of the grid to run
+// out of items puts the counters back to zero for the next call.
 //
 // The copy side of a warp walks its items ahead of the compute side (ItemIssue); when it
 // reaches an item that has pages for the warp it records the item in a small ring in shared
@@ -93,6 +95,7 @@ __device__ __forceinline__ ItemPages item_pages(const Args& a, const Item& it) {
 // (SeqCursor and the next item index) is kept in shared memory next to the ring, since it is
 // only needed once per item. Lane 0 writes the ring and that state.
 struct ItemIssue {
+  int claimed;    // lane 0: the item index claimed for the warp's next item
   int b, g;       // sequence and kv head of the item at the cursor
   int pg0, pstep; // page index of the k-th page of its walk: pg0 + pstep * k
   int n, k;       // the walk's page count, index of the next page
@@ -100,28 +103,28 @@ struct ItemIssue {
   bool more;      // a page is left at the cursor
   unsigned pushed;
 
-  // Shared memory of a warp's walk: kRing descriptors, then SeqCursor and the next item index.
-  static constexpr int kStateBytes = kRing * 16 + 32;
+  // Shared memory of a warp's walk: kRing descriptors, then SeqCursor.
+  static constexpr int kStateBytes = kRing * 16 + 16;
 
   __device__ __forceinline__ void load_bids(const Args& a, int lane) {
     const int kk = (k & ~31) + lane;
     bid = kk < n ? load_block(a, b, pg0 + pstep * kk) : -1;
   }
   // Moves to the warp's next item that has pages for it and records it in the ring.
-  __device__ __forceinline__ void next_item(const Args& a, uint32_t ring, int stride, int lane) {
+  __device__ __forceinline__ void next_item(const Args& a, uint32_t ring, int lane) {
     __syncwarp();  // the state lane 0 wrote last time is visible to the warp
     const uint32_t st = ring + kRing * 16;
     SeqCursor seq;
-    int next;
     asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
                  : "=r"(seq.b), "=r"(seq.base), "=r"(seq.L), "=r"(seq.np)
                  : "r"(st)
                  : "memory");
-    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(next) : "r"(st + 16) : "memory");
     const int per_part = a.ncg * a.ksub;
     seq.count = a.Hkv * seq.np * per_part;
     more = false;
-    for (; seq.seek(a, next, per_part); next += stride) {
+    for (int next = __shfl_sync(0xffffffffu, claimed, 0); seq.seek(a, next, per_part);
+         next = __shfl_sync(0xffffffffu, claimed, 0)) {
+      if (lane == 0) claimed = (int)atomicAdd(a.claim, 1u);  // the item after this one
       Item it;
       int r = next - seq.base;
       const int per_head = seq.np * per_part;
@@ -135,7 +138,6 @@ struct ItemIssue {
       it.sub = r - it.cg * a.ksub;
       const ItemPages ip = item_pages(a, it);
       if (ip.n > 0) {
-        next += stride;
         b = it.b;
         g = it.g;
         n = ip.n;
@@ -159,28 +161,40 @@ struct ItemIssue {
       asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(st), "r"(seq.b), "r"(seq.base), "r"(seq.L),
                    "r"(seq.np)
                    : "memory");
-      asm volatile("st.shared.b32 [%0], %1;" ::"r"(st + 16), "r"(next) : "memory");
     }
   }
-  __device__ __forceinline__ void init(const Args& a, int first_item, uint32_t ring, int stride, int lane) {
-    if (lane == 0) {  // no sequence yet; first item
+  __device__ __forceinline__ void init(const Args& a, uint32_t ring, int lane) {
+    if (lane == 0) {  // no sequence yet; claim the first item
       asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(ring + kRing * 16), "r"(-1), "r"(0), "r"(0),
                    "r"(0)
                    : "memory");
-      asm volatile("st.shared.b32 [%0], %1;" ::"r"(ring + kRing * 16 + 16), "r"(first_item) : "memory");
+      claimed = (int)atomicAdd(a.claim, 1u);
     }
     pushed = 0;
-    next_item(a, ring, stride, lane);
+    next_item(a, ring, lane);
   }
   // Physical block (-1: bad block id, nothing to load) of the page at the cursor, the same in
   // every lane; advances the cursor. Requires `more`.
-  __device__ __forceinline__ int take(const Args& a, uint32_t ring, int stride, int lane) {
+  __device__ __forceinline__ int take(const Args& a, uint32_t ring, int lane) {
     if (k > 0 && (k & 31) == 0) load_bids(a, lane);
     const int phys = __shfl_sync(0xffffffffu, bid, k & 31);
-    if (++k == n) next_item(a, ring, stride, lane);
+    if (++k == n) next_item(a, ring, lane);
     return phys;
   }
 };
+
+// A warp that has no items left counts itself out; the last warp of a grid of `warps` resets the
+// item counter and the count for the next call (every warp claims its last item before it counts
+// itself out, so no claim can follow the reset).
+__device__ __forceinline__ void count_warp_out(const Args& a, unsigned warps, int lane) {
+  if (lane == 0) {
+    __threadfence();
+    if (atomicAdd(a.claim + 1, 1u) == warps - 1) {
+      atomicExch(a.claim, 0u);
+      atomicExch(a.claim + 1, 0u);
+    }
+  }
+}
 
 // The compute side's view of the ring: the descriptor of the warp's next item.
 __device__ __forceinline__ Item ring_item(uint32_t ring, unsigned index) {

@@ -4,10 +4,10 @@
 // memory lookup table.
 //
 // A persistent kernel: one CTA per SM (16 warps at D = 128 with up to four columns, else 8)
-// builds the lookup tables once, then every warp walks its share of the call's flattened item
-// list (item_walk.cuh: one item per (sequence, kv head, partition, column group, sub-item);
-// warp gw takes items gw, gw + N, ...), so the load is balanced whatever the context lengths
-// and no warp ever waits for another. Each warp runs its own pipeline of shared-memory stages
+// builds the lookup tables once, then every warp claims items of the call's flattened item
+// list (item_walk.cuh: one item per (sequence, kv head, partition, column group, sub-item)) one
+// after the other from a counter until none is left, so the load is balanced whatever the
+// context lengths and no warp ever waits for another. Each warp runs its own pipeline of shared-memory stages
 // filled by TMA / bulk copies (a page's K codes, V codes and their per-token norms) and
 // signalled on an mbarrier; it continues across its items, and a stage is refilled as soon as
 // the page in it has been read into registers. Per page a warp computes, in the rotated basis
@@ -296,6 +296,7 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 1)
   const uint32_t blk = w < in_a ? a0 + w * C::kBlock : tbl + C::kLutV + C::kLutK + (w - in_a) * C::kBlock;
   if (blk + C::kBlock > start + C::kSmem || tbl + C::kLutV + C::kLutK > start + C::kSmem) {
     if (tid == 0) atomicOr(a.err, DA_DEVERR_SMEM_LAYOUT);  // the launcher checks this never happens
+    count_warp_out(a, gridDim.x * kWarps, lane);
     return;
   }
   const uint32_t code0 = blk, norm0 = blk + C::kOffNorms, ring = blk + C::kOffRing, bar0 = blk + C::kOffBars;
@@ -317,9 +318,8 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 1)
   const uint32_t vnoff = C::kKNorms ? 64 - knoff : 0;
 
   // ---- the warp's items and their pages, copied kStages pages ahead of the compute
-  const int stride = gridDim.x * kWarps;  // warps in the grid
   ItemIssue cur;
-  cur.init(a, blockIdx.x * kWarps + w, ring, stride, lane);
+  cur.init(a, ring, lane);
   unsigned issued = 0;  // stages issued
   int is = 0;           // stage of the next copies (issued % kNStages)
   auto issue_next = [&]() {  // all lanes; lane 0 issues the copies of the next kSlots pages
@@ -328,7 +328,7 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 1)
     for (int j = 0; j < C::kSlots; ++j)
       if (j == 0 || cur.more) {
         gk[j] = cur.g;
-        phys[j] = cur.take(a, ring, stride, lane);
+        phys[j] = cur.take(a, ring, lane);
         n = j + 1;
       }
     const int s = is;
@@ -777,6 +777,7 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 1)
     for (unsigned k = stall_from; k < issued; ++k)
       ptx::mbar_wait_until(bar0 + 8 * (k % C::kNStages), (k / C::kNStages) & 1, deadline);
   }
+  count_warp_out(a, gridDim.x * kWarps, lane);
 }
 
 // ---------------------------------------------------------------- host side

@@ -87,3 +87,43 @@ def test_three_bit_encoder_bit_exact(D):
     da.decode_attn_encode_codebook(x.cuda(), nvec, D, 3, sg.cuda(), torch.from_numpy(cb8).cuda(), packed, scales)
     assert np.array_equal(scales.cpu().numpy(), scales_ref)
     assert np.array_equal(packed.cpu().numpy(), packed_ref)
+
+
+@pytest.mark.parametrize("D,bits,nvec", [(128, 4, 200_000), (256, 4, 40_000), (128, 3, 100_000), (256, 3, 40_000)])
+def test_codebook_encoder_many_vectors_bit_exact(D, bits, nvec):
+    """Enough vectors that the writer's fast path meets its fallbacks many times over (rotated
+    coordinates within 1e-6 of a decision boundary, norms near a binary32 rounding boundary):
+    every code and norm still equals the plain sequential fp64 evaluation's."""
+    g = torch.Generator().manual_seed(D * 7 + bits)
+    x = torch.randn(nvec, D, generator=g)
+    x[1] = 0.0                      # a zero vector
+    x[2] = 0.0
+    x[2, 5] = 3.0                   # a one-hot vector (every rotated coordinate the same size)
+    x[3:100] *= 1e-20               # tiny and huge norms
+    x[100:200] *= 1e20
+    sg = (torch.randint(0, 2, (D,), generator=g) * 2 - 1).to(torch.float32)
+    cb = oracle.lloyd_max(1 << bits, 1.0 / math.sqrt(D))[1]
+    packed_ref, scales_ref = oracle.cb_encode(bits, x.numpy(), sg.numpy(), cb)
+    packed = torch.empty((nvec, D * bits // 8), dtype=torch.uint8, device="cuda")
+    scales = torch.empty(nvec, dtype=torch.float32, device="cuda")
+    da.decode_attn_encode_codebook(x.cuda(), nvec, D, bits, sg.cuda(), torch.from_numpy(cb).cuda(), packed, scales)
+    assert np.array_equal(scales.cpu().numpy(), scales_ref)
+    got = packed.cpu().numpy()
+    assert np.array_equal(got, packed_ref), f"{int((got != packed_ref).sum())} bytes differ"
+
+
+def test_codebook_encoder_unsorted_codebook():
+    """A codebook that is not strictly increasing takes the plain evaluation for every
+    coordinate: still the oracle's nearest level with ties to the lower index."""
+    D, nvec = 128, 3000
+    g = torch.Generator().manual_seed(5)
+    x = torch.randn(nvec, D, generator=g)
+    sg = (torch.randint(0, 2, (D,), generator=g) * 2 - 1).to(torch.float32)
+    cb = oracle.lloyd_max(16, 1.0 / math.sqrt(D))[1][::-1].copy()  # decreasing
+    cb[3] = cb[4]                                                     # and a repeated level
+    packed_ref, scales_ref = oracle.cb_encode(4, x.numpy(), sg.numpy(), cb)
+    packed = torch.empty((nvec, D // 2), dtype=torch.uint8, device="cuda")
+    scales = torch.empty(nvec, dtype=torch.float32, device="cuda")
+    da.decode_attn_encode_codebook(x.cuda(), nvec, D, 4, sg.cuda(), torch.from_numpy(cb).cuda(), packed, scales)
+    assert np.array_equal(scales.cpu().numpy(), scales_ref)
+    assert np.array_equal(packed.cpu().numpy(), packed_ref)

@@ -389,11 +389,11 @@ class Prepared:
                                 max_blocks_per_seq=self.lay.block_tables.shape[1], max_context_len=spec.ctx_max,
                                 kv_format=spec.kv_format, softmax_scale=spec.scale, softcap=spec.softcap,
                                 window=spec.window, partition_size=spec.partition_size,
-                                split_threshold=spec.split_threshold)
+                                split_threshold=spec.split_threshold, query_len=spec.query_len)
         self.ws = torch.empty(da.decode_attn_workspace_bytes(self.p), dtype=torch.uint8, device="cuda")
         da.attach_workspace(self.p, self.ws)
         da.decode_attn_workspace_init(self.p)
-        self.out = torch.empty((spec.batch, spec.num_q_heads, spec.head_dim), dtype=torch.float32, device="cuda")
+        self.out = torch.empty(tuple(self.host["q"].shape), dtype=torch.float32, device="cuda")  # [B, (T,) Hq, D]
         self.stream = torch.cuda.current_stream()
         d = self.dev
         self.call = (d["q"], d["k"], d["v"], d["k_scales"], d["v_scales"], d["codebook"], d["sign"], d["bt"],
@@ -625,7 +625,7 @@ def main():
                    "num_kv_heads": spec.num_kv_heads, "head_dim": spec.head_dim, "kv_format": spec.kv_format,
                    "context": [spec.ctx_min, spec.ctx_max], "window": spec.window, "softcap": spec.softcap,
                    "block_size": spec.block_size, "partition_size": spec.partition_size,
-                   "algorithmic_kv_bytes": kv_bytes, "cache_bytes": cache_bytes,
+                   "query_len": spec.query_len, "algorithmic_kv_bytes": kv_bytes, "cache_bytes": cache_bytes,
                    "l2": "inputs larger than L2 (KV cache %.2f GB vs 129 MB L2), no flush" % (cache_bytes / 1e9)
                    if cache_bytes > L2_BYTES else "inputs smaller than L2", "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "kernel": kernel, "achieved": part_gbs, "peak": peak, "unit": "GB/s",

@@ -74,6 +74,10 @@ WORKLOADS = {
     # BF16 sequences of U[512, 8192] tokens, and 32 4-bit sequences of U[1, 32768] tokens
     "llama3_8b_bf16_b16": WorkloadSpec("llama3_8b_bf16_b16", 16, 32, 8, 128, "bf16", 512, 8192, seed=1008),
     "cb4_spread_32k": WorkloadSpec("cb4_spread_32k", 32, 32, 8, 128, "cb4", 1, 32768, seed=1009),
+    # multi-token decode (4 draft tokens per sequence) on the Llama-shaped batch: 16 (query
+    # token, head) pairs per kv head, two column groups
+    "llama3_8b_bf16_t4": WorkloadSpec("llama3_8b_bf16_t4", 64, 32, 8, 128, "bf16", 512, 8192, seed=1002,
+                                      query_len=4),
 }
 
 

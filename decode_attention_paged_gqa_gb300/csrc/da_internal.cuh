@@ -38,6 +38,7 @@ struct Args {
   int window, psize, thresh;
   int P;                      // partitions the grid and the workspace are sized for
   int ppc;                    // partitions a partition-kernel CTA walks (set by its launcher)
+  int g_shift;                // log2 of the group size G = Hq / Hkv (a power of two)
   int ncg;                    // column groups: CTAs per partition chunk, each taking 8 of the T * G
                               // (query token, head) pairs when there are more than 8 (else 1)
   int ksub;                   // partials per partition: sub-items a partition's pages are dealt to
@@ -87,17 +88,21 @@ struct Range {
   int start, end;  // [start, end) token positions; start >= end means "no such partition"
 };
 
-// Token range of partition p of a sequence of (already clamped) length L with T query
-// tokens; partitions are counted from the span start.
-__host__ __device__ __forceinline__ Range partition_range(int L, int T, int p, int window, int psize, int thresh) {
+// Token range of partition p of a sequence of (already clamped) length L with T query tokens
+// and np partitions (seq_partitions); partitions are counted from the span start.
+__host__ __device__ __forceinline__ Range partition_range_np(int L, int T, int p, int window, int psize, int np) {
   const int s = span_start(L, T, window);
-  const int np = num_partitions(L - s, psize, thresh);
   Range r{0, 0};
   if (p >= np) return r;
   if (np == 1) return Range{s, L};
   r.start = s + p * psize;
   r.end = r.start + psize < L ? r.start + psize : L;
   return r;
+}
+
+// The same with the partition count computed here.
+__host__ __device__ __forceinline__ Range partition_range(int L, int T, int p, int window, int psize, int thresh) {
+  return partition_range_np(L, T, p, window, psize, seq_partitions(L, T, window, psize, thresh));
 }
 
 // Largest length a context_lens entry may take.
@@ -128,9 +133,9 @@ __device__ __forceinline__ int load_block(const Args& a, int b, int page) {
 }
 
 // Row of out and of the partials ([B][T][Hq] flattened) for virtual head vh = (query token) * G +
-// (head within the group) of kv head g of sequence b.
+// (head within the group) of kv head g of sequence b (G = 2^g_shift).
 __host__ __device__ __forceinline__ size_t query_row(const Args& a, int b, int g, int G, int vh) {
-  return ((size_t)b * a.T + vh / G) * a.Hq + (size_t)g * G + vh % G;
+  return ((size_t)b * a.T + (vh >> a.g_shift)) * a.Hq + (size_t)g * G + (vh & (G - 1));
 }
 
 // Column groups of a partition kernel: one when the T * G pairs fit one 8-column MMA tile.

@@ -102,6 +102,8 @@ Args make_args(const void* q, const void* k, const void* v, const float* ks, con
   a.P = host_max_partitions(*p);
   a.ppc = 1;
   a.ncg = column_groups(a.T, a.Hq / a.Hkv);
+  a.g_shift = 0;
+  while ((1 << a.g_shift) < a.Hq / a.Hkv) ++a.g_shift;  // G is 1, 2, 4 or 8 (check_params)
   a.ksub = sub_items(*p);
   a.lut_stride = 128;
   a.alibi = p->alibi_slopes;

@@ -32,6 +32,52 @@ namespace da {
 // end: kRing must exceed kStages + 2 (kStages <= 6).
 constexpr int kRing = 16;
 
+// Per-CTA table of the batch's sequences in shared memory, built once at the kernel's start
+// when it fits: entry b holds (first item of sequence b, its clamped length), entry B holds
+// (item count, 0). A warp then finds the sequence of an item by a binary search in shared
+// memory instead of walking the context lengths in global memory one sequence at a time.
+struct SeqTable {
+  uint32_t addr;  // shared address of entry 0 (8 bytes per entry)
+  bool on;        // the table holds the whole batch
+};
+
+// Builds the table (all threads of the CTA; ends with a barrier). scratch: 32 words of shared memory.
+__device__ __forceinline__ void build_seq_table(const Args& a, const SeqTable& t, uint32_t scratch, int per_part,
+                                                int tid, int nthreads) {
+  const int B = a.B, chunk = (B + nthreads - 1) / nthreads;
+  const int c0 = min(tid * chunk, B), c1 = min(c0 + chunk, B);
+  int sum = 0;  // items of the thread's sequences [c0, c1)
+  for (int b = c0; b < c1; ++b) {
+    const int L = load_len(a, b, true);
+    sum += a.Hkv * seq_partitions(L, a.T, a.window, a.psize, a.thresh) * per_part;
+  }
+  // exclusive prefix over the threads: within the warp by shuffles, across warps in scratch
+  const int lane = tid & 31, wid = tid >> 5;
+  int incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) asm volatile("st.shared.b32 [%0], %1;" ::"r"(scratch + 4 * wid), "r"(incl) : "memory");
+  __syncthreads();
+  int before = 0;
+  for (int ww = 0; ww < wid; ++ww) {
+    int x;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(x) : "r"(scratch + 4 * ww) : "memory");
+    before += x;
+  }
+  int first = before + incl - sum;
+  for (int b = c0; b < c1; ++b) {
+    const int L = load_len(a, b, false);
+    asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(t.addr + 8 * b), "r"(first), "r"(L) : "memory");
+    first += a.Hkv * seq_partitions(L, a.T, a.window, a.psize, a.thresh) * per_part;
+  }
+  if (c1 == B && c0 < c1 || (B == 0 && tid == 0))
+    asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(t.addr + 8 * B), "r"(first), "r"(0) : "memory");
+  __syncthreads();
+}
+
 // The sequence that holds a given item; items are only ever looked up in increasing order.
 struct SeqCursor {
   int b;      // current sequence (-1 before the first)
@@ -44,7 +90,27 @@ struct SeqCursor {
     base = count = L = np = 0;
   }
   // Moves to the sequence that holds item i; false when i is past the last item.
-  __device__ __forceinline__ bool seek(const Args& a, int i, int per_part) {
+  __device__ __forceinline__ bool seek(const Args& a, const SeqTable& t, int i, int per_part) {
+    if (i - base < count) return true;
+    if (t.on) {  // binary search for the last sequence whose first item is <= i, among b+1 .. B-1
+      int lo = b + 1, hi = a.B;  // the answer lies in [lo, hi); hi = B: past the last item
+      uint32_t total;
+      asm volatile("ld.shared.b32 %0, [%1];" : "=r"(total) : "r"(t.addr + 8 * a.B) : "memory");
+      if (i >= (int)total) return false;
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        int f;
+        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(f) : "r"(t.addr + 8 * mid) : "memory");
+        if (f <= i) lo = mid; else hi = mid;
+      }
+      int nf;
+      asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(base), "=r"(L) : "r"(t.addr + 8 * lo) : "memory");
+      asm volatile("ld.shared.b32 %0, [%1];" : "=r"(nf) : "r"(t.addr + 8 * (lo + 1)) : "memory");
+      b = lo;
+      count = nf - base;
+      np = seq_partitions(L, a.T, a.window, a.psize, a.thresh);
+      return true;
+    }
     while (i - base >= count) {
       base += count;
       if (++b >= a.B) return false;
@@ -56,19 +122,20 @@ struct SeqCursor {
   }
 };
 
-// One item: sequence, kv head, partition, column group, sub-item, and the sequence's length.
+// One item: sequence, kv head, partition, column group, sub-item, the sequence's length and
+// partition count.
 struct Item {
-  int b, g, p, cg, sub, L;
+  int b, g, p, cg, sub, L, np;
 };
 
 // Descriptor of an item in the ring (16 bytes).
 __device__ __forceinline__ uint4 pack_item(const Item& it) {
   return make_uint4((uint32_t)it.b | ((uint32_t)it.g << 16), (uint32_t)it.p | ((uint32_t)it.cg << 16) |
-                    ((uint32_t)it.sub << 20), (uint32_t)it.L, 0u);
+                    ((uint32_t)it.sub << 20), (uint32_t)it.L, (uint32_t)it.np);
 }
 __device__ __forceinline__ Item unpack_item(const uint4& d) {
   return Item{(int)(d.x & 0xffffu), (int)(d.x >> 16), (int)(d.y & 0xffffu), (int)((d.y >> 16) & 15u),
-              (int)(d.y >> 20), (int)d.z};
+              (int)(d.y >> 20), (int)d.z, (int)d.w};
 }
 
 // Pages of an item for its warp: the partition's first page, the warp's page count there and
@@ -82,7 +149,7 @@ struct ItemPages {
 };
 __device__ __forceinline__ ItemPages item_pages(const Args& a, const Item& it) {
   ItemPages ip;
-  ip.r = partition_range(it.L, a.T, it.p, a.window, a.psize, a.thresh);
+  ip.r = partition_range_np(it.L, a.T, it.p, a.window, a.psize, it.np);
   int npages;
   range_pages(ip.r, ip.first, npages);
   ip.n = warp_pages(npages, it.sub, a.ksub);
@@ -111,7 +178,7 @@ struct ItemIssue {
     bid = kk < n ? load_block(a, b, pg0 + pstep * kk) : -1;
   }
   // Moves to the warp's next item that has pages for it and records it in the ring.
-  __device__ __forceinline__ void next_item(const Args& a, uint32_t ring, int lane) {
+  __device__ __forceinline__ void next_item(const Args& a, const SeqTable& t, uint32_t ring, int lane) {
     __syncwarp();  // the state lane 0 wrote last time is visible to the warp
     const uint32_t st = ring + kRing * 16;
     SeqCursor seq;
@@ -122,7 +189,7 @@ struct ItemIssue {
     const int per_part = a.ncg * a.ksub;
     seq.count = a.Hkv * seq.np * per_part;
     more = false;
-    for (int next = __shfl_sync(0xffffffffu, claimed, 0); seq.seek(a, next, per_part);
+    for (int next = __shfl_sync(0xffffffffu, claimed, 0); seq.seek(a, t, next, per_part);
          next = __shfl_sync(0xffffffffu, claimed, 0)) {
       if (lane == 0) claimed = (int)atomicAdd(a.claim, 1u);  // the item after this one
       Item it;
@@ -130,6 +197,7 @@ struct ItemIssue {
       const int per_head = seq.np * per_part;
       it.b = seq.b;
       it.L = seq.L;
+      it.np = seq.np;
       it.g = r / per_head;
       r -= it.g * per_head;
       it.p = r / per_part;
@@ -163,7 +231,7 @@ struct ItemIssue {
                    : "memory");
     }
   }
-  __device__ __forceinline__ void init(const Args& a, uint32_t ring, int lane) {
+  __device__ __forceinline__ void init(const Args& a, const SeqTable& t, uint32_t ring, int lane) {
     if (lane == 0) {  // no sequence yet; claim the first item
       asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(ring + kRing * 16), "r"(-1), "r"(0), "r"(0),
                    "r"(0)
@@ -171,14 +239,14 @@ struct ItemIssue {
       claimed = (int)atomicAdd(a.claim, 1u);
     }
     pushed = 0;
-    next_item(a, ring, lane);
+    next_item(a, t, ring, lane);
   }
   // Physical block (-1: bad block id, nothing to load) of the page at the cursor, the same in
   // every lane; advances the cursor. Requires `more`.
-  __device__ __forceinline__ int take(const Args& a, uint32_t ring, int lane) {
+  __device__ __forceinline__ int take(const Args& a, const SeqTable& t, uint32_t ring, int lane) {
     if (k > 0 && (k & 31) == 0) load_bids(a, lane);
     const int phys = __shfl_sync(0xffffffffu, bid, k & 31);
-    if (++k == n) next_item(a, ring, lane);
+    if (++k == n) next_item(a, t, ring, lane);
     return phys;
   }
 };

@@ -262,7 +262,7 @@ __device__ __forceinline__ Cols item_cols(const Args& a, const Item& it, const R
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
     c.vh[j] = vbase + (NV <= 4 ? tig % V : (2 * tig + j) % V);
-    c.pos[j] = it.L - a.T + c.vh[j] / G;
+    c.pos[j] = it.L - a.T + (c.vh[j] >> a.g_shift);
     c.lo[j] = max(window_start(c.pos[j], a.window), r.start);
     c.hi[j] = min(c.pos[j] + 1, r.end);
   }
@@ -300,6 +300,15 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 1)
     return;
   }
   const uint32_t code0 = blk, norm0 = blk + C::kOffNorms, ring = blk + C::kOffRing, bar0 = blk + C::kOffBars;
+  // the batch's sequence table, in the space after the last block of region B when it fits
+  SeqTable seqs;
+  {
+    const int in_b = kWarps - (in_a < kWarps ? in_a : kWarps);
+    const uint32_t scratch = tbl + C::kLutV + C::kLutK + in_b * C::kBlock;
+    seqs.addr = scratch + 128;
+    seqs.on = (long long)seqs.addr + 8ll * (a.B + 1) <= (long long)start + C::kSmem;
+    if (seqs.on) build_seq_table(a, seqs, scratch, a.ncg * a.ksub, tid, kThreads);
+  }
 
   if (lane == 0) {
     ptx::prefetch_tensor_map(&kmap);
@@ -319,7 +328,7 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 1)
 
   // ---- the warp's items and their pages, copied kStages pages ahead of the compute
   ItemIssue cur;
-  cur.init(a, ring, lane);
+  cur.init(a, seqs, ring, lane);
   unsigned issued = 0;  // stages issued
   int is = 0;           // stage of the next copies (issued % kNStages)
   auto issue_next = [&]() {  // all lanes; lane 0 issues the copies of the next kSlots pages
@@ -328,7 +337,7 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 1)
     for (int j = 0; j < C::kSlots; ++j)
       if (j == 0 || cur.more) {
         gk[j] = cur.g;
-        phys[j] = cur.take(a, ring, lane);
+        phys[j] = cur.take(a, seqs, ring, lane);
         n = j + 1;
       }
     const int s = is;
@@ -625,10 +634,10 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 1)
           if (alibi || tok0 < lo_all || tok0 + kPage > hi_all) {
             // the column's limits and position again, from the item's ring entry (rare pages)
             const Item it2 = ring_item(ring, popped - 1);
-            const Cols c = item_cols<NV>(a, it2, partition_range(it2.L, a.T, it2.p, a.window, a.psize, a.thresh),
+            const Cols c = item_cols<NV>(a, it2, partition_range_np(it2.L, a.T, it2.p, a.window, a.psize, it2.np),
                                          tig, G);
             if (alibi) {  // + slope * (t - pos) for token t
-              const float slope = __ldg(a.alibi + it2.g * G + c.vh[0] % G) * kLog2e;
+              const float slope = __ldg(a.alibi + it2.g * G + (c.vh[0] & (G - 1))) * kLog2e;
 #pragma unroll
               for (int e = 0; e < 2; ++e) sp[e] += slope * (float)(tok0 + gid + 8 * e - c.pos[0]);
             }
@@ -651,12 +660,12 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 1)
           }
           if (alibi || tok0 < lo_all || tok0 + kPage > hi_all) {
             const Item it2 = ring_item(ring, popped - 1);
-            const Cols c = item_cols<NV>(a, it2, partition_range(it2.L, a.T, it2.p, a.window, a.psize, a.thresh),
+            const Cols c = item_cols<NV>(a, it2, partition_range_np(it2.L, a.T, it2.p, a.window, a.psize, it2.np),
                                          tig, G);
             if (alibi) {  // + slope * (t - pos) for token t of each element
 #pragma unroll
               for (int e = 0; e < 4; ++e)
-                sc[e] += __ldg(a.alibi + it2.g * G + c.vh[e & 1] % G) * kLog2e *
+                sc[e] += __ldg(a.alibi + it2.g * G + (c.vh[e & 1] & (G - 1))) * kLog2e *
                          (float)(tok0 + gid + (e >> 1) * 8 - c.pos[e & 1]);
             }
             if (tok0 < lo_all || tok0 + kPage > hi_all) mask_page(sc, tok0, gid, c.lo, c.hi);

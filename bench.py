@@ -38,6 +38,11 @@ UNIT = "GB/s"
 DEFAULT_WORKLOAD = "llama3_8b_bf16"
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 2 ** 20
+# device-side hold ahead of a timed loop: SM cycles per second (the maximum SM clock, so the
+# hold lasts at least as long at lower clocks), margin over the host's enqueue time, minimum
+HOLD_CYCLES_PER_S = 2.07e9
+HOLD_MARGIN = 2.0
+HOLD_MIN_S = 0.5e-3
 
 
 def parse_args():
@@ -405,31 +410,50 @@ class Prepared:
 
         da.decode_attn_paged(*self.call, stream=self.stream)
 
-    def phased_step(self, ev):
-        """The same phases through their own entry points, with events around the partition
-        kernel (an event between two kernels stops the second from being scheduled during the
-        first's tail, so these steps time the dominant kernel, not the call)."""
+    def partition_only(self):
+        """The partition phase alone, through its own entry point (its inputs -- the rotated query
+        for codebook keys -- left in place by an earlier call)."""
         import decode_attention_paged_gqa_gb300 as da
 
-        da.decode_attn_rotate_q(*self.call, stream=self.stream)
-        ev[0].record(self.stream)
         da.decode_attn_partition(*self.call, stream=self.stream)
-        ev[1].record(self.stream)
-        da.decode_attn_reduce(*self.call, stream=self.stream)
 
     def device_error(self):
         import decode_attention_paged_gqa_gb300 as da
 
         return da.decode_attn_get_device_error(self.p)
 
-    def time_calls(self, K, world=1):
-        """Device time of K back-to-back calls (CUDA events on the launching stream, barrier and
-        synchronize on both sides); ms per call, maxed over ranks."""
+    def host_seconds(self, fn, n=8):
+        """Host time to enqueue one fn() (the device is not waited for)."""
         import torch
 
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(n):
+            fn()
+        t1 = time.perf_counter()
+        torch.cuda.synchronize()
+        return (t1 - t0) / n
+
+    def hold(self, seconds):
+        """Queues a device-side busy wait of at least `seconds` on the stream. The timed launches
+        are enqueued behind it, so the device runs them back to back and the events around them
+        time the device's work, not the host's launch rate (which, for calls of a few tens of
+        microseconds through the Python binding, can be the slower of the two)."""
+        import torch
+
+        with torch.cuda.stream(self.stream):
+            torch.cuda._sleep(int(seconds * HOLD_CYCLES_PER_S))
+
+    def time_calls(self, K, world=1):
+        """Device time of K back-to-back calls (CUDA events on the launching stream, barrier and
+        synchronize on both sides, the calls queued behind a hold); ms per call, maxed over ranks."""
+        import torch
+
+        host_s = self.host_seconds(self.step)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         barrier(world)
         torch.cuda.synchronize()
+        self.hold(HOLD_MARGIN * K * host_s + HOLD_MIN_S)
         a.record(self.stream)
         for _ in range(K):
             self.step()
@@ -439,14 +463,24 @@ class Prepared:
         return max_over_ranks(a.elapsed_time(b) / K, world)
 
     def time_partition(self, K):
-        """Mean device time of the partition kernel over K phased calls (ms)."""
+        """Device time per launch of the partition kernel (ms): K launches back to back between two
+        events on the launching stream, queued behind a hold, after one full call that leaves the
+        phase's inputs in place. Each launch is scheduled during the previous one's last CTAs and
+        waits in-kernel for it to finish, as in a stream of calls, so the launch latency that an
+        event pair around a single launch would add is not counted."""
         import torch
 
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-        for k in range(K):
-            self.phased_step(evs[k])
+        self.step()
+        host_s = self.host_seconds(self.partition_only)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
-        return statistics.mean(a.elapsed_time(b) for a, b in evs)
+        self.hold(HOLD_MARGIN * K * host_s + HOLD_MIN_S)
+        a.record(self.stream)
+        for _ in range(K):
+            self.partition_only()
+        b.record(self.stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / K
 
 
 def soak(prep, seconds):
@@ -627,7 +661,9 @@ def main():
                    "block_size": spec.block_size, "partition_size": spec.partition_size,
                    "query_len": spec.query_len, "algorithmic_kv_bytes": kv_bytes, "cache_bytes": cache_bytes,
                    "l2": "inputs larger than L2 (KV cache %.2f GB vs 129 MB L2), no flush" % (cache_bytes / 1e9)
-                   if cache_bytes > L2_BYTES else "inputs smaller than L2", "parallelism": f"replicas x{world}"},
+                   if cache_bytes > L2_BYTES else "inputs smaller than L2",
+                   "timing": "CUDA events on the launching stream around K calls queued behind a device-side hold",
+                   "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "kernel": kernel, "achieved": part_gbs, "peak": peak, "unit": "GB/s",
                      "frac": part_gbs / peak, "peak_source": peak_src, "traffic": traffic,
                      "partition_us": part_ms * 1000, "bytes_per_launch": kv_bytes},

@@ -113,18 +113,24 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 3 : 2)
                         const __grid_constant__ CUtensorMap vmap) {
   using T = Tc<FMT, D, NV>;
   constexpr int DP = T::kDP;
-  const int g = blockIdx.y, b = blockIdx.z;
+  // grid: x runs over (column group, kv head, sequence), y over the chunks of ppc partitions,
+  // so that CTAs are scheduled partition-major: every sequence's first chunk before any
+  // sequence's second. The chunks scheduled last are the high partitions of the longest
+  // sequences, among them their partial last partitions, which shortens the tail of a batch
+  // that fills only a few waves.
+  const int cg = blockIdx.x % a.ncg, bg = blockIdx.x / a.ncg;
+  const int g = bg % a.Hkv, b = bg / a.Hkv;
   // the warp index through a shuffle from lane 0, which the compiler then treats as uniform
   const int tid = threadIdx.x, lane = tid & 31, w = __shfl_sync(kFull, tid >> 5, 0);
   const int gid = lane >> 2, tig = lane & 3;
   // the CTA's columns: virtual heads (query token, head of the group) vbase .. vbase + V - 1
-  const int G = a.Hq / a.Hkv, vbase = 8 * (blockIdx.x % a.ncg), V = min(NV, a.T * G - vbase);
+  const int G = a.Hq / a.Hkv, vbase = 8 * cg, V = min(NV, a.T * G - vbase);
   ptx::grid_dependency_wait();   // what the kernel before this one writes (q, the rotated q, ...)
   ptx::grid_dependents_launch();  // the reduce may be scheduled once every CTA has started
-  const int L = load_len(a, b, blockIdx.x == 0 && g == 0 && tid == 0);
+  const int L = load_len(a, b, blockIdx.y == 0 && cg == 0 && g == 0 && tid == 0);
   const int np = seq_partitions(L, a.T, a.window, a.psize, a.thresh);
   // this CTA's partitions of (b, g)
-  const int p_begin = (blockIdx.x / a.ncg) * a.ppc, p_end = min(p_begin + a.ppc, np);
+  const int p_begin = blockIdx.y * a.ppc, p_end = min(p_begin + a.ppc, np);
   if (p_begin >= p_end) return;
 
   extern __shared__ unsigned char smem_raw[];
@@ -591,7 +597,7 @@ cudaError_t launch_fixed(const Args& a, cudaStream_t s) {
   if (b.owner) b.ppc = kWarps * ((b.ppc + kWarps - 1) / kWarps);
   // scheduled during the previous kernel's last CTAs (the query rotation, for codebook keys);
   // waits in-kernel before its first read
-  return launch_pdl(kern, dim3((a.P + b.ppc - 1) / b.ppc * a.ncg, a.Hkv, a.B), dim3(kThreads), T::kSmem, s, b, km, vm);
+  return launch_pdl(kern, dim3(a.ncg * a.Hkv * a.B, (a.P + b.ppc - 1) / b.ppc), dim3(kThreads), T::kSmem, s, b, km, vm);
 }
 
 template <int FMT, int D, bool CAP>

@@ -67,7 +67,11 @@ struct Tc {
   static constexpr int kKS = D / 16;                        // k-steps of S^T
   static constexpr int kStageSmem = kWarps * kStages * kStageBytes;
   static constexpr int kDP = D + 4;  // padded row of the merge buffer
-  static constexpr int kMergeSmem = (kWarps * NV * kDP + 2 * kWarps * 8) * 4;
+  // the epilogue stages at most 4 columns at a time (two passes at NV = 8), which keeps the
+  // 8-column kernel within the shared memory of three CTAs per SM
+  static constexpr int kEpCols = NV < 4 ? NV : 4;
+  static constexpr int kEpPasses = NV / kEpCols;
+  static constexpr int kMergeSmem = (kWarps * kEpCols * kDP + 2 * kWarps * 8) * 4;
   static constexpr int kSmem = kStageSmem + kMergeSmem + 1024;
 };
 
@@ -247,8 +251,8 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 3 : 2)
 #pragma unroll
     for (int j = 0; j < 2; ++j) slope_c[j] = __ldg(a.alibi + g * G + (vbase + ((2 * tig + j) % NV) % V) % G) * kLog2e;
   }
-  float* ep_o = reinterpret_cast<float*>(smem_gen + T::kStageSmem);  // [kWarps][NV][DP]
-  float* ep_m = ep_o + kWarps * NV * DP;                              // [kWarps][8]
+  float* ep_o = reinterpret_cast<float*>(smem_gen + T::kStageSmem);  // [kWarps][kEpCols][DP]
+  float* ep_m = ep_o + kWarps * T::kEpCols * DP;                      // [kWarps][8]
   float* ep_l = ep_m + kWarps * 8;                                    // [kWarps][8]
   const float out_scale = FMT == DA_KV_FP8_E4M3 ? __ldg(a.v_scales) : 1.0f;
   const int mi = lane >> 3, ri = lane & 7;  // ldmatrix: matrix index and row of this lane's address
@@ -417,22 +421,7 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 3 : 2)
   if (owner) {
     // the warp's (o, m, l) is the partition's result: O^T (hi and lo columns added; divided
     // by l for an unsplit sequence) through the warp's staging buffer, then 16-byte stores
-    float* ep_w = ep_o + w * NV * DP;
-#pragma unroll
-    for (int mt = 0; mt < T::kMT; ++mt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        float v = o[0][mt][e];
-        if constexpr (NV == 8) v += o[T::kNT - 1][mt][e];
-        if constexpr (NV == 4) v += __shfl_xor_sync(kFull, v, 2);  // columns c, c + 4
-        if constexpr (NV == 2) v += __shfl_xor_sync(kFull, v, 1);  // columns c, c + 2
-        if constexpr (NV == 1) v += (e & 1) ? 0.0f : o[0][mt][e + 1];  // columns 0, 1
-        const int col = 2 * tig + (e & 1);
-        const float l = l_run[e & 1];
-        if (direct) v = l > 0.0f ? v * out_scale / l : 0.0f;
-        const int rowd = FMT == DA_KV_BF16 ? 16 * mt + gid + ((e >> 1) ? 8 : 0) : 16 * mt + 2 * gid + (e >> 1);
-        if (col < V) ep_w[col * DP + rowd] = v;
-      }
+    float* ep_w = ep_o + w * T::kEpCols * DP;
     if (!direct && gid == 0) {
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
@@ -444,37 +433,44 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 3 : 2)
         }
       }
     }
-    __syncwarp();
-    for (int idx = lane; idx < V * D / 4; idx += 32) {
-      const int v = idx / (D / 4), d = 4 * (idx % (D / 4));
-      const size_t bh = query_row(a, b, g, G, vbase + v);
-      const float4 x = *reinterpret_cast<const float4*>(ep_w + v * DP + d);
-      if (direct) {  // the caller's output is only 4-byte aligned
-        float* dst = a.out + bh * D + d;
-        dst[0] = x.x, dst[1] = x.y, dst[2] = x.z, dst[3] = x.w;
-      } else {
-        *reinterpret_cast<float4*>(a.part_o + (bh * a.P + p) * D + d) = x;
+#pragma unroll
+    for (int pass = 0; pass < T::kEpPasses; ++pass) {
+      const int c0 = pass * T::kEpCols;  // the pass's columns: c0 .. c0 + kEpCols - 1
+#pragma unroll
+      for (int mt = 0; mt < T::kMT; ++mt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          float v = o[0][mt][e];
+          if constexpr (NV == 8) v += o[T::kNT - 1][mt][e];
+          if constexpr (NV == 4) v += __shfl_xor_sync(kFull, v, 2);  // columns c, c + 4
+          if constexpr (NV == 2) v += __shfl_xor_sync(kFull, v, 1);  // columns c, c + 2
+          if constexpr (NV == 1) v += (e & 1) ? 0.0f : o[0][mt][e + 1];  // columns 0, 1
+          const int col = 2 * tig + (e & 1);
+          const float l = l_run[e & 1];
+          if (direct) v = l > 0.0f ? v * out_scale / l : 0.0f;
+          const int rowd = FMT == DA_KV_BF16 ? 16 * mt + gid + ((e >> 1) ? 8 : 0) : 16 * mt + 2 * gid + (e >> 1);
+          if (col >= c0 && col < c0 + T::kEpCols && col < V) ep_w[(col - c0) * DP + rowd] = v;
+        }
+      __syncwarp();
+      const int Vp = min(T::kEpCols, V - c0);
+      for (int idx = lane; idx < Vp * D / 4; idx += 32) {
+        const int v = idx / (D / 4), d = 4 * (idx % (D / 4));
+        const size_t bh = query_row(a, b, g, G, vbase + c0 + v);
+        const float4 x = *reinterpret_cast<const float4*>(ep_w + v * DP + d);
+        if (direct) {  // the caller's output is only 4-byte aligned
+          float* dst = a.out + bh * D + d;
+          dst[0] = x.x, dst[1] = x.y, dst[2] = x.z, dst[3] = x.w;
+        } else {
+          *reinterpret_cast<float4*>(a.part_o + (bh * a.P + p) * D + d) = x;
+        }
       }
+      __syncwarp();  // the staging buffer is rewritten by the next pass or partition
     }
-    __syncwarp();  // the staging buffer is rewritten by the warp's next partition
     continue;
   }
   // shared partition: each warp's (o, m, l) per virtual head into shared memory (hi and lo
   // columns added), then the warps merged into the partial (split sequence) or the
-  // normalised output (unsplit)
-#pragma unroll
-  for (int mt = 0; mt < T::kMT; ++mt)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      float v = o[0][mt][e];
-      if constexpr (NV == 8) v += o[T::kNT - 1][mt][e];
-      if constexpr (NV == 4) v += __shfl_xor_sync(kFull, v, 2);  // columns c, c + 4
-      if constexpr (NV == 2) v += __shfl_xor_sync(kFull, v, 1);  // columns c, c + 2
-      if constexpr (NV == 1) v += (e & 1) ? 0.0f : o[0][mt][e + 1];  // columns 0, 1
-      const int col = 2 * tig + (e & 1);
-      const int rowd = FMT == DA_KV_BF16 ? 16 * mt + gid + ((e >> 1) ? 8 : 0) : 16 * mt + 2 * gid + (e >> 1);
-      if (col < V) ep_o[(w * NV + col) * DP + rowd] = v;
-    }
+  // normalised output (unsplit), kEpCols columns per pass
   if (gid == 0) {
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
@@ -482,33 +478,51 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 3 : 2)
       ep_l[w * 8 + 2 * tig + j] = l_run[j];
     }
   }
-  __syncthreads();
-  for (int idx = tid; idx < V * D; idx += kThreads) {
-    const int v = idx / D, d = idx % D;
-    float M = -INFINITY;
 #pragma unroll
-    for (int ww = 0; ww < kWarps; ++ww) M = fmaxf(M, ep_m[ww * 8 + v]);
-    float acc = 0.0f, l = 0.0f;
+  for (int pass = 0; pass < T::kEpPasses; ++pass) {
+    const int c0 = pass * T::kEpCols;
 #pragma unroll
-    for (int ww = 0; ww < kWarps; ++ww) {
-      const float mw = ep_m[ww * 8 + v];
-      const float wt = mw == -INFINITY ? 0.0f : exp2f(mw - M);
-      acc += wt * ep_o[(ww * NV + v) * DP + d];
-      l += wt * ep_l[ww * 8 + v];
-    }
-    const size_t bh = query_row(a, b, g, G, vbase + v);
-    if (direct) {
-      a.out[bh * D + d] = l > 0.0f ? acc * out_scale / l : 0.0f;
-    } else {
-      const size_t pi = bh * a.P + p;
-      a.part_o[pi * D + d] = acc;
-      if (d == 0) {
-        a.part_m[pi] = M;
-        a.part_l[pi] = l;
+    for (int mt = 0; mt < T::kMT; ++mt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float v = o[0][mt][e];
+        if constexpr (NV == 8) v += o[T::kNT - 1][mt][e];
+        if constexpr (NV == 4) v += __shfl_xor_sync(kFull, v, 2);  // columns c, c + 4
+        if constexpr (NV == 2) v += __shfl_xor_sync(kFull, v, 1);  // columns c, c + 2
+        if constexpr (NV == 1) v += (e & 1) ? 0.0f : o[0][mt][e + 1];  // columns 0, 1
+        const int col = 2 * tig + (e & 1);
+        const int rowd = FMT == DA_KV_BF16 ? 16 * mt + gid + ((e >> 1) ? 8 : 0) : 16 * mt + 2 * gid + (e >> 1);
+        if (col >= c0 && col < c0 + T::kEpCols && col < V) ep_o[(w * T::kEpCols + col - c0) * DP + rowd] = v;
+      }
+    __syncthreads();
+    const int Vp = min(T::kEpCols, V - c0);
+    for (int idx = tid; idx < Vp * D; idx += kThreads) {
+      const int vp = idx / D, d = idx % D, v = c0 + vp;
+      float M = -INFINITY;
+#pragma unroll
+      for (int ww = 0; ww < kWarps; ++ww) M = fmaxf(M, ep_m[ww * 8 + v]);
+      float acc = 0.0f, l = 0.0f;
+#pragma unroll
+      for (int ww = 0; ww < kWarps; ++ww) {
+        const float mw = ep_m[ww * 8 + v];
+        const float wt = mw == -INFINITY ? 0.0f : exp2f(mw - M);
+        acc += wt * ep_o[(ww * T::kEpCols + vp) * DP + d];
+        l += wt * ep_l[ww * 8 + v];
+      }
+      const size_t bh = query_row(a, b, g, G, vbase + v);
+      if (direct) {
+        a.out[bh * D + d] = l > 0.0f ? acc * out_scale / l : 0.0f;
+      } else {
+        const size_t pi = bh * a.P + p;
+        a.part_o[pi * D + d] = acc;
+        if (d == 0) {
+          a.part_m[pi] = M;
+          a.part_l[pi] = l;
+        }
       }
     }
+    __syncthreads();  // the merge buffer is rewritten by the next pass or partition
   }
-  __syncthreads();  // the merge buffer is rewritten by the next partition
   }  // partitions
 
   if (stalled) {

@@ -160,6 +160,31 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
   return v;
 }
 __device__ __forceinline__ float ldsf(uint32_t addr) { return __uint_as_float(lds32(addr)); }
+// The same at a constant byte offset from addr (the offset is the instruction's immediate).
+template <int OFF>
+__device__ __forceinline__ uint4 lds128_at(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4+%5];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr), "n"(OFF));
+  return v;
+}
+template <int OFF>
+__device__ __forceinline__ uint2 lds64_at(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.b32 {%0, %1}, [%2+%3];" : "=r"(v.x), "=r"(v.y) : "r"(addr), "n"(OFF));
+  return v;
+}
+template <int OFF>
+__device__ __forceinline__ uint32_t lds32_at(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1+%2];" : "=r"(v) : "r"(addr), "n"(OFF));
+  return v;
+}
+template <int OFF>
+__device__ __forceinline__ float ldsf_at(uint32_t addr) {
+  return __uint_as_float(lds32_at<OFF>(addr));
+}
 // A load from the lookup tables, which no thread writes after the CTA's first barrier: not
 // volatile, so the compiler may interleave the lookups with the work around them.
 __device__ __forceinline__ uint32_t lds32_table(uint32_t addr) {
@@ -417,6 +442,19 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 1)
   const int PK = a.P * a.ksub;  // partial slots per output row
   const int mi = lane >> 3, ri = lane & 7;  // ldmatrix (FP8 keys): matrix index and row of this lane's address
   unsigned consumed = 0, stall_from = 0, popped = 0;  // pages computed; stage of a stall
+  // the page in registers: this lane's byte offsets within a code slot and a norm slot (the
+  // rest of each load's address is an immediate). 4-bit keys at D = 128 (64-byte rows, 64-byte
+  // swizzle: chunk c of row r at c ^ ((r >> 1) & 3)): row gid, chunk tig, and row gid + 8 at
+  // +512, whose swizzle is the same. Values at D = 128: rows 2 tig + {0, 1, 8, 9} at + {0, 64,
+  // 512, 576}, all with the swizzle term (row >> 1) & 3 = tig, the 8 bytes at 8 (gid & 1) of
+  // chunk (gid >> 1) ^ tig. 3-bit keys: the row's 3D/32 bytes at (3D/32) tig, row gid + 8 at
+  // + 8 kKRow. Norms: tokens gid and gid + 8 (+ 32) of each vector.
+  const uint32_t lane_k = KS == kSideCB4 ? koff + gid * 64 + ((tig ^ ((gid >> 1) & 3)) << 4)
+                                         : gid * C::kKRow + (3 * D / 32) * tig;
+  const uint32_t lane_v = voff + 2 * tig * 64 + (((gid >> 1) ^ tig) << 4) + 8 * (gid & 1);
+  const uint32_t lane_kn = knoff + 4 * gid, lane_vn = vnoff + 4 * gid;
+  int cpage = 0;      // slot of the next page to compute among the warp's kStages (consumed % kStages)
+  uint32_t cph = 0;   // the mbarrier phase parity of its stage
   bool stalled = false;  // a copy never arrived: no more waits, copies or compute
   int q_b = -1, q_g = -1, q_cg = -1;  // (sequence, kv head, column group) of the loaded query fragments
   uint32_t qf[C::kKS][2], ql[kPaired ? 1 : C::kKS][2];
@@ -534,16 +572,28 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 1)
     float v_unit = 1.0f;  // 2^(127 - ev_run)
 
     for (int i = 0; i < n_pages; ++i, ++consumed) {
-      // page `consumed` of the warp's stream: slot `slot` of stage use `use`
-      const unsigned use = consumed / C::kSlots, slot = consumed % C::kSlots;
-      const int s = use % C::kNStages;
-      if (slot == 0 && !ptx::mbar_wait(bar0 + 8 * s, (use / C::kNStages) & 1)) {
+      // page `consumed` of the warp's stream: slot `slot` of stage s, whose mbarrier phase has
+      // parity `parity`, page slot pg = s * kSlots + slot of the warp's block; at D = 128 from
+      // counters kept alongside (cheaper than dividing), at D = 256 from `consumed` (the
+      // 8-column kernels there have no registers to spare)
+      const unsigned use = consumed / C::kSlots;
+      const int slot = D == 128 ? cpage % C::kSlots : (int)(consumed % C::kSlots);
+      const int s = D == 128 ? cpage / C::kSlots : (int)(use % C::kNStages);
+      const int pg = D == 128 ? cpage : s * C::kSlots + slot;
+      const uint32_t parity = D == 128 ? cph : (use / C::kNStages) & 1;
+      if constexpr (D == 128) {
+        if (++cpage == C::kStages) {
+          cpage = 0;
+          cph ^= 1u;
+        }
+      }
+      if (slot == 0 && !ptx::mbar_wait(bar0 + 8 * s, parity)) {
         stalled = true;
-        stall_from = use;
+        stall_from = consumed / C::kSlots;
         break;
       }
-      const uint32_t cb0 = code0 + (s * C::kSlots + slot) * C::kCodeBytes, kb = cb0 + koff, vb = cb0 + voff;
-      const uint32_t nb = norm0 + (s * C::kSlots + slot) * C::kNormBytes;
+      const uint32_t cb0 = code0 + pg * C::kCodeBytes, kb = cb0 + koff, vb = cb0 + voff;
+      const uint32_t nb = norm0 + pg * C::kNormBytes;
       const int tok0 = tk0 + i * tkstep;
 
       // -- the page into registers: key bytes (codebook keys), value bytes, norms
@@ -551,9 +601,7 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 1)
       uint32_t k0[kWords + 1], k1[kWords + 1];
       k0[kWords] = k1[kWords] = 0u;
       if constexpr (KS == kSideCB4 && D == 128) {
-        // 64-byte rows, 64-byte swizzle: 16-byte chunk c of row r at c ^ ((r >> 1) & 3)
-        const uint32_t ch = (tig ^ ((gid >> 1) & 3)) << 4;  // the same for rows gid and gid + 8
-        const uint4 x0 = lds128(kb + gid * 64 + ch), x1 = lds128(kb + (gid + 8) * 64 + ch);
+        const uint4 x0 = lds128_at<0>(cb0 + lane_k), x1 = lds128_at<512>(cb0 + lane_k);
         k0[0] = x0.x, k0[1] = x0.y, k0[2] = x0.z, k0[3] = x0.w;
         k1[0] = x1.x, k1[1] = x1.y, k1[2] = x1.z, k1[3] = x1.w;
       } else if constexpr (KS == kSideCB4) {  // D = 256, 128-byte swizzle: chunks 2 tig, 2 tig + 1
@@ -566,32 +614,50 @@ __global__ void __launch_bounds__(Cb<KS, D, NV>::kThreads, 1)
           k1[4 * c] = x1.x, k1[4 * c + 1] = x1.y, k1[4 * c + 2] = x1.z, k1[4 * c + 3] = x1.w;
         }
       } else if constexpr (KS == kSideCB3) {  // 12 (D = 128) or 24 (D = 256) bytes per row at (3D/32) tig
+        if constexpr (D == 128) {
+          const uint32_t kl = kb + lane_k;
+          k0[0] = lds32_at<0>(kl), k0[1] = lds32_at<4>(kl), k0[2] = lds32_at<8>(kl);
+          k1[0] = lds32_at<8 * C::kKRow>(kl), k1[1] = lds32_at<8 * C::kKRow + 4>(kl);
+          k1[2] = lds32_at<8 * C::kKRow + 8>(kl);
+        } else {
 #pragma unroll
-        for (int c = 0; c < kWords; ++c) {
-          k0[c] = lds32(kb + gid * C::kKRow + (3 * D / 32) * tig + 4 * c);
-          k1[c] = lds32(kb + (gid + 8) * C::kKRow + (3 * D / 32) * tig + 4 * c);
+          for (int c = 0; c < kWords; ++c) {
+            k0[c] = lds32(kb + gid * C::kKRow + (3 * D / 32) * tig + 4 * c);
+            k1[c] = lds32(kb + (gid + 8) * C::kKRow + (3 * D / 32) * tig + 4 * c);
+          }
         }
       }
       // the thread's value bytes of tokens 2 tig, 2 tig + 1, 2 tig + 8, 2 tig + 9, D/16 bytes
       // each at byte (D/16) gid
       uint32_t vw[4][D / 64];
+      if constexpr (D == 128) {  // 64-byte rows, 64-byte swizzle
+        const uint32_t vl = cb0 + lane_v;
+        const uint2 x0 = lds64_at<0>(vl), x1 = lds64_at<64>(vl), x2 = lds64_at<512>(vl), x3 = lds64_at<576>(vl);
+        vw[0][0] = x0.x, vw[0][1] = x0.y, vw[1][0] = x1.x, vw[1][1] = x1.y;
+        vw[2][0] = x2.x, vw[2][1] = x2.y, vw[3][0] = x3.x, vw[3][1] = x3.y;
+      } else {
 #pragma unroll
-      for (int i4 = 0; i4 < 4; ++i4) {
-        const int row = 2 * tig + (i4 & 1) + 8 * (i4 >> 1);
-        if constexpr (D == 128) {  // 64-byte rows, 64-byte swizzle
-          const uint2 x = lds64(vb + row * 64 + ((((gid >> 1) ^ ((row >> 1) & 3))) << 4) + 8 * (gid & 1));
-          vw[i4][0] = x.x, vw[i4][1] = x.y;
-        } else {  // 128-byte rows, 128-byte swizzle
+        for (int i4 = 0; i4 < 4; ++i4) {  // 128-byte rows, 128-byte swizzle
+          const int row = 2 * tig + (i4 & 1) + 8 * (i4 >> 1);
           const uint4 x = lds128(vb + row * 128 + ((gid ^ (row & 7)) << 4));
           vw[i4][0] = x.x, vw[i4][1] = x.y, vw[i4][2] = x.z, vw[i4][3] = x.w;
         }
       }
       float kn0 = 1.0f, kn1 = 1.0f;
-      if constexpr (C::kKNorms) {
-        kn0 = ldsf(nb + knoff + 4 * gid);
-        kn1 = ldsf(nb + knoff + 4 * (gid + 8));
+      float vn0, vn1;
+      if constexpr (D == 128) {
+        if constexpr (C::kKNorms) {
+          kn0 = ldsf_at<0>(nb + lane_kn);
+          kn1 = ldsf_at<32>(nb + lane_kn);
+        }
+        vn0 = ldsf_at<0>(nb + lane_vn), vn1 = ldsf_at<32>(nb + lane_vn);
+      } else {  // (the 8-column kernels at D = 256 have no registers to spare for the offsets)
+        if constexpr (C::kKNorms) {
+          kn0 = ldsf(nb + knoff + 4 * gid);
+          kn1 = ldsf(nb + knoff + 4 * (gid + 8));
+        }
+        vn0 = ldsf(nb + vnoff + 4 * gid), vn1 = ldsf(nb + vnoff + 4 * (gid + 8));
       }
-      const float vn0 = ldsf(nb + vnoff + 4 * gid), vn1 = ldsf(nb + vnoff + 4 * (gid + 8));
       // FP8 keys are read with ldmatrix during the MMAs below, so their stage is refilled after
       if constexpr (KS != kSideFP8) {
         if (slot == C::kSlots - 1) {  // the stage's last page is in registers

@@ -247,6 +247,14 @@ inline int partitions_per_cta(const Args& a, int per_sm, int* cached_sms) {
   return waves < 1 ? 1 : (waves > 8 ? 8 : (int)waves);
 }
 
+// CTAs of a kernel with `per_sm` resident CTAs per SM that the device holds at once (0 when
+// the SM count is not known; partitions_per_cta caches it).
+inline long long resident_slots(int per_sm, const int* cached_sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || cached_sms[dev] <= 0) return 0;
+  return (long long)cached_sms[dev] * (per_sm > 0 ? per_sm : 1);
+}
+
 // Whether a partition kernel's warps own whole partitions: as requested, else when the
 // batch has at least `min_fill_x2` / 2 partitions (counted at the longest possible span) for
 // every warp the GPU holds at once. Below that, sharing each partition among a CTA's warps

@@ -110,6 +110,98 @@ __device__ __forceinline__ void mma(float (&d)[4], const uint32_t (&a)[4], uint3
     ptx::mma_f16(d, a, b0, b1);
 }
 
+// A CTA's work: kv head g, column group cg of sequence b (L tokens, np partitions), its
+// partitions [p_begin, p_end) (none when p_end <= p_begin).
+struct CtaWork {
+  int b, g, cg, L, np, p_begin, p_end;
+};
+
+// The launcher's fixed grid: x over (column group, kv head, sequence), y over chunks of ppc
+// partitions, so that CTAs are scheduled partition-major (every sequence's first chunk
+// before any sequence's second).
+__device__ __forceinline__ CtaWork fixed_work(const Args& a, int tid) {
+  CtaWork c;
+  c.cg = blockIdx.x % a.ncg;
+  const int bg = blockIdx.x / a.ncg;
+  c.g = bg % a.Hkv, c.b = bg / a.Hkv;
+  c.L = load_len(a, c.b, blockIdx.y == 0 && c.cg == 0 && c.g == 0 && tid == 0);
+  c.np = seq_partitions(c.L, a.T, a.window, a.psize, a.thresh);
+  c.p_begin = blockIdx.y * a.ppc, c.p_end = min(c.p_begin + a.ppc, c.np);
+  return c;
+}
+
+// Small batches (a.ppc == 0): a grid of one CTA per resident slot, all running at once. In each
+// CTA warp 0 reads every context length and takes the smallest chunk size k <= 8 for which the
+// batch's CTAs -- each sequence's partitions cut into chunks of k, times kv heads and column
+// groups -- fit the grid (the launcher makes sure k = 8 does; the search starts from the bound
+// that the total partition count gives), then the CTA of index blockIdx.x in (sequence, chunk,
+// kv head, column group) order; CTAs past the count have no work. One wave of CTAs, each
+// walking its chunk's partitions with one pipeline, avoids both the start-up gap of every
+// further wave and a tail of whole partitions scheduled last.
+constexpr int kMaxChunk = 8;
+constexpr int kSpreadSeqs = 4;  // sequences per lane of warp 0: batches of up to 128
+__device__ __forceinline__ CtaWork spread_work(const Args& a, int tid) {
+  __shared__ int s_pick[4];  // sequence (-1: no work), CTA index within it, its length, chunk size
+  if (tid < 32) {
+    const int lane = tid;
+    int lv[kSpreadSeqs], npv[kSpreadSeqs], total = 0;  // sequences b = lane + 32 i
+#pragma unroll
+    for (int i = 0; i < kSpreadSeqs; ++i) {
+      const int bb = lane + 32 * i;
+      lv[i] = bb < a.B ? load_len(a, bb, blockIdx.x == 0) : 0;
+      npv[i] = seq_partitions(lv[i], a.T, a.window, a.psize, a.thresh);
+      total += npv[i];
+    }
+    total = __reduce_add_sync(kFull, total);
+    const int per_chunk = a.Hkv * a.ncg;         // CTAs per chunk of partitions
+    const int fit = (int)gridDim.x / per_chunk;  // chunks the grid holds
+    // the smallest chunk size whose chunk count fits, from the bound total / fit up
+    int ppc = fit > 0 ? max(1, min((total + fit - 1) / fit, kMaxChunk)) : kMaxChunk;
+    for (;; ++ppc) {
+      int cnt = 0;
+#pragma unroll
+      for (int i = 0; i < kSpreadSeqs; ++i) cnt += (npv[i] + ppc - 1) / ppc;
+      cnt = __reduce_add_sync(kFull, cnt);
+      if (cnt <= fit || ppc == kMaxChunk) break;
+    }
+    // CTA j's sequence: an exclusive scan of the sequences' CTA counts in sequence order
+    // (over the lanes for i = 0, then i = 1, ...)
+    const int j = blockIdx.x;
+    int base = 0, pick = -1, r = 0, L = 0;
+#pragma unroll
+    for (int i = 0; i < kSpreadSeqs; ++i) {
+      if (32 * i >= a.B) break;
+      const int n = (npv[i] + ppc - 1) / ppc * per_chunk;
+      int incl = n;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const int first = base + incl - n;
+      if (j >= first && j < first + n) pick = lane + 32 * i, r = j - first, L = lv[i];
+      base += __shfl_sync(kFull, incl, 31);
+    }
+    const unsigned holder = __ballot_sync(kFull, pick >= 0);
+    if (holder == 0 && lane == 0) s_pick[0] = -1;
+    if (pick >= 0) s_pick[0] = pick, s_pick[1] = r, s_pick[2] = L, s_pick[3] = ppc;
+  }
+  __syncthreads();
+  CtaWork c;
+  c.b = s_pick[0];
+  if (c.b < 0) {  // past the batch's CTAs
+    c.b = c.g = c.cg = c.L = c.np = c.p_begin = c.p_end = 0;
+    return c;
+  }
+  const int rr = s_pick[1], ppc = s_pick[3];
+  c.cg = rr % a.ncg;
+  c.g = (rr / a.ncg) % a.Hkv;
+  c.L = s_pick[2];
+  c.np = seq_partitions(c.L, a.T, a.window, a.psize, a.thresh);
+  c.p_begin = rr / (a.Hkv * a.ncg) * ppc, c.p_end = min(c.p_begin + ppc, c.np);
+  return c;
+}
+
 // CAP: softcap on (a separate instantiation, so the plain kernel carries no tanh)
 template <int FMT, int D, int NV, bool CAP>
 __global__ void __launch_bounds__(kThreads, D == 128 ? 3 : 2)
@@ -117,25 +209,16 @@ __global__ void __launch_bounds__(kThreads, D == 128 ? 3 : 2)
                         const __grid_constant__ CUtensorMap vmap) {
   using T = Tc<FMT, D, NV>;
   constexpr int DP = T::kDP;
-  // grid: x runs over (column group, kv head, sequence), y over the chunks of ppc partitions,
-  // so that CTAs are scheduled partition-major: every sequence's first chunk before any
-  // sequence's second. The chunks scheduled last are the high partitions of the longest
-  // sequences, among them their partial last partitions, which shortens the tail of a batch
-  // that fills only a few waves.
-  const int cg = blockIdx.x % a.ncg, bg = blockIdx.x / a.ncg;
-  const int g = bg % a.Hkv, b = bg / a.Hkv;
   // the warp index through a shuffle from lane 0, which the compiler then treats as uniform
   const int tid = threadIdx.x, lane = tid & 31, w = __shfl_sync(kFull, tid >> 5, 0);
   const int gid = lane >> 2, tig = lane & 3;
-  // the CTA's columns: virtual heads (query token, head of the group) vbase .. vbase + V - 1
-  const int G = a.Hq / a.Hkv, vbase = 8 * cg, V = min(NV, a.T * G - vbase);
   ptx::grid_dependency_wait();   // what the kernel before this one writes (q, the rotated q, ...)
   ptx::grid_dependents_launch();  // the reduce may be scheduled once every CTA has started
-  const int L = load_len(a, b, blockIdx.y == 0 && cg == 0 && g == 0 && tid == 0);
-  const int np = seq_partitions(L, a.T, a.window, a.psize, a.thresh);
-  // this CTA's partitions of (b, g)
-  const int p_begin = blockIdx.y * a.ppc, p_end = min(p_begin + a.ppc, np);
-  if (p_begin >= p_end) return;
+  const CtaWork cw = a.ppc > 0 ? fixed_work(a, tid) : spread_work(a, tid);
+  if (cw.p_begin >= cw.p_end) return;
+  const int b = cw.b, g = cw.g, L = cw.L, np = cw.np, p_begin = cw.p_begin, p_end = cw.p_end;
+  // the CTA's columns: virtual heads (query token, head of the group) vbase .. vbase + V - 1
+  const int G = a.Hq / a.Hkv, vbase = 8 * cw.cg, V = min(NV, a.T * G - vbase);
 
   extern __shared__ unsigned char smem_raw[];
   __shared__ __align__(8) uint64_t bars[kWarps * T::kStages];
@@ -611,6 +694,17 @@ cudaError_t launch_fixed(const Args& a, cudaStream_t s) {
   if (b.owner) b.ppc = kWarps * ((b.ppc + kWarps - 1) / kWarps);
   // scheduled during the previous kernel's last CTAs (the query rotation, for codebook keys);
   // waits in-kernel before its first read
+  // a small batch of at least two waves of single partitions (at the longest possible span):
+  // one wave of CTAs, the chunk size chosen in-kernel from the lengths (below two waves the
+  // fixed grid is as good and saves the choice's start-up time)
+  const long long slots = resident_slots(per_sm, sms);
+  const long long units = (long long)a.P * a.Hkv * a.B * a.ncg;
+  if (!b.owner && a.ppc_req == 0 && a.schedule == 0 && slots > 0 && units >= 2 * slots &&
+      a.B <= 32 * kSpreadSeqs &&
+      (long long)a.B * a.Hkv * a.ncg * ((a.P + kMaxChunk - 1) / kMaxChunk) <= slots) {
+    b.ppc = 0;
+    return launch_pdl(kern, dim3((unsigned)slots), dim3(kThreads), T::kSmem, s, b, km, vm);
+  }
   return launch_pdl(kern, dim3(a.ncg * a.Hkv * a.B, (a.P + b.ppc - 1) / b.ppc), dim3(kThreads), T::kSmem, s, b, km, vm);
 }
 

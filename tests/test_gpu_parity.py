@@ -251,6 +251,27 @@ def test_spread_context_lengths(fmt):
 
 
 @pytest.mark.parametrize("fmt", ["bf16", "fp8"])
+@pytest.mark.parametrize("B,T,window", [(16, 1, 0), (16, 2, 0), (48, 1, 2048)])
+def test_small_batch_one_wave(fmt, B, T, window):
+    """Small batches of spread lengths (1 to 8192 tokens) whose partitions, at the longest
+    possible span, fill at least two waves of the tensor-core kernel's CTAs but few enough
+    that every sequence's partitions fit one wave in chunks of at most 8: the kernel then runs
+    one wave and picks the chunk size from the lengths in-kernel. Each partition's partial does
+    not depend on how partitions are chunked, so the output must equal, bit for bit, that of
+    the fixed grid of one partition per CTA; and it must match the oracle."""
+    rng = np.random.default_rng(1000 + B + T)
+    lens = [int(x) for x in rng.integers(1, 8193, size=B)]
+    lens[:6] = [1, 512, 513, 1024, 1025, 8192]
+    spec = wl.WorkloadSpec(f"wave_{fmt}", B, 32, 8, 128, fmt, 0, 8192, seed=77 + B, window=window, query_len=T)
+    c = make_case(spec, wl.make_layout(spec, lens=lens))
+    dev = to_device(c)
+    auto = run_gpu(c, dev)
+    fixed = run_gpu(c, dev, partition_schedule=1, partitions_per_cta=1)
+    np.testing.assert_array_equal(auto, fixed)
+    assert_close(auto, run_oracle(c), f"{fmt} B={B} T={T} window={window} one wave")
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "fp8"])
 @pytest.mark.parametrize("qscale", [1e-3, 3e2, 1e5])
 def test_query_magnitudes(fmt, qscale):
     """The FP8 path computes q.k with f16 operands: queries far outside the f16 range must

@@ -116,17 +116,16 @@ struct CtaWork {
   int b, g, cg, L, np, p_begin, p_end;
 };
 
-// The launcher's fixed grid: x over (column group, kv head, sequence), y over chunks of ppc
-// partitions, so that CTAs are scheduled partition-major (every sequence's first chunk
-// before any sequence's second).
+// The launcher's fixed grid: x over (chunk of ppc partitions, column group), y over kv heads,
+// z over sequences, so that the chunks of one (sequence, kv head) are neighbours in the
+// schedule: a page two chunks share (a window start inside a page) is read while in L2.
 __device__ __forceinline__ CtaWork fixed_work(const Args& a, int tid) {
   CtaWork c;
   c.cg = blockIdx.x % a.ncg;
-  const int bg = blockIdx.x / a.ncg;
-  c.g = bg % a.Hkv, c.b = bg / a.Hkv;
-  c.L = load_len(a, c.b, blockIdx.y == 0 && c.cg == 0 && c.g == 0 && tid == 0);
+  c.g = blockIdx.y, c.b = blockIdx.z;
+  c.L = load_len(a, c.b, blockIdx.x == 0 && c.g == 0 && tid == 0);
   c.np = seq_partitions(c.L, a.T, a.window, a.psize, a.thresh);
-  c.p_begin = blockIdx.y * a.ppc, c.p_end = min(c.p_begin + a.ppc, c.np);
+  c.p_begin = (blockIdx.x / a.ncg) * a.ppc, c.p_end = min(c.p_begin + a.ppc, c.np);
   return c;
 }
 
@@ -705,7 +704,7 @@ cudaError_t launch_fixed(const Args& a, cudaStream_t s) {
     b.ppc = 0;
     return launch_pdl(kern, dim3((unsigned)slots), dim3(kThreads), T::kSmem, s, b, km, vm);
   }
-  return launch_pdl(kern, dim3(a.ncg * a.Hkv * a.B, (a.P + b.ppc - 1) / b.ppc), dim3(kThreads), T::kSmem, s, b, km, vm);
+  return launch_pdl(kern, dim3((a.P + b.ppc - 1) / b.ppc * a.ncg, a.Hkv, a.B), dim3(kThreads), T::kSmem, s, b, km, vm);
 }
 
 template <int FMT, int D, bool CAP>

@@ -3,7 +3,9 @@
 //
 // A CTA of four warps takes `ppc` consecutive partitions of one (sequence, kv head). Either
 // the warps share each partition (pages dealt round-robin, the warps' results merged at the
-// partition's end) or each warp owns whole partitions; the launcher chooses per call. Every
+// partition's end) or each warp owns whole partitions; the launcher chooses per call. A small
+// batch runs as one wave of CTAs (one per resident slot) that choose `ppc` themselves from the
+// context lengths (spread_work). Every
 // warp runs its own pipeline of kStages shared-memory stages, each holding one page (16
 // tokens) of K and of V for the kv head, loaded by TMA (cp.async.bulk.tensor, 128-byte
 // swizzle) and signalled on an mbarrier, continuing across partition boundaries. Per page a

@@ -47,6 +47,23 @@ __global__ void __launch_bounds__(kThreads) reduce_kernel(const Args a) {
   __shared__ float4 red_o[kGroups][kCols];
   __shared__ float red_m[kThreads / 32], red_s[kThreads / 32];
   __shared__ float x_s[kUnrotate ? D : 1];
+  const int PK = a.P * a.ksub;  // partial slots per row
+  const size_t base = ((size_t)row * a.Hq + h) * PK;
+  // The thread's first partials (max and sum of slot tid; kPre float4 columns of its group's
+  // first slots), loaded together with the context length, before the row's partition count
+  // is known: every row has PK slots, and a slot is used below only if it holds a partial of
+  // this row. The three dependent rounds (length, then maxima and sums, then outputs) become
+  // one for a row of up to kPre * kGroups partials.
+  constexpr int kPre = 4;
+  const int col = tid % kCols, group = tid / kCols;
+  const float4* src = reinterpret_cast<const float4*>(a.part_o + base * D) + col;
+  const float m_pre = tid < PK ? a.part_m[base + tid] : -INFINITY, l_pre = tid < PK ? a.part_l[base + tid] : 0.0f;
+  float4 o_pre[kPre];
+#pragma unroll
+  for (int i = 0; i < kPre; ++i) {
+    const int j = group + i * kGroups;
+    o_pre[i] = j < PK ? src[(size_t)j * kCols] : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  }
   const int L = load_len(a, b, false);
   const int np = seq_partitions(L, a.T, a.window, a.psize, a.thresh);
   float* out = a.out + ((size_t)row * a.Hq + h) * D;
@@ -55,8 +72,7 @@ __global__ void __launch_bounds__(kThreads) reduce_kernel(const Args a) {
     return;
   }
   if (np == 1 && a.ksub == 1 && !kUnrotate) return;
-  const int PK = a.P * a.ksub, nk = np * a.ksub;  // partial slots per row; those of this row
-  const size_t base = ((size_t)row * a.Hq + h) * PK;
+  const int nk = np * a.ksub;  // partial slots of this row
 
   // M = max_p m_p and s = sum_p 2^(m_p - M) l_p, each thread folding its partials
   // j = tid, tid + kThreads, ... (m_p and l_p loaded together), then across the block
@@ -67,7 +83,8 @@ __global__ void __launch_bounds__(kThreads) reduce_kernel(const Args a) {
       const Range r = partition_range(L, a.T, j / a.ksub, a.window, a.psize, a.thresh);
       valid = j % a.ksub < (r.end - 1) / kBlockSize - r.start / kBlockSize + 1;
     }
-    const float m = valid ? a.part_m[base + j] : -INFINITY, l = valid ? a.part_l[base + j] : 0.0f;
+    float m = j == tid ? m_pre : a.part_m[base + j], l = j == tid ? l_pre : a.part_l[base + j];
+    if (!valid) m = -INFINITY, l = 0.0f;
     w_s[j] = m;
     fold(M, s, m, l);
   }
@@ -89,12 +106,21 @@ __global__ void __launch_bounds__(kThreads) reduce_kernel(const Args a) {
   __syncthreads();
 
   // sum_p w_p o_p: thread (group, column) takes float4 column `col` of partitions
-  // group, group + kGroups, ...; the groups are then added up
-  const int col = tid % kCols, group = tid / kCols;
-  const float4* src = reinterpret_cast<const float4*>(a.part_o + base * D) + col;
+  // group, group + kGroups, ... (the first kPre of them loaded above); the groups are then
+  // added up
   float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll
+  for (int i = 0; i < kPre; ++i) {
+    const int j = group + i * kGroups;
+    const float wp = j < nk ? w_s[j] : 0.0f;
+    if (wp == 0.0f) continue;  // an empty partial, a slot never written, or past the row's partials
+    acc.x = fmaf(wp, o_pre[i].x, acc.x);
+    acc.y = fmaf(wp, o_pre[i].y, acc.y);
+    acc.z = fmaf(wp, o_pre[i].z, acc.z);
+    acc.w = fmaf(wp, o_pre[i].w, acc.w);
+  }
 #pragma unroll 8
-  for (int j = group; j < nk; j += kGroups) {
+  for (int j = group + kPre * kGroups; j < nk; j += kGroups) {
     const float wp = w_s[j];
     if (wp == 0.0f) continue;  // an empty partial, or a sub-item slot that was never written
     const float4 o = src[(size_t)j * kCols];

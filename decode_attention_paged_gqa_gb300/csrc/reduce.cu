@@ -8,9 +8,10 @@
 // When the partition kernel dealt each partition's pages to ksub sub-items, every sub-item
 // that had pages wrote a partial of its own, and all of them are combined the same way
 // (sub-item s of partition p has pages when s < the partition's page count).
-// One CTA per (row, head); the partials' loads are issued together: m_p and l_p in one round,
-// the float4 columns of o_p in one or two more, with the partitions spread over thread groups
-// (128 threads: 4 groups at D = 128, 2 at D = 256; 256 threads, for 32 or more partitions: 8 / 4).
+// One CTA per (row, head); the partials' loads are issued together, with the partitions spread
+// over thread groups (128 threads: 4 groups at D = 128, 2 at D = 256; 256 threads, for 32 or
+// more partitions: 8 / 4): each thread's first m_p, l_p and float4 columns of o_p go out with
+// the context length, the rest of m_p and l_p in one round and of o_p in one more.
 // An empty sequence (or a query token that attends nothing) gets an all-zero row. An
 // unsplit sequence of a format without a codebook value side was written by the partition
 // kernel and is skipped here. When the values are stored on the rotated basis the result

@@ -37,3 +37,26 @@ def test_gpu_arm_refuses_without_gpu():
     assert r.returncode != 0
     assert "needs a CUDA GPU" in (r.stdout + r.stderr)
     assert not [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+
+
+def test_traffic_records_are_hash_locked(monkeypatch):
+    """The DRAM traffic a bench line reports comes from profiles/traffic.json, and only while
+    the kernel's sources hash to the profiled build: every record names an existing profile
+    summary that carries its hash, and a changed source hash turns the figure off."""
+    sys.path.insert(0, ROOT)
+    import bench
+
+    with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+        entries = json.load(f)["entries"]
+    assert entries
+    for e in entries:
+        assert e["kernel"] in bench.PARTITION_SOURCES
+        summary = os.path.join(ROOT, e["from"].split(" ")[0])
+        assert os.path.exists(summary), e["from"]
+        with open(summary) as f:
+            assert e["source_hash"] in f.read(), summary
+        assert e["dram_bytes_per_launch"] == e["dram_read_bytes"] + e["dram_write_bytes"]
+        monkeypatch.setattr(bench, "source_hash", lambda kernel, h=e["source_hash"]: h)
+        assert bench.recorded_traffic(e["kernel"], e["workload"]) == e["dram_bytes_per_launch"]
+        monkeypatch.setattr(bench, "source_hash", lambda kernel: "0" * 16)
+        assert bench.recorded_traffic(e["kernel"], e["workload"]) is None
